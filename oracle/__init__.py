@@ -1,0 +1,191 @@
+"""CPU oracle for the fused SwiGLU projection Y = SiLU(A x W1) (.) (A x W2).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  The product path never
+does, and this package never imports the product.  The arithmetic lives in
+``swiglu_oracle.c`` (plain C, double precision); this module builds it with gcc
+and wraps it with ctypes over numpy arrays.
+
+Source of the method: page "Riepilogo Tecnico: Sovrapposizione delle
+Attivazioni a Livello di Tile per l'Inferenza Efficiente di LLM" (gist.science
+paper 2607.02521), section "Definizione del Problema" (the formula) and section
+"Metodologia", item 2 (the interleaved W_fused layout and the pair step).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swiglu_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile swiglu_oracle.c into liboracle.so (gcc, OpenMP over rows)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        d = ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = d
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f64.restype = d
+        lib.oracle_silu.argtypes = [d]
+        lib.oracle_silu.restype = d
+        lib.oracle_swiglu_bf16.argtypes = [p, p, p, i64, i64, i64, p, i64, p, p, p]
+        lib.oracle_swiglu_bf16.restype = ctypes.c_int
+        lib.oracle_swiglu_e4m3.argtypes = [p, p, p, d, d, d, i64, i64, i64, p, i64, p, p, p]
+        lib.oracle_swiglu_e4m3.restype = ctypes.c_int
+        lib.oracle_pack_interleaved_u16.argtypes = [p, p, p, i64, i64]
+        lib.oracle_pack_interleaved_u16.restype = None
+        lib.oracle_pack_interleaved_u8.argtypes = [p, p, p, i64, i64]
+        lib.oracle_pack_interleaved_u8.restype = None
+        lib.oracle_swiglu_interleaved_bf16.argtypes = [p, p, i64, i64, i64, p, i64, p]
+        lib.oracle_swiglu_interleaved_bf16.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _u16(x) -> np.ndarray:
+    """Raw BF16 bit patterns as a C-contiguous uint16 array."""
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected BF16 bit patterns as uint16, got {a.dtype}")
+    return a
+
+
+def _u8(x) -> np.ndarray:
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected E4M3 codes as uint8, got {a.dtype}")
+    return a
+
+
+def _rows(rows, M):
+    if rows is None:
+        return None, M
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return r, int(r.size)
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().oracle_bf16_to_f64(int(bits))
+
+
+def e4m3_to_f64(code: int) -> float:
+    return _load().oracle_e4m3_to_f64(int(code))
+
+
+def silu(x: float) -> float:
+    return _load().oracle_silu(float(x))
+
+
+def swiglu_bf16(A, W1, W2, rows=None, with_gate_up: bool = False):
+    """Y[r, :] = SiLU(A[m_r] W1) * (A[m_r] W2) in double for BF16 inputs.
+
+    A [M,K], W1/W2 [K,N] are uint16 arrays of BF16 bit patterns (row-major).
+    ``rows`` selects rows of A (default: all).  Returns Y [nrows, N] float64,
+    or (G, U, Y) when ``with_gate_up``.
+    """
+    A, W1, W2 = _u16(A), _u16(W1), _u16(W2)
+    M, K = A.shape
+    K2, N = W1.shape
+    if K2 != K or W2.shape != (K, N):
+        raise ValueError("shape mismatch")
+    r, nr = _rows(rows, M)
+    Y = np.empty((nr, N), dtype=np.float64)
+    G = np.empty_like(Y) if with_gate_up else None
+    U = np.empty_like(Y) if with_gate_up else None
+    rc = _load().oracle_swiglu_bf16(
+        _ptr(A), _ptr(W1), _ptr(W2), M, N, K,
+        _ptr(r) if r is not None else None, nr,
+        _ptr(G) if G is not None else None, _ptr(U) if U is not None else None, _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_bf16 failed (bad row index or out of memory)")
+    return (G, U, Y) if with_gate_up else Y
+
+
+def swiglu_e4m3(Aq, W1q, W2q, sA: float, sW1: float, sW2: float, rows=None,
+                with_gate_up: bool = False):
+    """The definition on dequantised FP8 E4M3 operands (value = code * scale)."""
+    Aq, W1q, W2q = _u8(Aq), _u8(W1q), _u8(W2q)
+    M, K = Aq.shape
+    K2, N = W1q.shape
+    if K2 != K or W2q.shape != (K, N):
+        raise ValueError("shape mismatch")
+    r, nr = _rows(rows, M)
+    Y = np.empty((nr, N), dtype=np.float64)
+    G = np.empty_like(Y) if with_gate_up else None
+    U = np.empty_like(Y) if with_gate_up else None
+    rc = _load().oracle_swiglu_e4m3(
+        _ptr(Aq), _ptr(W1q), _ptr(W2q), float(sA), float(sW1), float(sW2), M, N, K,
+        _ptr(r) if r is not None else None, nr,
+        _ptr(G) if G is not None else None, _ptr(U) if U is not None else None, _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_e4m3 failed")
+    return (G, U, Y) if with_gate_up else Y
+
+
+def pack_interleaved(W1, W2) -> np.ndarray:
+    """W_fused[k, 2n] = W1[k, n], W_fused[k, 2n+1] = W2[k, n] (uint16 or uint8 codes)."""
+    W1 = np.ascontiguousarray(W1)
+    W2 = np.ascontiguousarray(W2)
+    if W1.shape != W2.shape or W1.dtype != W2.dtype:
+        raise ValueError("W1 and W2 must match in shape and dtype")
+    K, N = W1.shape
+    Wf = np.empty((K, 2 * N), dtype=W1.dtype)
+    if W1.dtype == np.uint16:
+        _load().oracle_pack_interleaved_u16(_ptr(W1), _ptr(W2), _ptr(Wf), K, N)
+    elif W1.dtype == np.uint8:
+        _load().oracle_pack_interleaved_u8(_ptr(W1), _ptr(W2), _ptr(Wf), K, N)
+    else:
+        raise TypeError("expected uint16 (BF16) or uint8 (FP8) codes")
+    return Wf
+
+
+def swiglu_interleaved_bf16(A, Wf, rows=None) -> np.ndarray:
+    """D = A x W_fused, then Y[m,n] = SiLU(D[m,2n]) * D[m,2n+1], in double."""
+    A, Wf = _u16(A), _u16(Wf)
+    M, K = A.shape
+    K2, N2 = Wf.shape
+    if K2 != K or N2 % 2:
+        raise ValueError("shape mismatch")
+    N = N2 // 2
+    r, nr = _rows(rows, M)
+    Y = np.empty((nr, N), dtype=np.float64)
+    rc = _load().oracle_swiglu_interleaved_bf16(
+        _ptr(A), _ptr(Wf), M, N, K, _ptr(r) if r is not None else None, nr, _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_interleaved_bf16 failed")
+    return Y
+
+
+from .check import parity_report, assert_parity  # noqa: E402,F401

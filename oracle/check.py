@@ -1,0 +1,74 @@
+"""Acceptance criterion for a computed Y against the oracle's double-precision Y.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The pages judge a fused kernel by the share of elements whose relative error
+against a higher-precision reference exceeds 1 % (page "Riepilogo Tecnico ...
+Inferenza Efficiente di LLM", section "Contributi Chiave", item 3: the fused
+kernels show 0 % such elements).  The bar applied here makes that concrete so
+that it is meaningful near zero, where a relative error is undefined:
+
+  (1) every element: |y - ref| <= 1e-2 * |ref| + 1e-3 * max|ref|;
+  (2) no element with |ref| > 1e-2 * rms(ref) has |y - ref| / |ref| > 1e-2.
+
+Non-finite values anywhere in y fail (1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+REL = 1e-2           # 1 % relative, the pages' mismatch threshold
+ABS_OF_MAX = 1e-3    # absolute floor as a fraction of max|ref|
+SIG_OF_RMS = 1e-2    # "significant" elements: |ref| above this fraction of rms(ref)
+
+
+def parity_report(y, ref) -> dict:
+    """Compare y (any float array) with ref (float64) element by element."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if y.shape != ref.shape:
+        raise ValueError(f"shape mismatch {y.shape} vs {ref.shape}")
+    n = ref.size
+    if n == 0:
+        return {"n": 0, "ok": True, "n_over_bound": 0, "n_rel_mismatch_sig": 0,
+                "mismatch_pct_all": 0.0, "max_abs_err": 0.0, "max_ref": 0.0,
+                "rms_ref": 0.0, "max_rel_err_sig": 0.0}
+    absref = np.abs(ref)
+    max_ref = float(absref.max())
+    rms_ref = float(np.sqrt(np.mean(ref * ref)))
+    finite = np.isfinite(y)
+    err = np.where(finite, np.abs(y - ref), np.inf)
+    bound = REL * absref + ABS_OF_MAX * max_ref
+    over = err > bound
+    sig = absref > SIG_OF_RMS * rms_ref
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rel = np.where(absref > 0, err / absref, np.where(err > 0, np.inf, 0.0))
+    rel_sig = rel[sig]
+    n_rel_sig = int(np.count_nonzero(rel_sig > REL))
+    nonzero = absref > 0
+    mismatch_all = float(np.count_nonzero(rel[nonzero] > REL)) / max(1, int(nonzero.sum()))
+    rep = {
+        "n": int(n),
+        "n_over_bound": int(np.count_nonzero(over)),
+        "n_rel_mismatch_sig": n_rel_sig,
+        "n_significant": int(sig.sum()),
+        "mismatch_pct_all": 100.0 * mismatch_all,
+        "max_abs_err": float(err.max()),
+        "max_ref": max_ref,
+        "rms_ref": rms_ref,
+        "max_rel_err_sig": float(rel_sig.max()) if rel_sig.size else 0.0,
+    }
+    rep["ok"] = rep["n_over_bound"] == 0 and n_rel_sig == 0
+    if not rep["ok"]:
+        idx = np.unravel_index(int(np.argmax(np.where(over, err - bound, -np.inf))), ref.shape)
+        rep["worst_index"] = [int(i) for i in idx]
+        rep["worst_y"] = float(y[idx])
+        rep["worst_ref"] = float(ref[idx])
+    return rep
+
+
+def assert_parity(y, ref, what: str = "") -> dict:
+    rep = parity_report(y, ref)
+    if not rep["ok"]:
+        raise AssertionError(f"parity failed {what}: {rep}")
+    return rep

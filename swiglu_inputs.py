@@ -1,0 +1,98 @@
+"""Seeded synthetic inputs for the fused SwiGLU projection.
+
+This module is the one piece shared by the CUDA path's tests and benchmark and
+by the oracle's checks.  It draws random numbers and converts them to the
+storage types; it holds none of the method's arithmetic.
+
+Recipe (the pages name Qwen-2.5 MLP shapes but print no data):
+  * a CPU ``torch.Generator`` seeded with ``seed``;
+  * W1 = randn(K, N) / sqrt(K), then W2 the same way, then A = randn(M, K),
+    all drawn in fp32 in that order and rounded to BF16 (round to nearest even)
+    so that, for one seed, the weights are identical across an M sweep;
+  * FP8 E4M3 operands: the same fp32 draws, a per-tensor scale
+    s = amax(|X|) / 448 (448 is the largest finite E4M3 value), and codes
+    q = E4M3(X / s) with round-to-nearest-even and saturation (torch's
+    ``float8_e4m3fn`` cast); the operand's value is q * s.
+
+Shapes used by the tests and the benchmark (Qwen-2.5 MLP projections):
+  0.5B: K=896,  N=4864;  7B: K=3584, N=18944;  72B: K=8192, N=29568.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+E4M3_MAX = 448.0
+
+QWEN_SHAPES = {
+    "qwen2.5-0.5b": (896, 4864),
+    "qwen2.5-7b": (3584, 18944),
+    "qwen2.5-72b": (8192, 29568),
+}
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def draw_fp32(M: int, N: int, K: int, seed: int):
+    """fp32 draws in the fixed order W1, W2, A."""
+    g = _gen(seed)
+    s = 1.0 / math.sqrt(K) if K > 0 else 1.0
+    W1 = torch.randn(K, N, generator=g, dtype=torch.float32) * s
+    W2 = torch.randn(K, N, generator=g, dtype=torch.float32) * s
+    A = torch.randn(M, K, generator=g, dtype=torch.float32)
+    return A, W1, W2
+
+
+def make_bf16(M: int, N: int, K: int, seed: int):
+    """A[M,K], W1[K,N], W2[K,N] as contiguous CPU bfloat16 tensors."""
+    A, W1, W2 = draw_fp32(M, N, K, seed)
+    return (A.to(torch.bfloat16).contiguous(), W1.to(torch.bfloat16).contiguous(),
+            W2.to(torch.bfloat16).contiguous())
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor amax scale and saturating RNE E4M3 codes: returns (q, s)."""
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    s = amax / E4M3_MAX if amax > 0 else 1.0
+    q = (x / s).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).contiguous()
+    return q, s
+
+
+def make_e4m3(M: int, N: int, K: int, seed: int):
+    """(Aq, W1q, W2q) float8_e4m3fn CPU tensors and their scales (sA, sW1, sW2)."""
+    A, W1, W2 = draw_fp32(M, N, K, seed)
+    Aq, sA = quantize_e4m3(A)
+    W1q, sW1 = quantize_e4m3(W1)
+    W2q, sW2 = quantize_e4m3(W2)
+    return (Aq, W1q, W2q), (sA, sW1, sW2)
+
+
+def bits_u16(t: torch.Tensor):
+    """Raw 16-bit patterns of a bfloat16 tensor as a numpy uint16 array."""
+    return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def bits_u8(t: torch.Tensor):
+    """Raw 8-bit codes of a float8 tensor as a numpy uint8 array."""
+    return t.contiguous().view(torch.uint8).numpy()
+
+
+def sample_rows(M: int, tile_m: int, n_random: int, seed: int):
+    """Row indices for checking a large M on a sample: the first and last row
+    of every ``tile_m``-row block, the last row, plus ``n_random`` seeded
+    random rows; sorted and unique."""
+    import numpy as np
+    rows = set()
+    for b in range(0, M, tile_m):
+        rows.add(b)
+        rows.add(min(M - 1, b + tile_m - 1))
+    rows.add(M - 1)
+    rng = np.random.default_rng(seed)
+    if n_random > 0 and M > 0:
+        rows.update(int(r) for r in rng.integers(0, M, size=n_random))
+    return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
