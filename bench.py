@@ -1,0 +1,592 @@
+#!/usr/bin/env python
+"""Benchmark of the fused SwiGLU projection on GB300.
+
+One step = the whole hot path over the Qwen-2.5-0.5B MLP workload
+(K=896, N=4864, M in {128, 512, 2048, 8192}), each M in both weight forms
+(separate W1/W2 and interleaved W_fused): eight fused-kernel launches.
+Metric: TFLOP/s = sum(4*M*N*K) / time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is device time of K back-to-back
+replays of a CUDA graph of the step, inputs resident in HBM; each call reads
+its own copy of the weights and its own A and writes its own Y, so every
+step touches ~390 MB (3x the 129 MB L2) and no call finds its inputs in L2.
+``e2e`` repeats the step through the public Python API with A copied in
+from pinned host memory and Y copied back every step.  ``--impl reference``
+times the CPU oracle (the deliberately slow reference arm) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Fused SwiGLU-GEMM TFLOP/s (4·M·N·K/t) and % of GB300 BF16 roofline"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+
+WORKLOADS = {
+    # name: (K, N, Ms, seed)
+    "qwen2.5-0.5b": (896, 4864, (128, 512, 2048, 8192), 1),
+    "qwen2.5-0.5b-m64": (896, 4864, (64,), 0),
+    "qwen2.5-7b": (3584, 18944, (256, 1024, 2048, 4096), 2),
+    "qwen2.5-72b": (8192, 29568, (2048, 8192, 16384), 3),
+}
+DEFAULT_WORKLOAD = "qwen2.5-0.5b"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "swiglu_gemm_transformer_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel_key: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when it is
+    absent or was taken on different kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    ent = d.get(kernel_key)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception as e:  # no nvidia-smi: report what we have
+            log(f"clock sampling unavailable: {e}")
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        smax = max(r[1] for r in rows)
+        pmax = max(r[2] for r in rows)
+        # samples "under load": power above half the run's maximum
+        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": pmax}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Workload:
+    """Device-resident inputs and the list of fused calls of one step."""
+
+    def __init__(self, name, dev, variant=0, forms=("separate", "interleaved")):
+        import torch
+        import swiglu_gemm_transformer_gb300 as sg
+        import swiglu_inputs as si
+        self.sg = sg
+        self.name = name
+        K, N, Ms, seed = WORKLOADS[name]
+        self.K, self.N, self.Ms, self.seed = K, N, Ms, seed
+        self.dev = dev
+        self.calls = []      # (form, M, variant_resolved, fn)
+        self.bytes_touched = 0
+        self.flops = 0
+        lib = sg.lib()
+        host = {}
+        for M in Ms:
+            A, W1, W2 = si.make_bf16(M, N, K, seed)
+            host[M] = (A, W1, W2)
+        self.host = host
+        self.buffers = []
+        for form in forms:
+            for M in Ms:
+                A, W1, W2 = host[M]
+                Ad = A.to(dev)
+                Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                if form == "separate":
+                    W1d, W2d = W1.to(dev), W2.to(dev)
+                    v = variant or lib.swiglu_select_variant(M, N, K, 0)
+                    ptrs = (Ad.data_ptr(), W1d.data_ptr(), W2d.data_ptr(), Y.data_ptr())
+                    fn = (lambda p=ptrs, M=M, v=v: self._sep(p, M, v))
+                    self.buffers.append((Ad, W1d, W2d, Y))
+                    wbytes = 2 * K * N * 2
+                else:
+                    W1d, W2d = W1.to(dev), W2.to(dev)
+                    Wf = sg.swiglu_pack_interleaved(W1d, W2d)
+                    del W1d, W2d
+                    v = variant or lib.swiglu_select_variant(M, N, K, 1)
+                    ptrs = (Ad.data_ptr(), Wf.data_ptr(), Y.data_ptr())
+                    fn = (lambda p=ptrs, M=M, v=v: self._inter(p, M, v))
+                    self.buffers.append((Ad, Wf, Y))
+                    wbytes = 2 * K * N * 2
+                self.calls.append((form, M, v, fn))
+                self.bytes_touched += M * K * 2 + wbytes + M * N * 2
+                self.flops += 4 * M * N * K
+        torch.cuda.synchronize(dev)
+
+    def _stream(self):
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+
+    def _sep(self, p, M, v):
+        rc = self.sg.lib().swiglu_fused_ex(p[0], p[1], p[2], p[3], M, self.N, self.K, v, self._stream())
+        if rc:
+            raise self.sg.SwigluError("swiglu_fused_ex", rc)
+
+    def _inter(self, p, M, v):
+        rc = self.sg.lib().swiglu_fused_interleaved_ex(p[0], p[1], p[2], M, self.N, self.K, v, self._stream())
+        if rc:
+            raise self.sg.SwigluError("swiglu_fused_interleaved_ex", rc)
+
+    def step(self):
+        for _, _, _, fn in self.calls:
+            fn()
+
+    def algorithmic_bytes(self, M):
+        return M * self.K * 2 + 2 * self.K * self.N * 2 + M * self.N * 2
+
+
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+    import swiglu_gemm_transformer_gb300 as sg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sg.lib()
+    wl = Workload(args.workload, dev, variant=sg.VARIANTS[args.variant])
+    stream = torch.cuda.Stream(device=dev)
+    n_calls = len(wl.calls)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):          # load modules, set function attributes, before capture
+            wl.step()
+        stream.synchronize()
+        rc, detail = sg.swiglu_device_status(stream)
+        if rc != sg.OK:
+            raise RuntimeError(f"device status after warm-up: {sg.status_string(rc)} ({detail})")
+        g_step = capture(wl.step, stream)
+
+        # instrumented copies of the step: an external timing event after each call
+        n_ev_graphs = 16
+        ev_graphs = []
+        for _ in range(n_ev_graphs):
+            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_calls + 1)]
+
+            def body(evs=evs):
+                evs[0].record()
+                for i, (_, _, _, fn) in enumerate(wl.calls):
+                    fn()
+                    evs[i + 1].record()
+            ev_graphs.append((capture(body, stream), evs))
+
+        for _ in range(args.warmup):
+            g_step.replay()
+        stream.synchronize()
+
+    sampler = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take a baseline sample
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    per_call = [[] for _ in range(n_calls)]
+    with torch.cuda.stream(stream):
+        t_start.record()
+        done = 0
+        while done < args.steps:
+            batch = min(n_ev_graphs, args.steps - done)
+            for i in range(batch):
+                ev_graphs[i][0].replay()
+            # harvest this batch's per-call durations (the sync costs a few us per batch)
+            ev_graphs[batch - 1][1][-1].synchronize()
+            for i in range(batch):
+                evs = ev_graphs[i][1]
+                for c in range(n_calls):
+                    per_call[c].append(evs[c].elapsed_time(evs[c + 1]))
+            done += batch
+        t_end.record()
+    t_end.synchronize()
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    clocks = sampler.stop()
+    rc, detail = sg.swiglu_device_status(stream)
+    if rc != sg.OK:
+        raise RuntimeError(f"device status after timing: {sg.status_string(rc)} ({detail})")
+
+    # plain-graph timing of the same step (no events inside), for the overhead check
+    with torch.cuda.stream(stream):
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record()
+        for _ in range(args.steps):
+            g_step.replay()
+        p1.record()
+    p1.synchronize()
+    ms_plain = p0.elapsed_time(p1)
+
+    t_max = ms_total
+    if ws > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    ms_per_step = t_max / args.steps
+    value = ws * wl.flops * args.steps / (t_max * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    sustained = t_max > 1000.0
+    peak_tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    kernels = []
+    for c, (form, M, v, _) in enumerate(wl.calls):
+        us = statistics.mean(per_call[c]) * 1e3
+        flops = 4 * M * wl.N * wl.K
+        abytes = wl.algorithmic_bytes(M)
+        t_hbm = abytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = flops / (peak_tf * 1e12)
+        bound = "tensor" if t_tc >= t_hbm else "hbm"
+        achieved_tf = flops / (us * 1e-6) / 1e12
+        achieved_gbs = abytes / (us * 1e-6) / 1e9
+        kernels.append({
+            "form": form, "M": M, "variant": sg.variant_name(v), "us": round(us, 3),
+            "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
+            "frac_of_roofline": round(max(t_tc, t_hbm) / (us * 1e-6), 4),
+            "share": 0.0,
+        })
+    tot_us = sum(k["us"] for k in kernels)
+    for k in kernels:
+        k["share"] = round(k["us"] / tot_us, 4)
+    dom = max(range(n_calls), key=lambda i: kernels[i]["us"])
+    dk = kernels[dom]
+    form, M, v, _ = wl.calls[dom]
+    kernel_key = f"{wl.name}:{form}:M{M}:{sg.variant_name(v)}"
+    if dk["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": dk["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(dk["tflops"] / peak_tf, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(dk["gbs"] / peaks["hbm_gbs"], 4)}
+    roof["traffic"] = load_traffic(kernel_key)
+    roof["kernel"] = kernel_key
+    roof["algorithmic_per_launch"] = (4 * M * wl.N * wl.K if dk["bound"] == "tensor"
+                                      else wl.algorithmic_bytes(M))
+    roof["peak_source"] = f"{peak_src} ({'sustained' if sustained and dk['bound'] == 'tensor' else 'burst'})"
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "impl": "ours",
+        "config": {
+            "workload": f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
+                        f"separate and interleaved weights, seed {wl.seed}",
+            "calls_per_step": n_calls,
+            "l2": f"inputs larger than L2: each call has its own A, weights and Y; "
+                  f"{wl.bytes_touched / 2**20:.0f} MiB per step vs {L2_BYTES / 2**20:.0f} MiB L2",
+            "timing": "CUDA graph of one step, external CUDA events after each call, "
+                      "max over ranks",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "gpu_launches": n_calls * args.steps,
+        "roofline": roof,
+        "clocks": clocks,
+        "kernels": kernels,
+        "timing_check": {"ms_per_step_plain_graph": round(ms_plain / args.steps, 5)},
+    }
+    return out, wl, stream
+
+
+def run_e2e(args, wl, stream, ws):
+    """Same step through the public API: A in from pinned host memory, Y out to it."""
+    import torch
+    import swiglu_gemm_transformer_gb300 as sg
+    dev = wl.dev
+    # pinned host copies of each call's A and a pinned landing buffer for each Y
+    host_a, host_y, dev_bufs = [], [], []
+    h2d = d2h = 0
+    for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
+        A_host = wl.host[M][0].pin_memory()
+        Y_host = torch.empty((M, wl.N), dtype=torch.bfloat16).pin_memory()
+        host_a.append(A_host)
+        host_y.append(Y_host)
+        dev_bufs.append(bufs)
+        h2d += A_host.numel() * 2
+        d2h += Y_host.numel() * 2
+
+    def step():
+        for (form, M, v, _), A_h, Y_h, bufs in zip(wl.calls, host_a, host_y, dev_bufs):
+            Ad = bufs[0]
+            Ad.copy_(A_h, non_blocking=True)
+            if form == "separate":
+                Y = sg.swiglu_fused(Ad, bufs[1], bufs[2], bufs[3], variant=v)
+            else:
+                Y = sg.swiglu_fused_interleaved(Ad, bufs[1], bufs[2], variant=v)
+            Y_h.copy_(Y, non_blocking=True)
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    val = ws * wl.flops * steps / (ms * 1e-3) / 1e12
+    return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "weights resident in HBM; each step copies every call's A in and Y out (pinned host)"}
+
+
+def run_unfused_context(wl, stream, steps):
+    """Context only: the unfused eager path (two cuBLAS GEMMs, SiLU, multiply) on the same inputs."""
+    import torch
+    import torch.nn.functional as F
+
+    def step():
+        for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
+            if form != "separate":
+                continue
+            A, W1, W2, Y = bufs
+            torch.mul(F.silu(A @ W1), A @ W2, out=Y)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        g = capture(step, stream)
+        for _ in range(3):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = sum(4 * M * wl.N * wl.K for (f, M, _, _) in wl.calls if f == "separate")
+    return {"what": "torch eager: A@W1, A@W2 (cuBLAS), silu, mul; separate-weight calls only",
+            "ms_per_step": round(ms, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample(workload: str, target_s: float):
+    """Time the CPU oracle on a bounded sample of the workload: for every call
+    (form, M) of the step, the same number of seeded rows.  Returns
+    (TFLOP/s, threads, description, seconds)."""
+    import numpy as np
+    import oracle
+    import swiglu_inputs as si
+    K, N, Ms, seed = WORKLOADS[workload]
+    oracle.build()
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    _, W1, W2 = si.make_bf16(1, N, K, seed)
+    w1, w2 = si.bits_u16(W1), si.bits_u16(W2)
+    wf = oracle.pack_interleaved(w1, w2)
+    rng = np.random.default_rng(seed)
+    A = si.bits_u16(si.make_bf16(max(Ms), N, K, seed)[0])
+
+    def one(rows_per_call):
+        t0 = time.perf_counter()
+        flops = 0
+        for form in ("separate", "interleaved"):
+            for M in Ms:
+                rows = np.sort(rng.integers(0, M, size=rows_per_call))
+                if form == "separate":
+                    oracle.swiglu_bf16(A[:M], w1, w2, rows=rows)
+                else:
+                    oracle.swiglu_interleaved_bf16(A[:M], wf, rows=rows)
+                flops += 4 * rows_per_call * N * K
+        return flops, time.perf_counter() - t0
+
+    f0, s0 = one(max(1, threads))               # calibration
+    rate = f0 / s0
+    per_row = 4 * N * K * 2 * len(Ms)
+    rows = max(1, int(target_s * rate / per_row))
+    flops, secs = one(rows)
+    desc = (f"{rows} seeded rows of each of the {2 * len(Ms)} calls (M in {list(Ms)}, separate and "
+            f"interleaved), all N={N} columns, K={K}: {flops / 1e9:.1f} GFLOP in {secs:.1f} s")
+    return flops / secs / 1e12, threads, desc, secs
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    target = 12.0 / max(1, args.steps + args.warmup)
+    target = max(0.5, min(target, 6.0))
+    import numpy as np  # noqa: F401
+    vals = []
+    desc = ""
+    threads = 0
+    for i in range(args.warmup + args.steps):
+        v, threads, desc, secs = oracle_sample(args.workload, target)
+        if i >= args.warmup:
+            vals.append((v, secs))
+    tot_flops = sum(v * s for v, s in vals)
+    tot_s = sum(s for _, s in vals)
+    value = tot_flops / tot_s
+    K, N, Ms, seed = WORKLOADS[args.workload]
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / max(1, len(vals)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{args.workload} MLP projection K={K} N={N} M={list(Ms)}, "
+                               f"separate and interleaved weights, seed {seed}",
+                   "sample": "each step is a bounded row sample; see cpu_baseline"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--variant", choices=("auto", "1sm_n128", "1sm_n64"), default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="bounded CPU-oracle sample size for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        out = run_reference(args, ws, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        out, wl, stream = run_ours(args, ws, rank, local)
+        out["e2e"] = run_e2e(args, wl, stream, ws)
+        if not args.no_context:
+            out["context_unfused_torch"] = run_unfused_context(wl, stream, min(args.steps, 200))
+        if rank == 0:
+            if args.no_cpu_baseline or ws > 1:
+                out["cpu_baseline"] = None
+            else:
+                v, threads, desc, _ = oracle_sample(args.workload, args.cpu_seconds)
+                out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads,
+                                       "kind": "oracle", "sample": desc}
+            print(json.dumps(out), flush=True)
+    finally:
+        if ws > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

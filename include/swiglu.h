@@ -1,0 +1,145 @@
+/*
+ * swiglu.h -- C ABI of the GB300 (sm_103a) fused SwiGLU projection library.
+ *
+ * The operation (page "Riepilogo Tecnico: Sovrapposizione delle Attivazioni a
+ * Livello di Tile per l'Inferenza Efficiente di LLM", gist.science paper
+ * 2607.02521, section "Definizione del Problema"):
+ *
+ *     Y[M,N] = SiLU(A[M,K] x W1[K,N]) (.) (A[M,K] x W2[K,N]),
+ *     SiLU(x) = x / (1 + e^-x),
+ *
+ * computed on tcgen05 tensor cores with FP32 accumulation; the gate and up
+ * products stay on chip (tensor memory) and only Y is written, rounded once
+ * to BF16 (round to nearest even).
+ *
+ * Conventions shared by every entry point:
+ *   - All matrices are dense row-major with no padding: A is [M,K] (K
+ *     contiguous), weights are [K,N] (N contiguous), Y is [M,N].
+ *   - All tensor pointers are CUDA device pointers owned by the caller; the
+ *     library never allocates, frees or retains them past the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued asynchronously; no entry point synchronises
+ *     except swiglu_device_status().
+ *   - Argument errors are reported synchronously, before anything is enqueued.
+ *     CUDA launch errors are reported as SWIGLU_ERR_CUDA.  A device-side wait
+ *     that exceeded its time limit (see swiglu_set_wait_timeout_ns) is recorded
+ *     on the device and reported by swiglu_device_status().
+ *   - Alignment rules come from the tensor-memory-accelerator copy engine:
+ *     every base pointer 16-byte aligned, and every row pitch a multiple of
+ *     16 bytes (K and N multiples of 8 for BF16, of 16 for FP8).
+ *   - Y must not overlap any input.
+ *   - M, N or K equal to 0 is valid: M = 0 or N = 0 enqueues nothing; K = 0
+ *     makes every product zero, so Y is filled with zeros.
+ *   - Dimensions must be below 2^31.
+ *   - Threading: calls may come from several host threads; the lazily built
+ *     per-device state is guarded by a lock.
+ */
+#ifndef SWIGLU_GB300_H
+#define SWIGLU_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    SWIGLU_OK = 0,
+    SWIGLU_ERR_INVALID_ARG = 1,  /* null pointer, negative size, overlap, bad variant */
+    SWIGLU_ERR_MISALIGNED = 2,   /* base not 16-byte aligned or row pitch not a multiple of 16 bytes */
+    SWIGLU_ERR_UNSUPPORTED = 3,  /* device is not sm_103 / sm_100 family, or size beyond limits */
+    SWIGLU_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    SWIGLU_ERR_TIMEOUT = 5       /* a device-side wait ran past its limit (see swiglu_device_status) */
+} swiglu_status;
+
+/* Kernel variants.  SWIGLU_VARIANT_AUTO lets the library choose by (M,N,K). */
+typedef enum {
+    SWIGLU_VARIANT_AUTO = 0,
+    /* one CTA per SM, 128-row tiles, 128 output columns per tile
+       (one 128x256 MMA covers the gate and up halves) */
+    SWIGLU_VARIANT_1SM_N128 = 1,
+    /* one CTA per SM, 128-row tiles, 64 output columns per tile (more tiles for small M) */
+    SWIGLU_VARIANT_1SM_N64 = 2,
+    SWIGLU_VARIANT_COUNT_ = 3
+} swiglu_variant;
+
+/*
+ * Y = SiLU(A x W1) (.) (A x W2) with BF16 A, W1, W2 and BF16 Y.
+ * Page section "Metodologia", item 1 ("Kernel-1"): two weight matrices, the
+ * gate and up products of one output tile computed together.
+ *   A  : device, BF16 [M,K] row-major        (read)
+ *   W1 : device, BF16 [K,N] row-major (gate)  (read)
+ *   W2 : device, BF16 [K,N] row-major (up)    (read)
+ *   Y  : device, BF16 [M,N] row-major        (written)
+ */
+int swiglu_fused(const void *A, const void *W1, const void *W2, void *Y,
+                 int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * The interleaved form.  Page section "Metodologia", item 2 ("Kernel-2"):
+ * one weight matrix W_fused[K,2N] whose even column 2n is gate column n and
+ * whose odd column 2n+1 is up column n; one product over [M,2N,K] whose
+ * adjacent accumulator columns (2n, 2n+1) give Y[m,n] = SiLU(D[m,2n]) * D[m,2n+1].
+ *   A      : device, BF16 [M,K] row-major  (read)
+ *   Wfused : device, BF16 [K,2N] row-major (read), as made by swiglu_pack_interleaved
+ *   Y      : device, BF16 [M,N] row-major  (written)
+ */
+int swiglu_fused_interleaved(const void *A, const void *Wfused, void *Y,
+                             int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * Weight packer for the interleaved form (same page, section "Metodologia",
+ * item 2): Wfused[k,2n] = W1[k,n], Wfused[k,2n+1] = W2[k,n].  A one-off step at
+ * model load, not part of the per-call path.
+ *   W1, W2 : device, BF16 [K,N] row-major (read)
+ *   Wfused : device, BF16 [K,2N] row-major (written; must not overlap W1/W2)
+ */
+int swiglu_pack_interleaved(const void *W1, const void *W2, void *Wfused,
+                            int64_t K, int64_t N, void *stream);
+
+/* swiglu_fused / swiglu_fused_interleaved with an explicit variant
+ * (SWIGLU_VARIANT_*) instead of the library's choice; for sweeps and tests. */
+int swiglu_fused_ex(const void *A, const void *W1, const void *W2, void *Y,
+                    int64_t M, int64_t N, int64_t K, int32_t variant, void *stream);
+int swiglu_fused_interleaved_ex(const void *A, const void *Wfused, void *Y,
+                                int64_t M, int64_t N, int64_t K, int32_t variant,
+                                void *stream);
+
+/* The variant SWIGLU_VARIANT_AUTO resolves to for this shape and form
+ * (interleaved = 0 or 1) on the current device.  Host-only. */
+int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved);
+
+/* Short name of a variant ("1sm_n128", ...); "?" for an unknown value. */
+const char *swiglu_variant_name(int32_t variant);
+
+/* Human-readable text of a status code. */
+const char *swiglu_status_string(int32_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns SWIGLU_OK, SWIGLU_ERR_TIMEOUT if a kernel gave up a wait since
+ * the last call (its CTA stopped early, so that launch's Y is incomplete), or
+ * SWIGLU_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
+ * NULL it receives a code naming the wait that gave up (0 if none).
+ */
+int swiglu_device_status(void *stream, uint32_t *detail);
+
+/* Time limit of every device-side wait, in nanoseconds (default 2e9, i.e. two
+ * seconds; minimum 1e6).  Applies to launches enqueued after the call. */
+int swiglu_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Failure-detection self test: enqueues one small kernel whose single wait
+ * is on a barrier that nothing ever completes, with a limit of `timeout_us`
+ * microseconds (1..10^6).  The kernel gives up, records SWIGLU_ERR_TIMEOUT in
+ * the device error word and returns normally; the context stays usable.  Read
+ * the result with swiglu_device_status().
+ */
+int swiglu_selftest_wait_timeout(uint32_t timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_GB300_H */

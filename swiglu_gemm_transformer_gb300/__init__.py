@@ -1,0 +1,187 @@
+"""Python binding of the GB300 fused SwiGLU library (argument marshalling only).
+
+Every function here forwards to the C ABI of ``libswiglu_gb300.so`` (declared
+in ``include/swiglu.h``) with the same name; all arithmetic runs in the CUDA
+kernels.  There is no CPU fallback: if the library is missing or a call fails
+the function raises.
+
+    Y = SiLU(A @ W1) * (A @ W2)   A: [M,K] bf16, W1/W2: [K,N] bf16, Y: [M,N] bf16
+
+PyTorch supplies device memory and the current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswiglu_gb300.so")
+
+OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
+VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64 = 0, 1, 2
+VARIANTS = {"auto": VARIANT_AUTO, "1sm_n128": VARIANT_1SM_N128, "1sm_n64": VARIANT_1SM_N64}
+
+EXPORTS = {
+    # name: (argtypes, restype)
+    "swiglu_fused": ("pppp lll p", ctypes.c_int),
+    "swiglu_fused_ex": ("pppp lll i p", ctypes.c_int),
+    "swiglu_fused_interleaved": ("ppp lll p", ctypes.c_int),
+    "swiglu_fused_interleaved_ex": ("ppp lll i p", ctypes.c_int),
+    "swiglu_pack_interleaved": ("ppp ll p", ctypes.c_int),
+    "swiglu_select_variant": ("lll i", ctypes.c_int),
+    "swiglu_variant_name": ("i", ctypes.c_char_p),
+    "swiglu_status_string": ("i", ctypes.c_char_p),
+    "swiglu_device_status": ("p P", ctypes.c_int),
+    "swiglu_set_wait_timeout_ns": ("Q", ctypes.c_int),
+    "swiglu_selftest_wait_timeout": ("I p", ctypes.c_int),
+}
+_CT = {"p": ctypes.c_void_p, "l": ctypes.c_int64, "i": ctypes.c_int32, "Q": ctypes.c_uint64,
+       "I": ctypes.c_uint32, "P": ctypes.POINTER(ctypes.c_uint32)}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SwigluError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (sig, res) in EXPORTS.items():
+            f = getattr(l, name)
+            f.argtypes = [_CT[c] for c in sig.replace(" ", "")]
+            f.restype = res
+        _lib = l
+        return l
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().swiglu_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still give a message
+        return f"status {status}"
+
+
+def variant_name(v: int) -> str:
+    return lib().swiglu_variant_name(int(v)).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != OK:
+        raise SwigluError(fn, rc)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype=None, ndim=2):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+    return t
+
+
+def swiglu_fused(A, W1, W2, Y=None, *, variant: int = VARIANT_AUTO, stream=None):
+    """Y = SiLU(A @ W1) * (A @ W2) with separate [K,N] weights; returns Y."""
+    import torch
+    bf = torch.bfloat16
+    _need(A, "A", bf), _need(W1, "W1", bf), _need(W2, "W2", bf)
+    M, K = A.shape
+    if W1.shape[0] != K or W2.shape != W1.shape:
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, W1 {tuple(W1.shape)}, W2 {tuple(W2.shape)}")
+    N = W1.shape[1]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=bf, device=A.device)
+    else:
+        _need(Y, "Y", bf)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [M, N]")
+    rc = lib().swiglu_fused_ex(A.data_ptr(), W1.data_ptr(), W2.data_ptr(), Y.data_ptr(),
+                               M, N, K, int(variant), _stream(stream))
+    _check("swiglu_fused", rc)
+    return Y
+
+
+def swiglu_fused_interleaved(A, Wfused, Y=None, *, variant: int = VARIANT_AUTO, stream=None):
+    """Y[m,n] = SiLU(D[m,2n]) * D[m,2n+1] with D = A @ Wfused, Wfused [K,2N]; returns Y."""
+    import torch
+    bf = torch.bfloat16
+    _need(A, "A", bf), _need(Wfused, "Wfused", bf)
+    M, K = A.shape
+    if Wfused.shape[0] != K or Wfused.shape[1] % 2:
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, Wfused {tuple(Wfused.shape)}")
+    N = Wfused.shape[1] // 2
+    if Y is None:
+        Y = torch.empty((M, N), dtype=bf, device=A.device)
+    else:
+        _need(Y, "Y", bf)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [M, N]")
+    rc = lib().swiglu_fused_interleaved_ex(A.data_ptr(), Wfused.data_ptr(), Y.data_ptr(),
+                                           M, N, K, int(variant), _stream(stream))
+    _check("swiglu_fused_interleaved", rc)
+    return Y
+
+
+def swiglu_pack_interleaved(W1, W2, Wfused=None, *, stream=None):
+    """Wfused[k,2n] = W1[k,n], Wfused[k,2n+1] = W2[k,n]; returns Wfused [K,2N]."""
+    import torch
+    if W1.dtype != W2.dtype or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must match in shape and dtype")
+    _need(W1, "W1", torch.bfloat16), _need(W2, "W2", torch.bfloat16)
+    K, N = W1.shape
+    if Wfused is None:
+        Wfused = torch.empty((K, 2 * N), dtype=W1.dtype, device=W1.device)
+    else:
+        _need(Wfused, "Wfused", W1.dtype)
+        if tuple(Wfused.shape) != (K, 2 * N):
+            raise ValueError("Wfused must be [K, 2N]")
+    rc = lib().swiglu_pack_interleaved(W1.data_ptr(), W2.data_ptr(), Wfused.data_ptr(), K, N,
+                                       _stream(stream))
+    _check("swiglu_pack_interleaved", rc)
+    return Wfused
+
+
+def swiglu_select_variant(M: int, N: int, K: int, interleaved: bool = False) -> int:
+    return lib().swiglu_select_variant(M, N, K, 1 if interleaved else 0)
+
+
+def swiglu_device_status(stream=None):
+    """Synchronise the stream; return (status, detail) and clear the device error word."""
+    detail = ctypes.c_uint32(0)
+    rc = lib().swiglu_device_status(_stream(stream), ctypes.byref(detail))
+    return rc, detail.value
+
+
+def swiglu_set_wait_timeout_ns(ns: int):
+    _check("swiglu_set_wait_timeout_ns", lib().swiglu_set_wait_timeout_ns(int(ns)))
+
+
+def swiglu_selftest_wait_timeout(timeout_us: int, stream=None):
+    _check("swiglu_selftest_wait_timeout",
+           lib().swiglu_selftest_wait_timeout(int(timeout_us), _stream(stream)))

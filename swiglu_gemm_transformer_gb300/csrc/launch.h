@@ -1,0 +1,35 @@
+// launch.h -- internal interface between the C-ABI host code and the kernel
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "swiglu_tc_kernel.cuh"
+
+namespace swiglu {
+
+struct LaunchArgs {
+  CUtensorMap a, b0, b1, y;
+  KParams p;
+  int grid;
+  int device;
+  cudaStream_t stream;
+};
+
+// Tile geometry of each BF16 variant (SWIGLU_VARIANT_*), for host-side planning.
+struct VariantGeom {
+  int bm, bn, bk;     // output rows, output columns, K per stage
+  int box_b;          // weight box width (columns) per TMA copy
+};
+
+VariantGeom variant_geom(int variant);
+
+cudaError_t launch_bf16_separate(int variant, const LaunchArgs &la);
+cudaError_t launch_bf16_interleaved(int variant, const LaunchArgs &la);
+cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf, int64_t n_elems,
+                                        int sm_count, cudaStream_t s);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t *err, cudaStream_t s);
+
+}  // namespace swiglu

@@ -1,0 +1,313 @@
+// swiglu_api.cu -- host side of the C ABI declared in include/swiglu.h:
+// argument validation, per-device state, TMA tensor-map encoding, variant
+// choice and launch.  No entry point allocates device memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+#include "swiglu.h"
+
+using namespace swiglu;
+
+// Device error word: [0] = first status recorded by a kernel since the last
+// swiglu_device_status(), [1] = which wait gave up.
+__device__ uint32_t g_swiglu_err_word[2];
+
+namespace {
+
+struct DeviceState {
+  bool ready = false;
+  int status = SWIGLU_OK;  // sticky result of the one-time set-up
+  int sm_count = 0;
+  uint32_t *err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState **out, int *dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState &st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SWIGLU_ERR_CUDA;
+    }
+    // The kernels are built for sm_103a only (arch-specific tcgen05 code).
+    if (major != 10 || minor != 3) return SWIGLU_ERR_UNSUPPORTED;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err), g_swiglu_err_word) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return SWIGLU_ERR_CUDA;
+    }
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void *fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.sm_count = sms;
+    st.ready = true;
+  }
+  *out = &st;
+  *dev_out = dev;
+  return SWIGLU_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, uint64_t an, const void *b, uint64_t bn) {
+  if (!a || !b || an == 0 || bn == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
+              uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int choose_variant(int64_t M, int64_t N, int64_t /*K*/, bool /*interleaved*/, int sm_count) {
+  // Small M: too few 128-column tiles to occupy every SM, so halve the tile
+  // width (the page's Kernel-2 argument: more thread blocks for small batches).
+  const int64_t tiles128 = cdiv(M, 128) * cdiv(N, 128);
+  if (tiles128 < sm_count) return SWIGLU_VARIANT_1SM_N64;
+  return SWIGLU_VARIANT_1SM_N128;
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, int64_t N,
+             int64_t K, int32_t variant, bool interleaved, void *stream) {
+  if (variant < 0 || variant >= SWIGLU_VARIANT_COUNT_) return SWIGLU_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || 2 * N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SWIGLU_OK;
+  if (!Y) return SWIGLU_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B0 || (!interleaved && !B1))) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(Y)) return SWIGLU_ERR_MISALIGNED;
+  if (K > 0 && (!aligned16(A) || !aligned16(B0) || (!interleaved && !aligned16(B1))))
+    return SWIGLU_ERR_MISALIGNED;
+  if (N % 8 != 0 || K % 8 != 0) return SWIGLU_ERR_MISALIGNED;
+  const uint64_t y_bytes = uint64_t(M) * N * 2, a_bytes = uint64_t(M) * K * 2;
+  const uint64_t w_bytes = uint64_t(K) * N * 2 * (interleaved ? 2 : 1);
+  if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, B0, w_bytes) ||
+      (!interleaved && overlaps(Y, y_bytes, B1, w_bytes)))
+    return SWIGLU_ERR_INVALID_ARG;
+
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {  // every product is zero, and SiLU(0) * 0 = 0
+    return cudaMemsetAsync(Y, 0, y_bytes, s) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  }
+  if (variant == SWIGLU_VARIANT_AUTO) variant = choose_variant(M, N, K, interleaved, st->sm_count);
+  const VariantGeom g = variant_geom(variant);
+
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof la);
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  rc = encode_2d(&la.a, BF16, A, K, M, K * 2, g.bk, g.bm, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == SWIGLU_OK) {
+    if (interleaved) {
+      rc = encode_2d(&la.b0, BF16, B0, 2 * N, K, 4 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
+      la.b1 = la.b0;
+    } else {
+      rc = encode_2d(&la.b0, BF16, B0, N, K, 2 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc == SWIGLU_OK)
+        rc = encode_2d(&la.b1, BF16, B1, N, K, 2 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+  }
+  if (rc == SWIGLU_OK)
+    rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc != SWIGLU_OK) return rc;
+
+  KParams &p = la.p;
+  p.M = int32_t(M);
+  p.N = int32_t(N);
+  p.K = int32_t(K);
+  p.num_m_blk = int32_t(cdiv(M, g.bm));
+  p.num_n_blk = int32_t(cdiv(N, g.bn));
+  p.num_k_blk = int32_t(cdiv(K, g.bk));
+  p.group_m = p.num_m_blk < 16 ? p.num_m_blk : 16;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.err = st->err;
+  const int64_t tiles = int64_t(p.num_m_blk) * p.num_n_blk;
+  if (tiles > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  la.grid = int(tiles < st->sm_count ? tiles : st->sm_count);
+  la.device = dev;
+  la.stream = s;
+  cudaError_t e = interleaved ? launch_bf16_interleaved(variant, la)
+                              : launch_bf16_separate(variant, la);
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace swiglu {
+
+VariantGeom variant_geom(int variant) {
+  switch (variant) {
+    case SWIGLU_VARIANT_1SM_N64:
+      return {128, 64, 64, 64};
+    case SWIGLU_VARIANT_1SM_N128:
+    default:
+      return {128, 128, 64, 64};
+  }
+}
+
+}  // namespace swiglu
+
+extern "C" {
+
+int swiglu_fused(const void *A, const void *W1, const void *W2, void *Y, int64_t M, int64_t N,
+                 int64_t K, void *stream) {
+  return run_bf16(A, W1, W2, Y, M, N, K, SWIGLU_VARIANT_AUTO, false, stream);
+}
+
+int swiglu_fused_ex(const void *A, const void *W1, const void *W2, void *Y, int64_t M, int64_t N,
+                    int64_t K, int32_t variant, void *stream) {
+  return run_bf16(A, W1, W2, Y, M, N, K, variant, false, stream);
+}
+
+int swiglu_fused_interleaved(const void *A, const void *Wfused, void *Y, int64_t M, int64_t N,
+                             int64_t K, void *stream) {
+  return run_bf16(A, Wfused, nullptr, Y, M, N, K, SWIGLU_VARIANT_AUTO, true, stream);
+}
+
+int swiglu_fused_interleaved_ex(const void *A, const void *Wfused, void *Y, int64_t M, int64_t N,
+                                int64_t K, int32_t variant, void *stream) {
+  return run_bf16(A, Wfused, nullptr, Y, M, N, K, variant, true, stream);
+}
+
+int swiglu_pack_interleaved(const void *W1, const void *W2, void *Wfused, int64_t K, int64_t N,
+                            void *stream) {
+  if (K < 0 || N < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (K > kMaxDim || 2 * N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (K == 0 || N == 0) return SWIGLU_OK;
+  if (!W1 || !W2 || !Wfused) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W2) || !aligned16(Wfused)) return SWIGLU_ERR_MISALIGNED;
+  if (N % 8 != 0) return SWIGLU_ERR_MISALIGNED;
+  const uint64_t w = uint64_t(K) * N * 2;
+  if (overlaps(Wfused, 2 * w, W1, w) || overlaps(Wfused, 2 * w, W2, w))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaError_t e = launch_pack_interleaved_u16(W1, W2, Wfused, K * N, st->sm_count,
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved) {
+  if (M < 0 || N < 0 || K < 0) return SWIGLU_VARIANT_AUTO;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 152;  // GB300's SM count, for host-only planning without a device
+  }
+  return choose_variant(M, N, K, interleaved != 0, sms);
+}
+
+const char *swiglu_variant_name(int32_t variant) {
+  switch (variant) {
+    case SWIGLU_VARIANT_AUTO: return "auto";
+    case SWIGLU_VARIANT_1SM_N128: return "1sm_n128";
+    case SWIGLU_VARIANT_1SM_N64: return "1sm_n64";
+    default: return "?";
+  }
+}
+
+const char *swiglu_status_string(int32_t status) {
+  switch (status) {
+    case SWIGLU_OK: return "ok";
+    case SWIGLU_ERR_INVALID_ARG: return "invalid argument";
+    case SWIGLU_ERR_MISALIGNED: return "misaligned pointer or row pitch";
+    case SWIGLU_ERR_UNSUPPORTED: return "unsupported device or size";
+    case SWIGLU_ERR_CUDA: return "CUDA error";
+    case SWIGLU_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int swiglu_device_status(void *stream, uint32_t *detail) {
+  if (detail) *detail = 0;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  uint32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, st->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_ERR_CUDA;
+  }
+  if (h[0] != 0) {
+    const uint32_t z[2] = {0, 0};
+    if (cudaMemcpy(st->err, z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return SWIGLU_ERR_CUDA;
+    }
+  }
+  if (detail) *detail = h[1];
+  return h[0] != 0 ? int(h[0]) : SWIGLU_OK;
+}
+
+int swiglu_set_wait_timeout_ns(uint64_t ns) {
+  if (ns < 1000000ull) return SWIGLU_ERR_INVALID_ARG;
+  g_timeout_ns.store(ns, std::memory_order_relaxed);
+  return SWIGLU_OK;
+}
+
+int swiglu_selftest_wait_timeout(uint32_t timeout_us, void *stream) {
+  if (timeout_us < 1 || timeout_us > 1000000u) return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaError_t e = launch_selftest_wait(uint64_t(timeout_us) * 1000ull, st->err,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,387 @@
+// swiglu_tc_kernel.cuh -- the fused SwiGLU tcgen05 kernel for sm_103a.
+//
+// Computes Y = SiLU(A x W1) (.) (A x W2) (page "Riepilogo Tecnico:
+// Sovrapposizione delle Attivazioni a Livello di Tile per l'Inferenza
+// Efficiente di LLM", section "Definizione del Problema") one 128-row output
+// tile at a time, in either weight form the page describes (section
+// "Metodologia": two separate weight matrices, item 1, or one interleaved
+// W_fused[K,2N], item 2).
+//
+// GB300 design (the page's kernels target H100 and register accumulators):
+//   * persistent CTAs, one per SM, walk the output tiles in a grouped order so
+//     that concurrently running tiles share A rows and weight columns in L2;
+//   * warp 4 (one thread) streams A[128 x 64] and the weight tile
+//     [64 x MMA_N] of every K step into a STAGES-deep shared-memory ring with
+//     TMA (128-byte swizzle), completion counted on mbarriers;
+//   * warp 5 (one thread) issues tcgen05.mma.kind::f16 M=128 x N=MMA_N x K=16.
+//     The B operand of one MMA holds the gate columns AND the up columns of the
+//     tile side by side, so a single instruction produces both accumulators in
+//     tensor memory: separate form -> TMEM columns [0,BN) = gate, [BN,2BN) = up;
+//     interleaved form -> column 2j = gate j, 2j+1 = up j (the page's
+//     PairMulStore pairing, now on adjacent TMEM columns);
+//   * the accumulators are double-buffered in TMEM (2 x MMA_N columns) so the
+//     epilogue of tile i overlaps the MMAs of tile i+1;
+//   * warps 0-3 (the epilogue) read their 32 TMEM lanes with tcgen05.ld, apply
+//     y = g * u / (1 + e^-g) in FP32, round to BF16 (RNE), stage 32x32 blocks
+//     in shared memory (64-byte swizzle, bank-conflict free) and write them
+//     with TMA stores whose completion overlaps the next block's arithmetic
+//     (the compute/store overlap of the page's Kernel-2).
+//   Gate and up values never leave the SM.
+//
+// Every mbarrier wait is bounded by a time limit.  On expiry the waiting
+// thread records SWIGLU_ERR_TIMEOUT in the device error word, raises a CTA
+// abort flag so the other roles stop at their next wait, in-flight copies and
+// MMAs are drained (again with a limit), TMEM is freed and the CTA returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+
+namespace swiglu {
+
+// Where a wait gave up (device error word, second slot).
+enum : uint32_t {
+  WAIT_PRODUCER_EMPTY = 1,
+  WAIT_MMA_FULL = 2,
+  WAIT_MMA_ACC_EMPTY = 3,
+  WAIT_EPI_ACC_FULL = 4,
+  WAIT_DRAIN = 5,
+  WAIT_SELFTEST = 6,
+};
+
+constexpr uint32_t kErrTimeout = 5;  // == SWIGLU_ERR_TIMEOUT
+
+struct KParams {
+  int32_t M, N, K;
+  int32_t num_m_blk, num_n_blk, num_k_blk;
+  int32_t group_m;       // grouped raster: this many m-blocks walk the n-blocks together
+  int32_t pad_;
+  uint64_t timeout_ns;   // limit of every mbarrier wait
+  uint32_t *err;         // device error word: [0] = status, [1] = where
+};
+
+template <int NB_ATOMS_, bool INTERLEAVED_, int STAGES_>
+struct TileCfg {
+  static constexpr int NB_ATOMS = NB_ATOMS_;
+  static constexpr bool INTERLEAVED = INTERLEAVED_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int BM = 128;                 // rows per tile (MMA M)
+  static constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of BF16
+  static constexpr int MMA_N = NB_ATOMS * 64;    // gate+up accumulator columns per tile
+  static constexpr int BN = MMA_N / 2;           // output columns per tile
+  static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+  static constexpr int ATOM_BYTES = BK * 128;    // one 64-column weight box: 64 K-rows x 128 B
+  static constexpr int B_BYTES = NB_ATOMS * ATOM_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int STG_BYTES = 32 * 64;      // a warp's 32 rows x 32 BF16 columns
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full[S], empty[S], acc_full[2], acc_empty[2], drain
+  static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + slot/flag + alignment slack
+  static constexpr int TMEM_COLS = (2 * MMA_N <= 256) ? 256 : 512;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
+  static_assert(NB_ATOMS == 2 || NB_ATOMS == 4, "MMA N of 128 or 256");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Bounded wait, slow path.  Returns false on timeout or when another role of
+// this CTA already gave up.
+__device__ __noinline__ static bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag, uint32_t *err,
+                                              uint32_t where) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      if (atomicCAS(err, 0u, kErrTimeout) == 0u) atomicExch(err + 1, where);
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ static bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                volatile int *abort_flag, uint32_t *err,
+                                                uint32_t where) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, limit_ns, abort_flag, err, where);
+}
+
+__device__ __forceinline__ static void tile_coords(int t, const KParams &p, int &mb, int &nb) {
+  const int per_group = p.group_m * p.num_n_blk;
+  const int g = t / per_group;
+  const int first = g * p.group_m;
+  const int rows = min(p.group_m, p.num_m_blk - first);
+  const int r = t - g * per_group;
+  mb = first + r % rows;
+  nb = r / rows;
+}
+
+__device__ __forceinline__ static float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    swiglu_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB0,  // W1, or W_fused
+                          const __grid_constant__ CUtensorMap tmB1,  // W2 (separate form only)
+                          const __grid_constant__ CUtensorMap tmY, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw);
+
+  const uint32_t bars = base + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * C::STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(accf_bar(b), 1);
+      ptx::mbar_init(acce_bar(b), C::EPI_WARPS);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB0);
+    if (!C::INTERLEAVED) ptx::prefetch_tmap(&tmB1);
+    ptx::prefetch_tmap(&tmY);
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.num_m_blk * p.num_n_blk;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        for (int kb = 0; kb < p.num_k_blk; ++kb) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
+                        WAIT_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t fb = full_bar(stage);
+          ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
+          if (C::INTERLEAVED) {
+#pragma unroll
+            for (int j = 0; j < C::NB_ATOMS; ++j)
+              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::MMA_N + j * 64,
+                               kb * C::BK);
+          } else {
+#pragma unroll
+            for (int j = 0; j < C::NB_ATOMS / 2; ++j) {
+              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::BN + j * 64, kb * C::BK);
+              ptx::tma_load_2d(sb + (C::NB_ATOMS / 2 + j) * C::ATOM_BYTES, &tmB1, fb,
+                               nb * C::BN + j * 64, kb * C::BK);
+            }
+          }
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA's shared
+        // memory is released: wait for the last min(issued, STAGES) loads.
+        const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
+        for (uint32_t i = issued - n; i < issued; ++i) {
+          const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1u;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(full_bar(s), ph) &&
+                 ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        if (!wait_bar(acce_bar(abuf), aphase ^ 1u, p.timeout_ns, abort_flag, p.err,
+                      WAIT_MMA_ACC_EMPTY)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + abuf * C::MMA_N;
+        for (int kb = 0; kb < p.num_k_blk; ++kb) {
+          if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            // A: K-major, 128-byte swizzle; 16 K-elements = 32 bytes along the row.
+            const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
+            // B: MN-major, 128-byte swizzle; 64-column boxes ATOM_BYTES apart (LBO),
+            // 8-row K groups 1024 bytes apart (SBO); 16 K-rows = 2048 bytes.
+            const uint64_t bdesc =
+                ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
+            ptx::mma_f16(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(accf_bar(abuf));
+        if (++abuf == 2) {
+          abuf = 0;
+          aphase ^= 1u;
+        }
+      }
+      // Every MMA this thread issued completes before TMEM can be freed.
+      ptx::mma_commit(drain_bar);
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3)
+    const int q = warp;  // TMEM lanes [32q, 32q+32) = tile rows [32q, 32q+32)
+    const uint32_t stg_base = base + C::STG_OFF + q * 2 * C::STG_BYTES;
+    uint32_t abuf = 0, aphase = 0, it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      bool ok = wait_bar(accf_bar(abuf), aphase, p.timeout_ns, abort_flag, p.err,
+                         WAIT_EPI_ACC_FULL);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
+      const int row0 = mb * C::BM + q * 32;
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 32; ++c) {
+        uint32_t g[32], u[32];
+        if (C::INTERLEAVED) {
+          ptx::tmem_ld32(trow + c * 64, g);
+          ptx::tmem_ld32(trow + c * 64 + 32, u);
+        } else {
+          ptx::tmem_ld32(trow + c * 32, g);
+          ptx::tmem_ld32(trow + C::BN + c * 32, u);
+        }
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(g);
+        ptx::reg_fence(u);
+        if (c == C::BN / 32 - 1) {
+          // This warp is done reading the accumulator buffer.
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(acce_bar(abuf));
+        }
+        uint32_t packed[16];
+        if (C::INTERLEAVED) {
+          // g holds TMEM columns 64c..64c+31 = pairs (gate, up) for outputs 32c..32c+15,
+          // u holds the pairs for outputs 32c+16..32c+31.
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            packed[i] = pack_bf16x2(
+                silu_mul(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1])),
+                silu_mul(__uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3])));
+            packed[8 + i] = pack_bf16x2(
+                silu_mul(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1])),
+                silu_mul(__uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = pack_bf16x2(
+                silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+        }
+        const int col0 = nb * C::BN + c * 32;
+        const uint32_t stg = stg_base + (it & 1u) * C::STG_BYTES;
+        // The store issued from this buffer two blocks ago must have finished reading it.
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+        uint4 *rowp = reinterpret_cast<uint4 *>(smem + (stg - base) + lane * 64);
+        const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk i -> i ^ ((row >> 1) & 3)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rowp[i ^ sw] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.M && col0 < p.N) {
+          ptx::tma_store_2d(&tmY, stg, col0, row0);
+        }
+        if (lane == 0) ptx::bulk_commit();
+        ++it;
+      }
+      if (++abuf == 2) {
+        abuf = 0;
+        aphase ^= 1u;
+      }
+    }
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// A kernel whose only wait is on a barrier that nothing ever completes: it
+// exercises the bounded-wait failure path (records SWIGLU_ERR_TIMEOUT and
+// returns).
+__global__ void selftest_wait_kernel(uint64_t limit_ns, uint32_t *err);
+
+}  // namespace swiglu

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the public
+header declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import swiglu_gemm_transformer_gb300 as sg
+from swiglu_gemm_transformer_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "swiglu.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sg.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swiglu_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("swiglu_fused", "swiglu_fused_interleaved", "swiglu_pack_interleaved",
+                 "swiglu_device_status", "swiglu_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared in swiglu.h but not exported"
+        assert name in sg.EXPORTS, f"{name} has no binding in the Python package"
+
+
+def test_status_and_variant_strings(lib):
+    assert sg.status_string(sg.OK) == "ok"
+    assert "timed out" in sg.status_string(sg.ERR_TIMEOUT)
+    assert sg.variant_name(sg.VARIANT_1SM_N128) == "1sm_n128"
+    assert sg.variant_name(99) == "?"
+
+
+def test_host_side_variant_choice(lib):
+    # 0.5B shape, M = 64: 1 x 38 tiles of 128 columns cannot fill 152 SMs
+    assert lib.swiglu_select_variant(64, 4864, 896, 0) == sg.VARIANT_1SM_N64
+    assert lib.swiglu_select_variant(8192, 4864, 896, 0) == sg.VARIANT_1SM_N128
+
+
+# Fake, never-dereferenced device addresses: validation is pure host arithmetic.
+A_, W1_, W2_, Y_ = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A_, W1_, W2_, Y_, -1, 64, 64), sg.ERR_INVALID_ARG),
+    ((A_, W1_, W2_, Y_, 64, -8, 64), sg.ERR_INVALID_ARG),
+    ((A_, W1_, W2_, None, 64, 64, 64), sg.ERR_INVALID_ARG),
+    ((None, W1_, W2_, Y_, 64, 64, 64), sg.ERR_INVALID_ARG),
+    ((A_, None, W2_, Y_, 64, 64, 64), sg.ERR_INVALID_ARG),
+    ((A_, W1_, None, Y_, 64, 64, 64), sg.ERR_INVALID_ARG),
+    ((A_ + 8, W1_, W2_, Y_, 64, 64, 64), sg.ERR_MISALIGNED),
+    ((A_, W1_, W2_, Y_ + 2, 64, 64, 64), sg.ERR_MISALIGNED),
+    ((A_, W1_, W2_, Y_, 64, 60, 64), sg.ERR_MISALIGNED),      # row pitch 120 B
+    ((A_, W1_, W2_, Y_, 64, 64, 36), sg.ERR_MISALIGNED),
+    ((A_, W1_, W2_, A_ + 64, 64, 64, 64), sg.ERR_INVALID_ARG),  # Y overlaps A
+    ((A_, W1_, W2_, W2_, 64, 64, 64), sg.ERR_INVALID_ARG),      # Y overlaps W2
+    ((A_, W1_, W2_, Y_, 1 << 31, 64, 64), sg.ERR_UNSUPPORTED),
+    ((A_, W1_, W2_, Y_, 0, 64, 64), sg.OK),                     # empty: nothing to do
+    ((A_, W1_, W2_, Y_, 64, 0, 64), sg.OK),
+])
+def test_fused_argument_validation(lib, args, want):
+    assert lib.swiglu_fused(*args, None) == want
+
+
+def test_bad_variant_rejected(lib):
+    assert lib.swiglu_fused_ex(A_, W1_, W2_, Y_, 64, 64, 64, 77, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_fused_interleaved_ex(A_, W1_, Y_, 64, 64, 64, -1, None) == sg.ERR_INVALID_ARG
+
+
+def test_interleaved_and_pack_validation(lib):
+    assert lib.swiglu_fused_interleaved(A_, None, Y_, 64, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_fused_interleaved(A_, W1_, W1_ + 16, 64, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_pack_interleaved(W1_, W2_, None, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_pack_interleaved(W1_, W2_, Y_ + 4, 64, 64, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_pack_interleaved(W1_, W2_, Y_, 64, 12, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_pack_interleaved(W1_, W2_, W1_, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_pack_interleaved(W1_, W2_, Y_, 0, 64, None) == sg.OK
+
+
+def test_timeout_setters_validate(lib):
+    assert lib.swiglu_set_wait_timeout_ns(10) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_set_wait_timeout_ns(2_000_000_000) == sg.OK
+    assert lib.swiglu_selftest_wait_timeout(0, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_selftest_wait_timeout(2_000_000, None) == sg.ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_a_device_reports_cuda_error(lib):
+    rc = lib.swiglu_fused(A_, W1_, W2_, Y_, 64, 64, 64, None)
+    assert rc in (sg.ERR_CUDA, sg.ERR_UNSUPPORTED)
+    detail = ctypes.c_uint32(7)
+    assert lib.swiglu_device_status(None, ctypes.byref(detail)) in (sg.ERR_CUDA, sg.ERR_UNSUPPORTED)
+    assert detail.value == 0
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    A = torch.zeros(8, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        sg.swiglu_fused(A, A, A)
