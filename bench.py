@@ -158,7 +158,7 @@ class ClockSampler:
 class Workload:
     """Device-resident inputs and the list of fused calls of one step."""
 
-    def __init__(self, name, dev, variant=0, forms=("separate", "interleaved")):
+    def __init__(self, name, dev, variant=0, forms=("separate", "interleaved"), only=None):
         import torch
         import swiglu_gemm_transformer_gb300 as sg
         import swiglu_inputs as si
@@ -179,6 +179,8 @@ class Workload:
         self.buffers = []
         for form in forms:
             for M in Ms:
+                if only is not None and (form, M) not in only:
+                    continue
                 A, W1, W2 = host[M]
                 Ad = A.to(dev)
                 Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -225,6 +227,45 @@ class Workload:
         return M * self.K * 2 + 2 * self.K * self.N * 2 + M * self.N * 2
 
 
+def measure_calls(wl, stream, launches):
+    """Average duration (us) of each call of the step, launched alone and back
+    to back inside a CUDA graph, rotating over copies of its inputs so that
+    the copies together exceed 2.5x the L2 size."""
+    import torch
+    out = []
+    for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
+        per = wl.algorithmic_bytes(M)
+        ncopy = max(2, min(24, math.ceil(2.5 * L2_BYTES / per)))
+        copies = [bufs] + [tuple(t.clone() for t in bufs) for _ in range(ncopy - 1)]
+        fns = []
+        for cb in copies:
+            if form == "separate":
+                p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr(), cb[3].data_ptr())
+                fns.append(lambda p=p, M=M, v=v: wl._sep(p, M, v))
+            else:
+                p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr())
+                fns.append(lambda p=p, M=M, v=v: wl._inter(p, M, v))
+        reps = max(1, math.ceil(launches / ncopy))
+
+        def body():
+            for _ in range(reps):
+                for f in fns:
+                    f()
+        with torch.cuda.stream(stream):
+            g = capture(body, stream)
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+        e1.synchronize()
+        out.append(1e3 * e0.elapsed_time(e1) / (reps * ncopy))
+        del g, copies, fns
+    torch.cuda.empty_cache()
+    return out
+
+
 def capture(fn, stream):
     import torch
     g = torch.cuda.CUDAGraph()
@@ -241,7 +282,10 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sg.lib()
-    wl = Workload(args.workload, dev, variant=sg.VARIANTS[args.variant])
+    only = None
+    if args.only:
+        only = {(f, int(m)) for f, m in (x.split(":") for x in args.only.split(","))}
+    wl = Workload(args.workload, dev, variant=sg.VARIANTS[args.variant], only=only)
     stream = torch.cuda.Stream(device=dev)
     n_calls = len(wl.calls)
 
@@ -253,20 +297,6 @@ def run_ours(args, ws, rank, local):
         if rc != sg.OK:
             raise RuntimeError(f"device status after warm-up: {sg.status_string(rc)} ({detail})")
         g_step = capture(wl.step, stream)
-
-        # instrumented copies of the step: an external timing event after each call
-        n_ev_graphs = 16
-        ev_graphs = []
-        for _ in range(n_ev_graphs):
-            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_calls + 1)]
-
-            def body(evs=evs):
-                evs[0].record()
-                for i, (_, _, _, fn) in enumerate(wl.calls):
-                    fn()
-                    evs[i + 1].record()
-            ev_graphs.append((capture(body, stream), evs))
-
         for _ in range(args.warmup):
             g_step.replay()
         stream.synchronize()
@@ -279,21 +309,10 @@ def run_ours(args, ws, rank, local):
     time.sleep(0.3)  # let the sampler take a baseline sample
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    per_call = [[] for _ in range(n_calls)]
     with torch.cuda.stream(stream):
         t_start.record()
-        done = 0
-        while done < args.steps:
-            batch = min(n_ev_graphs, args.steps - done)
-            for i in range(batch):
-                ev_graphs[i][0].replay()
-            # harvest this batch's per-call durations (the sync costs a few us per batch)
-            ev_graphs[batch - 1][1][-1].synchronize()
-            for i in range(batch):
-                evs = ev_graphs[i][1]
-                for c in range(n_calls):
-                    per_call[c].append(evs[c].elapsed_time(evs[c + 1]))
-            done += batch
+        for _ in range(args.steps):
+            g_step.replay()
         t_end.record()
     t_end.synchronize()
     torch.cuda.synchronize(dev)
@@ -305,16 +324,9 @@ def run_ours(args, ws, rank, local):
     if rc != sg.OK:
         raise RuntimeError(f"device status after timing: {sg.status_string(rc)} ({detail})")
 
-    # plain-graph timing of the same step (no events inside), for the overhead check
-    with torch.cuda.stream(stream):
-        p0 = torch.cuda.Event(enable_timing=True)
-        p1 = torch.cuda.Event(enable_timing=True)
-        p0.record()
-        for _ in range(args.steps):
-            g_step.replay()
-        p1.record()
-    p1.synchronize()
-    ms_plain = p0.elapsed_time(p1)
+    # Per-call launch durations: each call alone, launched back to back on
+    # rotating copies of its inputs (enough copies to exceed 2.5x L2), in a graph.
+    per_call_us = measure_calls(wl, stream, args.call_launches)
 
     t_max = ms_total
     if ws > 1:
@@ -329,7 +341,7 @@ def run_ours(args, ws, rank, local):
     peak_tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     kernels = []
     for c, (form, M, v, _) in enumerate(wl.calls):
-        us = statistics.mean(per_call[c]) * 1e3
+        us = per_call_us[c]
         flops = 4 * M * wl.N * wl.K
         abytes = wl.algorithmic_bytes(M)
         t_hbm = abytes / (peaks["hbm_gbs"] * 1e9)
@@ -373,15 +385,16 @@ def run_ours(args, ws, rank, local):
             "calls_per_step": n_calls,
             "l2": f"inputs larger than L2: each call has its own A, weights and Y; "
                   f"{wl.bytes_touched / 2**20:.0f} MiB per step vs {L2_BYTES / 2**20:.0f} MiB L2",
-            "timing": "CUDA graph of one step, external CUDA events after each call, "
-                      "max over ranks",
+            "timing": "CUDA graph of one step replayed back to back, CUDA events around the "
+                      "timed region, max over ranks; per-call durations from graphs of "
+                      "back-to-back launches of that call on rotating input copies",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
         "gpu_launches": n_calls * args.steps,
         "roofline": roof,
         "clocks": clocks,
         "kernels": kernels,
-        "timing_check": {"ms_per_step_plain_graph": round(ms_plain / args.steps, 5)},
+        "timing_check": {"sum_of_call_ms": round(sum(per_call_us) / 1e3, 5)},
     }
     return out, wl, stream
 
@@ -545,16 +558,21 @@ def run_reference(args, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", choices=("auto", "1sm_n128", "1sm_n64"), default="auto")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--call-launches", type=int, default=96,
+                    help="launches per call when timing calls one by one")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bounded CPU-oracle sample size for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="restrict the step to calls FORM:M[,FORM:M...] (profiling a single kernel)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -572,7 +590,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     try:
         out, wl, stream = run_ours(args, ws, rank, local)
-        out["e2e"] = run_e2e(args, wl, stream, ws)
+        out["e2e"] = None if args.no_e2e else run_e2e(args, wl, stream, ws)
         if not args.no_context:
             out["context_unfused_torch"] = run_unfused_context(wl, stream, min(args.steps, 200))
         if rank == 0:
