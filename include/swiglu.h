@@ -61,7 +61,10 @@ typedef enum {
     SWIGLU_VARIANT_1SM_N128 = 1,
     /* one CTA per SM, 128-row tiles, 64 output columns per tile (more tiles for small M) */
     SWIGLU_VARIANT_1SM_N64 = 2,
-    SWIGLU_VARIANT_COUNT_ = 3
+    /* CTA pair (2-CTA cluster, tcgen05 cta_group::2): 256-row tiles, 128 output
+       columns, each CTA streams A rows and one weight block (large M) */
+    SWIGLU_VARIANT_2SM_N128 = 3,
+    SWIGLU_VARIANT_COUNT_ = 4
 } swiglu_variant;
 
 /*

@@ -19,8 +19,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libswiglu_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
-VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64 = 0, 1, 2
-VARIANTS = {"auto": VARIANT_AUTO, "1sm_n128": VARIANT_1SM_N128, "1sm_n64": VARIANT_1SM_N64}
+VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64, VARIANT_2SM_N128 = 0, 1, 2, 3
+VARIANTS = {"auto": VARIANT_AUTO, "1sm_n128": VARIANT_1SM_N128, "1sm_n64": VARIANT_1SM_N64,
+            "2sm_n128": VARIANT_2SM_N128}
 
 EXPORTS = {
     # name: (argtypes, restype)

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "swiglu_tc_kernel.cuh"
+#include "tc_common.cuh"
 
 namespace swiglu {
 
@@ -20,8 +21,10 @@ struct LaunchArgs {
 
 // Tile geometry of each BF16 variant (SWIGLU_VARIANT_*), for host-side planning.
 struct VariantGeom {
-  int bm, bn, bk;     // output rows, output columns, K per stage
+  int bm, bn, bk;     // output rows, output columns, K per stage (per tile)
   int box_b;          // weight box width (columns) per TMA copy
+  int box_a;          // A box height (rows) per TMA copy
+  int cluster;        // CTAs per tile (1, or 2 for the CTA-pair kernel)
 };
 
 VariantGeom variant_geom(int variant);

@@ -4,6 +4,7 @@
 #include <atomic>
 
 #include "launch.h"
+#include "swiglu_tc2_kernel.cuh"
 
 namespace swiglu {
 
@@ -23,6 +24,44 @@ cudaError_t launch_tc(const LaunchArgs &la) {
   swiglu_bf16_tc_kernel<C><<<la.grid, C::THREADS, C::SMEM_BYTES, la.stream>>>(la.a, la.b0, la.b1,
                                                                                 la.y, la.p);
   return cudaGetLastError();
+}
+
+// CTA-pair kernel: 2-CTA clusters, persistent over as many clusters as can be
+// resident at once (queried once per device).
+template <class C>
+cudaError_t launch_pair(const LaunchArgs &la) {
+  static std::atomic<uint64_t> configured{0};
+  static int max_clusters[64] = {0};
+  const uint64_t bit = 1ull << (la.device & 63);
+  auto kern = swiglu_bf16_pair_kernel<C>;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = la.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * 64, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[la.device & 63] = n;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int64_t tiles = int64_t(la.p.num_m_blk) * la.p.num_n_blk;
+  const int n = max_clusters[la.device & 63];
+  const int clusters = int(tiles < n ? tiles : n);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
 }
 
 }  // namespace swiglu

@@ -105,6 +105,9 @@ int choose_variant(int64_t M, int64_t N, int64_t /*K*/, bool /*interleaved*/, in
   // width (the page's Kernel-2 argument: more thread blocks for small batches).
   const int64_t tiles128 = cdiv(M, 128) * cdiv(N, 128);
   if (tiles128 < sm_count) return SWIGLU_VARIANT_1SM_N64;
+  // Larger M: one 256x128 tile per CTA pair halves the weight bytes each SM
+  // streams per K step (32 KB instead of 48 KB).
+  if (M > 128) return SWIGLU_VARIANT_2SM_N128;
   return SWIGLU_VARIANT_1SM_N128;
 }
 
@@ -142,7 +145,7 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   LaunchArgs la;
   std::memset(&la, 0, sizeof la);
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  rc = encode_2d(&la.a, BF16, A, K, M, K * 2, g.bk, g.bm, CU_TENSOR_MAP_SWIZZLE_128B);
+  rc = encode_2d(&la.a, BF16, A, K, M, K * 2, g.bk, g.box_a, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == SWIGLU_OK) {
     if (interleaved) {
       rc = encode_2d(&la.b0, BF16, B0, 2 * N, K, 4 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -164,12 +167,13 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   p.num_m_blk = int32_t(cdiv(M, g.bm));
   p.num_n_blk = int32_t(cdiv(N, g.bn));
   p.num_k_blk = int32_t(cdiv(K, g.bk));
-  p.group_m = p.num_m_blk < 16 ? p.num_m_blk : 16;
+  const int gm = g.cluster == 2 ? 8 : 16;
+  p.group_m = p.num_m_blk < gm ? p.num_m_blk : gm;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
   const int64_t tiles = int64_t(p.num_m_blk) * p.num_n_blk;
   if (tiles > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
-  la.grid = int(tiles < st->sm_count ? tiles : st->sm_count);
+  la.grid = int(tiles < st->sm_count ? tiles : st->sm_count);  // one-CTA kernels
   la.device = dev;
   la.stream = s;
   cudaError_t e = interleaved ? launch_bf16_interleaved(variant, la)
@@ -184,10 +188,12 @@ namespace swiglu {
 VariantGeom variant_geom(int variant) {
   switch (variant) {
     case SWIGLU_VARIANT_1SM_N64:
-      return {128, 64, 64, 64};
+      return {128, 64, 64, 64, 128, 1};
+    case SWIGLU_VARIANT_2SM_N128:
+      return {256, 128, 64, 64, 128, 2};
     case SWIGLU_VARIANT_1SM_N128:
     default:
-      return {128, 128, 64, 64};
+      return {128, 128, 64, 64, 128, 1};
   }
 }
 
@@ -251,6 +257,7 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_AUTO: return "auto";
     case SWIGLU_VARIANT_1SM_N128: return "1sm_n128";
     case SWIGLU_VARIANT_1SM_N64: return "1sm_n64";
+    case SWIGLU_VARIANT_2SM_N128: return "2sm_n128";
     default: return "?";
   }
 }

@@ -1,0 +1,235 @@
+// swiglu_tc2_kernel.cuh -- the CTA-pair (cta_group::2) fused SwiGLU kernel.
+//
+// Same computation as the one-CTA kernel (page "Riepilogo Tecnico ...
+// Inferenza Efficiente di LLM", sections "Definizione del Problema" and
+// "Metodologia", items 1 and 2), with one output tile of 256 rows x 128
+// columns per pair of CTAs (a 2-CTA cluster on one TPC):
+//   * one tcgen05.mma.cta_group::2 M=256 x N=256 x K=16, issued by the even
+//     CTA, reads A rows [0,128) from the even CTA's shared memory and rows
+//     [128,256) from the odd CTA's, and weight columns [0,128) from the even
+//     CTA and [128,256) from the odd CTA.  In the separate form the even CTA
+//     therefore loads W1's 128-column block and the odd CTA W2's: each CTA
+//     streams A[128 x 64] + one weight block [64 x 128] = 32 KB per K step
+//     (48 KB for the one-CTA 128x256 tile), which is what lets the pair reach
+//     the tensor pipe's rate from L2;
+//   * each CTA's TMEM receives its own 128 rows x 256 columns (gate | up, or
+//     the interleaved pairs), double-buffered, so the epilogue is local;
+//   * the even CTA owns the "full" barriers (both CTAs' TMA copies count on
+//     them) and the "accumulator empty" barriers (all eight epilogue warps
+//     arrive there); MMA completion is multicast to both CTAs' "empty" and
+//     "accumulator full" barriers.
+// Waits are bounded as in the one-CTA kernel.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+#include "tc_common.cuh"
+
+namespace swiglu {
+
+template <bool INTERLEAVED_, int STAGES_>
+struct PairCfg {
+  static constexpr bool INTERLEAVED = INTERLEAVED_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int BM = 128;                 // rows per CTA (MMA M = 256 per pair)
+  static constexpr int BK = 64;
+  static constexpr int MMA_M = 256;
+  static constexpr int MMA_N = 256;              // gate+up columns per tile
+  static constexpr int BN = 128;                 // output columns per tile
+  static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+  static constexpr int ATOM_BYTES = BK * 128;    // 64 K-rows x 64 columns
+  static constexpr int B_ATOMS = 2;              // this CTA's 128 weight columns
+  static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int STG_BYTES = 32 * 64;
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC = ptx::idesc_bf16(MMA_M, MMA_N, false, true);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    swiglu_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB0,  // W1, or W_fused
+                            const __grid_constant__ CUtensorMap tmB1,  // W2 (separate form only)
+                            const __grid_constant__ CUtensorMap tmY, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw);
+
+  const uint32_t bars = base + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * C::STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0 = the pair's leader
+  const int cid = static_cast<int>(ptx::cluster_id_x());
+  const int ncl = static_cast<int>(ptx::num_clusters_x());
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(accf_bar(b), 1);
+      ptx::mbar_init(acce_bar(b), 2 * C::EPI_WARPS);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(rank == 0 || C::INTERLEAVED ? &tmB0 : &tmB1);
+    ptx::prefetch_tmap(&tmY);
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.num_m_blk * p.num_n_blk;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const CUtensorMap *tmB = (C::INTERLEAVED || rank == 0) ? &tmB0 : &tmB1;
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < num_tiles; t += ncl) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        const int arow = mb * 2 * C::BM + static_cast<int>(rank) * C::BM;
+        const int bcol = C::INTERLEAVED ? nb * C::MMA_N + static_cast<int>(rank) * 128 : nb * C::BN;
+        for (int kb = 0; kb < p.num_k_blk; ++kb) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
+                        WAIT_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+          ptx::tma_load_2d_pair(sa, &tmA, fb, kb * C::BK, arow);
+#pragma unroll
+          for (int j = 0; j < C::B_ATOMS; ++j)
+            ptx::tma_load_2d_pair(sb + j * C::ATOM_BYTES, tmB, fb, bcol + j * 64, kb * C::BK);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (ok) {
+        // Consume the MMA-completion arrivals still due on this CTA's "empty"
+        // barriers, so no multicast arrive targets this CTA after it exits.
+        const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
+        for (uint32_t i = issued - n; i < issued; ++i)
+          wait_quiet(empty_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
+      } else {
+        // Aborted: give copies already in flight into this CTA time to land.
+        spin_ns(100000);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < num_tiles; t += ncl) {
+        if (!wait_bar(acce_bar(abuf), aphase ^ 1u, p.timeout_ns, abort_flag, p.err,
+                      WAIT_MMA_ACC_EMPTY)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + abuf * C::MMA_N;
+        for (int kb = 0; kb < p.num_k_blk; ++kb) {
+          if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
+            const uint64_t bdesc =
+                ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
+            ptx::mma_f16_pair(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_mc(accf_bar(abuf), 0x3);
+        if (++abuf == 2) {
+          abuf = 0;
+          aphase ^= 1u;
+        }
+      }
+      ptx::mma_commit_pair_mc(drain_bar, 0x1);
+      wait_quiet(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3, both CTAs)
+    const int q = warp;
+    const uint32_t stg_base = base + C::STG_OFF + q * 2 * C::STG_BYTES;
+    uint32_t abuf = 0, aphase = 0, it = 0;
+    for (int t = cid; t < num_tiles; t += ncl) {
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      bool ok = wait_bar(accf_bar(abuf), aphase, p.timeout_ns, abort_flag, p.err,
+                         WAIT_EPI_ACC_FULL);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
+      const int row0 = mb * 2 * C::BM + static_cast<int>(rank) * C::BM + q * 32;
+      epilogue_tile<C::INTERLEAVED, C::BN>(tacc, row0, nb * C::BN, &tmY, p.M, p.N, smem, base,
+                                           stg_base, it, lane,
+                                           ptx::mapa_shared(acce_bar(abuf), 0));
+      if (++abuf == 2) {
+        abuf = 0;
+        aphase ^= 1u;
+      }
+    }
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace swiglu

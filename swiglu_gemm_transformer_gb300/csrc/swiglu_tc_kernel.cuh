@@ -39,29 +39,9 @@
 #include <stdint.h>
 
 #include "sm103_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace swiglu {
-
-// Where a wait gave up (device error word, second slot).
-enum : uint32_t {
-  WAIT_PRODUCER_EMPTY = 1,
-  WAIT_MMA_FULL = 2,
-  WAIT_MMA_ACC_EMPTY = 3,
-  WAIT_EPI_ACC_FULL = 4,
-  WAIT_DRAIN = 5,
-  WAIT_SELFTEST = 6,
-};
-
-constexpr uint32_t kErrTimeout = 5;  // == SWIGLU_ERR_TIMEOUT
-
-struct KParams {
-  int32_t M, N, K;
-  int32_t num_m_blk, num_n_blk, num_k_blk;
-  int32_t group_m;       // grouped raster: this many m-blocks walk the n-blocks together
-  int32_t pad_;
-  uint64_t timeout_ns;   // limit of every mbarrier wait
-  uint32_t *err;         // device error word: [0] = status, [1] = where
-};
 
 template <int NB_ATOMS_, bool INTERLEAVED_, int STAGES_>
 struct TileCfg {
@@ -88,50 +68,6 @@ struct TileCfg {
   static_assert(NB_ATOMS == 2 || NB_ATOMS == 4, "MMA N of 128 or 256");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
-
-// Bounded wait, slow path.  Returns false on timeout or when another role of
-// this CTA already gave up.
-__device__ __noinline__ static bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int *abort_flag, uint32_t *err,
-                                              uint32_t where) {
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > limit_ns) {
-      *abort_flag = 1;
-      if (atomicCAS(err, 0u, kErrTimeout) == 0u) atomicExch(err + 1, where);
-      __threadfence();
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ static bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                volatile int *abort_flag, uint32_t *err,
-                                                uint32_t where) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, limit_ns, abort_flag, err, where);
-}
-
-__device__ __forceinline__ static void tile_coords(int t, const KParams &p, int &mb, int &nb) {
-  const int per_group = p.group_m * p.num_n_blk;
-  const int g = t / per_group;
-  const int first = g * p.group_m;
-  const int rows = min(p.group_m, p.num_m_blk - first);
-  const int r = t - g * per_group;
-  mb = first + r % rows;
-  nb = r / rows;
-}
-
-__device__ __forceinline__ static float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
-__device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -302,66 +238,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
-      const int row0 = mb * C::BM + q * 32;
-#pragma unroll 1
-      for (int c = 0; c < C::BN / 32; ++c) {
-        uint32_t g[32], u[32];
-        if (C::INTERLEAVED) {
-          ptx::tmem_ld32(trow + c * 64, g);
-          ptx::tmem_ld32(trow + c * 64 + 32, u);
-        } else {
-          ptx::tmem_ld32(trow + c * 32, g);
-          ptx::tmem_ld32(trow + C::BN + c * 32, u);
-        }
-        ptx::tmem_wait_ld();
-        ptx::reg_fence(g);
-        ptx::reg_fence(u);
-        if (c == C::BN / 32 - 1) {
-          // This warp is done reading the accumulator buffer.
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(acce_bar(abuf));
-        }
-        uint32_t packed[16];
-        if (C::INTERLEAVED) {
-          // g holds TMEM columns 64c..64c+31 = pairs (gate, up) for outputs 32c..32c+15,
-          // u holds the pairs for outputs 32c+16..32c+31.
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            packed[i] = pack_bf16x2(
-                silu_mul(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1])),
-                silu_mul(__uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3])));
-            packed[8 + i] = pack_bf16x2(
-                silu_mul(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1])),
-                silu_mul(__uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[i] = pack_bf16x2(
-                silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-        }
-        const int col0 = nb * C::BN + c * 32;
-        const uint32_t stg = stg_base + (it & 1u) * C::STG_BYTES;
-        // The store issued from this buffer two blocks ago must have finished reading it.
-        if (lane == 0) ptx::bulk_wait_read<1>();
-        __syncwarp();
-        uint4 *rowp = reinterpret_cast<uint4 *>(smem + (stg - base) + lane * 64);
-        const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk i -> i ^ ((row >> 1) & 3)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          rowp[i ^ sw] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                    packed[4 * i + 3]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < p.M && col0 < p.N) {
-          ptx::tma_store_2d(&tmY, stg, col0, row0);
-        }
-        if (lane == 0) ptx::bulk_commit();
-        ++it;
-      }
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
+      epilogue_tile<C::INTERLEAVED, C::BN>(tacc, mb * C::BM + q * 32, nb * C::BN, &tmY, p.M, p.N,
+                                           smem, base, stg_base, it, lane, acce_bar(abuf));
       if (++abuf == 2) {
         abuf = 0;
         aphase ^= 1u;

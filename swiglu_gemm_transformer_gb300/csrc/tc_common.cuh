@@ -1,0 +1,171 @@
+// tc_common.cuh -- pieces shared by the one-CTA and CTA-pair fused SwiGLU
+// kernels: launch parameters, bounded mbarrier waits, the tile order, and the
+// epilogue that turns a (gate, up) accumulator tile in TMEM into BF16 Y.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+
+namespace swiglu {
+
+// Where a wait gave up (device error word, second slot).
+enum : uint32_t {
+  WAIT_PRODUCER_EMPTY = 1,
+  WAIT_MMA_FULL = 2,
+  WAIT_MMA_ACC_EMPTY = 3,
+  WAIT_EPI_ACC_FULL = 4,
+  WAIT_DRAIN = 5,
+  WAIT_SELFTEST = 6,
+};
+
+constexpr uint32_t kErrTimeout = 5;  // == SWIGLU_ERR_TIMEOUT
+
+struct KParams {
+  int32_t M, N, K;
+  int32_t num_m_blk, num_n_blk, num_k_blk;
+  int32_t group_m;       // grouped raster: this many m-blocks walk the n-blocks together
+  int32_t pad_;
+  uint64_t timeout_ns;   // limit of every mbarrier wait
+  uint32_t *err;         // device error word: [0] = status, [1] = where
+};
+
+// Bounded wait, slow path.  Returns false on timeout or when another role of
+// this CTA already gave up.
+__device__ __noinline__ static bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag, uint32_t *err,
+                                              uint32_t where) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      if (atomicCAS(err, 0u, kErrTimeout) == 0u) atomicExch(err + 1, where);
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ static bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                volatile int *abort_flag, uint32_t *err,
+                                                uint32_t where) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, limit_ns, abort_flag, err, where);
+}
+
+// Bounded wait that records nothing (used while draining after an abort).
+__device__ __forceinline__ static void wait_quiet(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < limit_ns) {
+  }
+}
+
+// Spin for `ns` nanoseconds (bounded), letting in-flight copies land.
+__device__ __forceinline__ static void spin_ns(uint64_t ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ptx::globaltimer_ns() - t0 < ns) {
+  }
+}
+
+// Grouped tile order: `group_m` m-blocks walk all n-blocks together, so tiles
+// that run at the same time share A rows and weight columns in L2.
+__device__ __forceinline__ static void tile_coords(int t, const KParams &p, int &mb, int &nb) {
+  const int per_group = p.group_m * p.num_n_blk;
+  const int g = t / per_group;
+  const int first = g * p.group_m;
+  const int rows = min(p.group_m, p.num_m_blk - first);
+  const int r = t - g * per_group;
+  mb = first + r % rows;
+  nb = r / rows;
+}
+
+// SiLU(g) * u = g * u / (1 + e^-g), FP32.
+__device__ __forceinline__ static float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Epilogue of one accumulator tile, for one warp (32 TMEM lanes = 32 rows).
+//   tacc      : TMEM address of this warp's lanes at the tile's first column;
+//               separate form: columns [0,BN) gate, [BN,2BN) up;
+//               interleaved form: column 2j gate j, 2j+1 up j.
+//   row0/col0 : Y coordinates of the warp's first row and the tile's first column.
+//   stg_base  : this warp's two 2 KB staging buffers (shared::cta address).
+//   it        : running staging-buffer counter of this warp.
+//   release   : cluster address of the barrier to arrive on once the warp has
+//               read the whole accumulator (frees the TMEM buffer for the MMA).
+template <bool INTERLEAVED, int BN>
+__device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, int col0,
+                                                     const CUtensorMap *tmY, int M, int N,
+                                                     uint8_t *smem, uint32_t smem_base,
+                                                     uint32_t stg_base, uint32_t &it, int lane,
+                                                     uint32_t release) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t g[32], u[32];
+    if (INTERLEAVED) {
+      ptx::tmem_ld32(tacc + c * 64, g);
+      ptx::tmem_ld32(tacc + c * 64 + 32, u);
+    } else {
+      ptx::tmem_ld32(tacc + c * 32, g);
+      ptx::tmem_ld32(tacc + BN + c * 32, u);
+    }
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(g);
+    ptx::reg_fence(u);
+    if (c == BN / 32 - 1) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(release);
+    }
+    uint32_t packed[16];
+    if (INTERLEAVED) {
+      // g: columns 64c..64c+31 = (gate, up) pairs of outputs 32c..32c+15;
+      // u: the pairs of outputs 32c+16..32c+31.
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        packed[i] =
+            pack_bf16x2(silu_mul(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1])),
+                        silu_mul(__uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3])));
+        packed[8 + i] =
+            pack_bf16x2(silu_mul(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1])),
+                        silu_mul(__uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        packed[i] =
+            pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                        silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+    }
+    const int ccol = col0 + c * 32;
+    const uint32_t stg = stg_base + (it & 1u) * 2048u;
+    // The store issued from this buffer two blocks ago must have finished reading it.
+    if (lane == 0) ptx::bulk_wait_read<1>();
+    __syncwarp();
+    uint4 *rowp = reinterpret_cast<uint4 *>(smem + (stg - smem_base) + lane * 64);
+    const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk i -> i ^ ((row >> 1) & 3)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      rowp[i ^ sw] =
+          make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (row0 < M && ccol < N) ptx::tma_store_2d(tmY, stg, ccol, row0);
+      ptx::bulk_commit();
+    }
+    ++it;
+  }
+}
+
+}  // namespace swiglu

@@ -43,13 +43,14 @@ def test_status_and_variant_strings(lib):
     assert sg.status_string(sg.OK) == "ok"
     assert "timed out" in sg.status_string(sg.ERR_TIMEOUT)
     assert sg.variant_name(sg.VARIANT_1SM_N128) == "1sm_n128"
+    assert sg.variant_name(sg.VARIANT_2SM_N128) == "2sm_n128"
     assert sg.variant_name(99) == "?"
 
 
 def test_host_side_variant_choice(lib):
     # 0.5B shape, M = 64: 1 x 38 tiles of 128 columns cannot fill 152 SMs
     assert lib.swiglu_select_variant(64, 4864, 896, 0) == sg.VARIANT_1SM_N64
-    assert lib.swiglu_select_variant(8192, 4864, 896, 0) == sg.VARIANT_1SM_N128
+    assert lib.swiglu_select_variant(8192, 4864, 896, 0) == sg.VARIANT_2SM_N128
 
 
 # Fake, never-dereferenced device addresses: validation is pure host arithmetic.
