@@ -44,6 +44,7 @@ WORKLOADS = {
     "qwen2.5-0.5b-m64": (896, 4864, (64,), 0),
     "qwen2.5-7b": (3584, 18944, (256, 1024, 2048, 4096), 2),
     "qwen2.5-72b": (8192, 29568, (2048, 8192, 16384), 3),
+    "qwen2.5-7b-fp8": (3584, 18944, (512, 4096), 4),
 }
 DEFAULT_WORKLOAD = "qwen2.5-0.5b"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -171,15 +172,24 @@ class Workload:
         self.bytes_touched = 0
         self.flops = 0
         lib = sg.lib()
+        self.fp8 = name.endswith("-fp8")
+        self.eb = 1 if self.fp8 else 2
         host = {}
         for M in Ms:
-            A, W1, W2 = si.make_bf16(M, N, K, seed)
-            host[M] = (A, W1, W2)
+            if self.fp8:
+                q, sc = si.make_e4m3(M, N, K, seed)
+                host[M] = (q[0], q[1].t().contiguous(), q[2].t().contiguous(), sc)
+            else:
+                A, W1, W2 = si.make_bf16(M, N, K, seed)
+                host[M] = (A, W1, W2)
         self.host = host
         self.buffers = []
         for form in forms:
             for M in Ms:
                 if only is not None and (form, M) not in only:
+                    continue
+                if self.fp8:
+                    self._add_fp8(form, M, host[M], dev)
                     continue
                 A, W1, W2 = host[M]
                 Ad = A.to(dev)
@@ -205,6 +215,42 @@ class Workload:
                 self.flops += 4 * M * N * K
         torch.cuda.synchronize(dev)
 
+    def _add_fp8(self, form, M, h, dev):
+        import torch
+        sg = self.sg
+        K, N = self.K, self.N
+        Aq, W1t, W2t, sc = h
+        Ad = Aq.to(dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        s = torch.tensor(list(sc), dtype=torch.float32, device=dev)
+        sp = (s.data_ptr(), s.data_ptr() + 4, s.data_ptr() + 8)
+        W1d, W2d = W1t.to(dev), W2t.to(dev)
+        if form == "separate":
+            ptrs = (Ad.data_ptr(), W1d.data_ptr(), W2d.data_ptr(), Y.data_ptr())
+            fn = (lambda p=ptrs, M=M: self._fp8_sep(p, sp, M))
+            self.buffers.append((Ad, W1d, W2d, Y, s))
+        else:
+            Wf = sg.swiglu_pack_interleaved_fp8(W1d, W2d)
+            del W1d, W2d
+            ptrs = (Ad.data_ptr(), Wf.data_ptr(), Y.data_ptr())
+            fn = (lambda p=ptrs, M=M: self._fp8_inter(p, sp, M))
+            self.buffers.append((Ad, Wf, Y, s))
+        self.calls.append((form, M, -1, fn))
+        self.bytes_touched += M * K + 2 * K * N + M * N * 2
+        self.flops += 4 * M * N * K
+
+    def _fp8_sep(self, p, sp, M):
+        rc = self.sg.lib().swiglu_fused_fp8(p[0], p[1], p[2], sp[0], sp[1], sp[2], p[3], M, self.N,
+                                            self.K, self._stream())
+        if rc:
+            raise self.sg.SwigluError("swiglu_fused_fp8", rc)
+
+    def _fp8_inter(self, p, sp, M):
+        rc = self.sg.lib().swiglu_fused_interleaved_fp8(p[0], p[1], sp[0], sp[1], sp[2], p[2], M,
+                                                        self.N, self.K, self._stream())
+        if rc:
+            raise self.sg.SwigluError("swiglu_fused_interleaved_fp8", rc)
+
     def _stream(self):
         import torch
         return torch.cuda.current_stream().cuda_stream
@@ -224,7 +270,7 @@ class Workload:
             fn()
 
     def algorithmic_bytes(self, M):
-        return M * self.K * 2 + 2 * self.K * self.N * 2 + M * self.N * 2
+        return self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
 
 
 def measure_calls(wl, stream, launches):
@@ -239,7 +285,16 @@ def measure_calls(wl, stream, launches):
         copies = [bufs] + [tuple(t.clone() for t in bufs) for _ in range(ncopy - 1)]
         fns = []
         for cb in copies:
-            if form == "separate":
+            if wl.fp8:
+                sd = cb[-1].data_ptr()
+                sp = (sd, sd + 4, sd + 8)
+                if form == "separate":
+                    p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr(), cb[3].data_ptr())
+                    fns.append(lambda p=p, sp=sp, M=M: wl._fp8_sep(p, sp, M))
+                else:
+                    p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr())
+                    fns.append(lambda p=p, sp=sp, M=M: wl._fp8_inter(p, sp, M))
+            elif form == "separate":
                 p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr(), cb[3].data_ptr())
                 fns.append(lambda p=p, M=M, v=v: wl._sep(p, M, v))
             else:
@@ -339,6 +394,8 @@ def run_ours(args, ws, rank, local):
     peaks, peak_src = load_peaks()
     sustained = t_max > 1000.0
     peak_tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    if wl.fp8:
+        peak_tf *= 2.0  # dense FP8 = 2x dense BF16 (nominal 4.5 vs 2.25 PFLOP/s)
     kernels = []
     for c, (form, M, v, _) in enumerate(wl.calls):
         us = per_call_us[c]
@@ -350,7 +407,8 @@ def run_ours(args, ws, rank, local):
         achieved_tf = flops / (us * 1e-6) / 1e12
         achieved_gbs = abytes / (us * 1e-6) / 1e9
         kernels.append({
-            "form": form, "M": M, "variant": sg.variant_name(v), "us": round(us, 3),
+            "form": form, "M": M, "variant": "2sm_fp8" if wl.fp8 else sg.variant_name(v),
+            "us": round(us, 3),
             "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
             "frac_of_roofline": round(max(t_tc, t_hbm) / (us * 1e-6), 4),
             "share": 0.0,
@@ -361,7 +419,7 @@ def run_ours(args, ws, rank, local):
     dom = max(range(n_calls), key=lambda i: kernels[i]["us"])
     dk = kernels[dom]
     form, M, v, _ = wl.calls[dom]
-    kernel_key = f"{wl.name}:{form}:M{M}:{sg.variant_name(v)}"
+    kernel_key = f"{wl.name}:{form}:M{M}:{dk['variant']}"
     if dk["bound"] == "tensor":
         roof = {"bound": "tensor", "achieved": dk["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(dk["tflops"] / peak_tf, 4)}
@@ -372,12 +430,14 @@ def run_ours(args, ws, rank, local):
     roof["kernel"] = kernel_key
     roof["algorithmic_per_launch"] = (4 * M * wl.N * wl.K if dk["bound"] == "tensor"
                                       else wl.algorithmic_bytes(M))
-    roof["peak_source"] = f"{peak_src} ({'sustained' if sustained and dk['bound'] == 'tensor' else 'burst'})"
+    roof["peak_source"] = (f"{peak_src} ({'sustained' if sustained and dk['bound'] == 'tensor' else 'burst'})"
+                           + (", x2 for FP8" if wl.fp8 and dk["bound"] == "tensor" else ""))
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3" if wl.fp8 else "bf16",
+        "data": "synthetic",
         "impl": "ours",
         "config": {
             "workload": f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
@@ -413,14 +473,21 @@ def run_e2e(args, wl, stream, ws):
         host_a.append(A_host)
         host_y.append(Y_host)
         dev_bufs.append(bufs)
-        h2d += A_host.numel() * 2
+        h2d += A_host.numel() * wl.eb
         d2h += Y_host.numel() * 2
 
     def step():
         for (form, M, v, _), A_h, Y_h, bufs in zip(wl.calls, host_a, host_y, dev_bufs):
             Ad = bufs[0]
             Ad.copy_(A_h, non_blocking=True)
-            if form == "separate":
+            if wl.fp8:
+                sc = bufs[-1]
+                s3 = (sc[0:1], sc[1:2], sc[2:3])
+                if form == "separate":
+                    Y = sg.swiglu_fused_fp8(Ad, bufs[1], bufs[2], *s3, bufs[3])
+                else:
+                    Y = sg.swiglu_fused_interleaved_fp8(Ad, bufs[1], *s3, bufs[2])
+            elif form == "separate":
                 Y = sg.swiglu_fused(Ad, bufs[1], bufs[2], bufs[3], variant=v)
             else:
                 Y = sg.swiglu_fused_interleaved(Ad, bufs[1], bufs[2], variant=v)
@@ -454,6 +521,8 @@ def run_unfused_context(wl, stream, steps):
     """Context only: the unfused eager path (two cuBLAS GEMMs, SiLU, multiply) on the same inputs."""
     import torch
     import torch.nn.functional as F
+    if wl.fp8:
+        return None
 
     def step():
         for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
@@ -562,7 +631,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--variant", choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128"), default="auto")
+    ap.add_argument("--variant", choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32"), default="auto")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--call-launches", type=int, default=96,
                     help="launches per call when timing calls one by one")

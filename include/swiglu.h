@@ -64,7 +64,10 @@ typedef enum {
     /* CTA pair (2-CTA cluster, tcgen05 cta_group::2): 256-row tiles, 128 output
        columns, each CTA streams A rows and one weight block (large M) */
     SWIGLU_VARIANT_2SM_N128 = 3,
-    SWIGLU_VARIANT_COUNT_ = 4
+    /* one CTA per SM, 128-row tiles, 32 output columns per tile (small M: one
+       tile per SM for N = 4864 on 152 SMs) */
+    SWIGLU_VARIANT_1SM_N32 = 4,
+    SWIGLU_VARIANT_COUNT_ = 5
 } swiglu_variant;
 
 /*
@@ -100,6 +103,39 @@ int swiglu_fused_interleaved(const void *A, const void *Wfused, void *Y,
  */
 int swiglu_pack_interleaved(const void *W1, const void *W2, void *Wfused,
                             int64_t K, int64_t N, void *stream);
+
+/*
+ * FP8 E4M3 operands with per-tensor scales (page section "Definizione del
+ * Problema": quantisation to FP8 raises tensor-core density, which makes the
+ * memory-bound gate/up traffic matter more).  The value of an operand element
+ * is code * scale; the result is the same definition on those values,
+ *     Y = SiLU(sA*sW1 * (Aq x W1q)) (.) (sA*sW2 * (Aq x W2q)),
+ * with FP32 accumulation and BF16 Y.  FP8 weights are taken K-major, i.e. as
+ * the [N,K] row-major transpose of the [K,N] weights of the BF16 entry points
+ * (each output column's K weights contiguous), the layout quantised
+ * checkpoints use.
+ *   Aq       : device, E4M3 [M,K] row-major  (read)
+ *   W1t, W2t : device, E4M3 [N,K] row-major  (read)
+ *   sA, sW1, sW2 : device pointers to one float each (read at kernel time)
+ *   Y        : device, BF16 [M,N] row-major  (written)
+ * K must be a multiple of 16 and N of 8; pointers 16-byte aligned.
+ */
+int swiglu_fused_fp8(const void *Aq, const void *W1t, const void *W2t, const float *sA,
+                     const float *sW1, const float *sW2, void *Y, int64_t M, int64_t N,
+                     int64_t K, void *stream);
+
+/* The interleaved form with FP8 operands: Wfused_t [2N,K] row-major, row 2n =
+ * gate row n (scale sW1), row 2n+1 = up row n (scale sW2), as made by
+ * swiglu_pack_interleaved_fp8. */
+int swiglu_fused_interleaved_fp8(const void *Aq, const void *Wfused_t, const float *sA,
+                                 const float *sW1, const float *sW2, void *Y, int64_t M,
+                                 int64_t N, int64_t K, void *stream);
+
+/* Packer for the FP8 interleaved form, K-major: Wfused_t[2n,:] = W1t[n,:],
+ * Wfused_t[2n+1,:] = W2t[n,:] (the column interleave of the page's Kernel-2
+ * in transposed storage).  W1t, W2t: E4M3 [N,K]; Wfused_t: E4M3 [2N,K]. */
+int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t, int64_t N,
+                                int64_t K, void *stream);
 
 /* swiglu_fused / swiglu_fused_interleaved with an explicit variant
  * (SWIGLU_VARIANT_*) instead of the library's choice; for sweeps and tests. */

@@ -19,9 +19,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libswiglu_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
-VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64, VARIANT_2SM_N128 = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64, VARIANT_2SM_N128, VARIANT_1SM_N32 = range(5)
 VARIANTS = {"auto": VARIANT_AUTO, "1sm_n128": VARIANT_1SM_N128, "1sm_n64": VARIANT_1SM_N64,
-            "2sm_n128": VARIANT_2SM_N128}
+            "2sm_n128": VARIANT_2SM_N128, "1sm_n32": VARIANT_1SM_N32}
 
 EXPORTS = {
     # name: (argtypes, restype)
@@ -30,6 +30,9 @@ EXPORTS = {
     "swiglu_fused_interleaved": ("ppp lll p", ctypes.c_int),
     "swiglu_fused_interleaved_ex": ("ppp lll i p", ctypes.c_int),
     "swiglu_pack_interleaved": ("ppp ll p", ctypes.c_int),
+    "swiglu_fused_fp8": ("ppp ppp p lll p", ctypes.c_int),
+    "swiglu_fused_interleaved_fp8": ("pp ppp p lll p", ctypes.c_int),
+    "swiglu_pack_interleaved_fp8": ("ppp ll p", ctypes.c_int),
     "swiglu_select_variant": ("lll i", ctypes.c_int),
     "swiglu_variant_name": ("i", ctypes.c_char_p),
     "swiglu_status_string": ("i", ctypes.c_char_p),
@@ -166,6 +169,79 @@ def swiglu_pack_interleaved(W1, W2, Wfused=None, *, stream=None):
                                        _stream(stream))
     _check("swiglu_pack_interleaved", rc)
     return Wfused
+
+
+def _fp8(t, name, ndim=2):
+    import torch
+    return _need(t, name, torch.float8_e4m3fn, ndim)
+
+
+def _scale(s, name):
+    import torch
+    if not isinstance(s, torch.Tensor) or not s.is_cuda or s.dtype != torch.float32 or s.numel() != 1:
+        raise TypeError(f"{name} must be a one-element float32 CUDA tensor")
+    return s.data_ptr()
+
+
+def swiglu_fused_fp8(Aq, W1t, W2t, sA, sW1, sW2, Y=None, *, stream=None):
+    """Y = SiLU(sA*sW1 * Aq@W1t.T) * (sA*sW2 * Aq@W2t.T); Aq [M,K], W1t/W2t [N,K] E4M3."""
+    import torch
+    _fp8(Aq, "Aq"), _fp8(W1t, "W1t"), _fp8(W2t, "W2t")
+    M, K = Aq.shape
+    N = W1t.shape[0]
+    if W1t.shape[1] != K or W2t.shape != W1t.shape:
+        raise ValueError(f"shape mismatch: Aq {tuple(Aq.shape)}, W1t {tuple(W1t.shape)}, W2t {tuple(W2t.shape)}")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=Aq.device)
+    else:
+        _need(Y, "Y", torch.bfloat16)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [M, N]")
+    rc = lib().swiglu_fused_fp8(Aq.data_ptr(), W1t.data_ptr(), W2t.data_ptr(), _scale(sA, "sA"),
+                                _scale(sW1, "sW1"), _scale(sW2, "sW2"), Y.data_ptr(), M, N, K,
+                                _stream(stream))
+    _check("swiglu_fused_fp8", rc)
+    return Y
+
+
+def swiglu_fused_interleaved_fp8(Aq, Wfused_t, sA, sW1, sW2, Y=None, *, stream=None):
+    """FP8 interleaved form: Wfused_t [2N,K] (even rows gate, odd rows up)."""
+    import torch
+    _fp8(Aq, "Aq"), _fp8(Wfused_t, "Wfused_t")
+    M, K = Aq.shape
+    if Wfused_t.shape[1] != K or Wfused_t.shape[0] % 2:
+        raise ValueError(f"shape mismatch: Aq {tuple(Aq.shape)}, Wfused_t {tuple(Wfused_t.shape)}")
+    N = Wfused_t.shape[0] // 2
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=Aq.device)
+    else:
+        _need(Y, "Y", torch.bfloat16)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [M, N]")
+    rc = lib().swiglu_fused_interleaved_fp8(Aq.data_ptr(), Wfused_t.data_ptr(), _scale(sA, "sA"),
+                                            _scale(sW1, "sW1"), _scale(sW2, "sW2"), Y.data_ptr(),
+                                            M, N, K, _stream(stream))
+    _check("swiglu_fused_interleaved_fp8", rc)
+    return Y
+
+
+def swiglu_pack_interleaved_fp8(W1t, W2t, Wfused_t=None, *, stream=None):
+    """Wfused_t[2n,:] = W1t[n,:], Wfused_t[2n+1,:] = W2t[n,:] (E4M3, K-major)."""
+    import torch
+    _fp8(W1t, "W1t"), _fp8(W2t, "W2t")
+    if W1t.shape != W2t.shape:
+        raise ValueError("W1t and W2t must match in shape")
+    N, K = W1t.shape
+    if Wfused_t is None:
+        Wfused_t = torch.empty((2 * N, K), dtype=W1t.dtype, device=W1t.device)
+    else:
+        _fp8(Wfused_t, "Wfused_t")
+        if tuple(Wfused_t.shape) != (2 * N, K):
+            raise ValueError("Wfused_t must be [2N, K]")
+    rc = lib().swiglu_pack_interleaved_fp8(W1t.data_ptr(), W2t.data_ptr(), Wfused_t.data_ptr(),
+                                           N, K, _stream(stream))
+    _check("swiglu_pack_interleaved_fp8", rc)
+    return Wfused_t
 
 
 def swiglu_select_variant(M: int, N: int, K: int, interleaved: bool = False) -> int:

@@ -23,16 +23,20 @@ struct LaunchArgs {
 struct VariantGeom {
   int bm, bn, bk;     // output rows, output columns, K per stage (per tile)
   int box_b;          // weight box width (columns) per TMA copy
+  int b_swizzle_64;   // 1: weight boxes use the 64-byte swizzle (32-column boxes)
   int box_a;          // A box height (rows) per TMA copy
   int cluster;        // CTAs per tile (1, or 2 for the CTA-pair kernel)
 };
 
-VariantGeom variant_geom(int variant);
+VariantGeom variant_geom(int variant, bool interleaved);
 
 cudaError_t launch_bf16_separate(int variant, const LaunchArgs &la);
 cudaError_t launch_bf16_interleaved(int variant, const LaunchArgs &la);
 cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf, int64_t n_elems,
                                         int sm_count, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t *err, cudaStream_t s);
+cudaError_t launch_fp8(bool interleaved, const LaunchArgs &la);
+cudaError_t launch_pack_rows_interleaved_u8(const void *W1t, const void *W2t, void *Wft,
+                                            int64_t N, int64_t K, int sm_count, cudaStream_t s);
 
 }  // namespace swiglu

@@ -8,22 +8,37 @@
 
 namespace swiglu {
 
+// Launch attributes shared by every fused kernel: programmatic dependent
+// launch (the prologue may overlap the previous kernel on the stream; the
+// kernel waits on griddepcontrol.wait before touching global memory).
+inline void pdl_attr(cudaLaunchAttribute &a) {
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+}
+
 template <class C>
 cudaError_t launch_tc(const LaunchArgs &la) {
   // The dynamic shared-memory opt-in is a per-device function attribute; set it
   // once per device.
   static std::atomic<uint64_t> configured{0};
   const uint64_t bit = 1ull << (la.device & 63);
+  auto kern = swiglu_bf16_tc_kernel<C>;
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(swiglu_bf16_tc_kernel<C>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  swiglu_bf16_tc_kernel<C><<<la.grid, C::THREADS, C::SMEM_BYTES, la.stream>>>(la.a, la.b0, la.b1,
-                                                                                la.y, la.p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_attr(attr[0]);
+  cfg.gridDim = dim3(la.grid, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = la.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
 }
 
 // CTA-pair kernel: 2-CTA clusters, persistent over as many clusters as can be
@@ -35,16 +50,17 @@ cudaError_t launch_pair(const LaunchArgs &la) {
   const uint64_t bit = 1ull << (la.device & 63);
   auto kern = swiglu_bf16_pair_kernel<C>;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  pdl_attr(attr[1]);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = la.stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
@@ -61,6 +77,7 @@ cudaError_t launch_pair(const LaunchArgs &la) {
   const int n = max_clusters[la.device & 63];
   const int clusters = int(tiles < n ? tiles : n);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
 }
 

@@ -286,6 +286,17 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
+// Pair MMA, kind::f8f6f4 (8-bit float inputs), same operand split as above.
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask` when
 // all tcgen05 ops issued so far by this thread complete.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {

@@ -101,14 +101,14 @@ int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int choose_variant(int64_t M, int64_t N, int64_t /*K*/, bool /*interleaved*/, int sm_count) {
-  // Small M: too few 128-column tiles to occupy every SM, so halve the tile
-  // width (the page's Kernel-2 argument: more thread blocks for small batches).
-  const int64_t tiles128 = cdiv(M, 128) * cdiv(N, 128);
-  if (tiles128 < sm_count) return SWIGLU_VARIANT_1SM_N64;
   // Larger M: one 256x128 tile per CTA pair halves the weight bytes each SM
   // streams per K step (32 KB instead of 48 KB).
   if (M > 128) return SWIGLU_VARIANT_2SM_N128;
-  return SWIGLU_VARIANT_1SM_N128;
+  // Small M (one 128-row block): narrow the tiles until they occupy every SM
+  // (the page's Kernel-2 argument: more thread blocks for small batches).
+  if (cdiv(N, 128) >= sm_count) return SWIGLU_VARIANT_1SM_N128;
+  if (cdiv(N, 64) >= sm_count) return SWIGLU_VARIANT_1SM_N64;
+  return SWIGLU_VARIANT_1SM_N32;
 }
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
@@ -140,7 +140,9 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
     return cudaMemsetAsync(Y, 0, y_bytes, s) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
   }
   if (variant == SWIGLU_VARIANT_AUTO) variant = choose_variant(M, N, K, interleaved, st->sm_count);
-  const VariantGeom g = variant_geom(variant);
+  const VariantGeom g = variant_geom(variant, interleaved);
+  const CUtensorMapSwizzle bsw =
+      g.b_swizzle_64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
 
   LaunchArgs la;
   std::memset(&la, 0, sizeof la);
@@ -148,12 +150,11 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, g.bk, g.box_a, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == SWIGLU_OK) {
     if (interleaved) {
-      rc = encode_2d(&la.b0, BF16, B0, 2 * N, K, 4 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
+      rc = encode_2d(&la.b0, BF16, B0, 2 * N, K, 4 * N, g.box_b, g.bk, bsw);
       la.b1 = la.b0;
     } else {
-      rc = encode_2d(&la.b0, BF16, B0, N, K, 2 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc == SWIGLU_OK)
-        rc = encode_2d(&la.b1, BF16, B1, N, K, 2 * N, g.box_b, g.bk, CU_TENSOR_MAP_SWIZZLE_128B);
+      rc = encode_2d(&la.b0, BF16, B0, N, K, 2 * N, g.box_b, g.bk, bsw);
+      if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, BF16, B1, N, K, 2 * N, g.box_b, g.bk, bsw);
     }
   }
   if (rc == SWIGLU_OK)
@@ -181,19 +182,91 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
+
+// FP8 E4M3 path: CTA-pair kernel, K-major weights, per-tensor scales.
+int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, const float *sW1,
+            const float *sW2, void *Y, int64_t M, int64_t N, int64_t K, bool interleaved,
+            void *stream) {
+  if (M < 0 || N < 0 || K < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || 2 * N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SWIGLU_OK;
+  if (!Y) return SWIGLU_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B0 || (!interleaved && !B1) || !sA || !sW1 || !sW2))
+    return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(Y)) return SWIGLU_ERR_MISALIGNED;
+  if (K > 0 && (!aligned16(A) || !aligned16(B0) || (!interleaved && !aligned16(B1))))
+    return SWIGLU_ERR_MISALIGNED;
+  if (K > 0 && ((reinterpret_cast<uintptr_t>(sA) | reinterpret_cast<uintptr_t>(sW1) |
+                 reinterpret_cast<uintptr_t>(sW2)) & 3u))
+    return SWIGLU_ERR_MISALIGNED;
+  if (N % 8 != 0 || K % 16 != 0) return SWIGLU_ERR_MISALIGNED;
+  const uint64_t y_bytes = uint64_t(M) * N * 2, a_bytes = uint64_t(M) * K;
+  const uint64_t w_bytes = uint64_t(K) * N * (interleaved ? 2 : 1);
+  if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, B0, w_bytes) ||
+      (!interleaved && overlaps(Y, y_bytes, B1, w_bytes)))
+    return SWIGLU_ERR_INVALID_ARG;
+
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cudaMemsetAsync(Y, 0, y_bytes, s) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof la);
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  rc = encode_2d(&la.a, U8, A, K, M, K, 128, 128, SW);
+  if (rc == SWIGLU_OK) {
+    if (interleaved) {
+      rc = encode_2d(&la.b0, U8, B0, K, 2 * N, K, 128, 128, SW);
+      la.b1 = la.b0;
+    } else {
+      rc = encode_2d(&la.b0, U8, B0, K, N, K, 128, 128, SW);
+      if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, B1, K, N, K, 128, 128, SW);
+    }
+  }
+  if (rc == SWIGLU_OK)
+    rc = encode_2d(&la.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, 2 * N, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc != SWIGLU_OK) return rc;
+  KParams &p = la.p;
+  p.M = int32_t(M);
+  p.N = int32_t(N);
+  p.K = int32_t(K);
+  p.num_m_blk = int32_t(cdiv(M, 256));
+  p.num_n_blk = int32_t(cdiv(N, 128));
+  p.num_k_blk = int32_t(cdiv(K, 128));
+  p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.err = st->err;
+  p.sA = sA;
+  p.sW1 = sW1;
+  p.sW2 = sW2;
+  if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  la.device = dev;
+  la.stream = s;
+  return launch_fp8(interleaved, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace swiglu {
 
-VariantGeom variant_geom(int variant) {
+VariantGeom variant_geom(int variant, bool interleaved) {
   switch (variant) {
     case SWIGLU_VARIANT_1SM_N64:
-      return {128, 64, 64, 64, 128, 1};
+      return {128, 64, 64, 64, 0, 128, 1};
+    case SWIGLU_VARIANT_1SM_N32:
+      // separate: two 32-column boxes (W1, W2); interleaved: one 64-column W_fused box
+      return interleaved ? VariantGeom{128, 32, 64, 64, 0, 128, 1}
+                         : VariantGeom{128, 32, 64, 32, 1, 128, 1};
     case SWIGLU_VARIANT_2SM_N128:
-      return {256, 128, 64, 64, 128, 2};
+      return {256, 128, 64, 64, 0, 128, 2};
     case SWIGLU_VARIANT_1SM_N128:
     default:
-      return {128, 128, 64, 64, 128, 1};
+      return {128, 128, 64, 64, 0, 128, 1};
   }
 }
 
@@ -241,6 +314,38 @@ int swiglu_pack_interleaved(const void *W1, const void *W2, void *Wfused, int64_
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
+int swiglu_fused_fp8(const void *Aq, const void *W1t, const void *W2t, const float *sA,
+                     const float *sW1, const float *sW2, void *Y, int64_t M, int64_t N,
+                     int64_t K, void *stream) {
+  return run_fp8(Aq, W1t, W2t, sA, sW1, sW2, Y, M, N, K, false, stream);
+}
+
+int swiglu_fused_interleaved_fp8(const void *Aq, const void *Wfused_t, const float *sA,
+                                 const float *sW1, const float *sW2, void *Y, int64_t M,
+                                 int64_t N, int64_t K, void *stream) {
+  return run_fp8(Aq, Wfused_t, nullptr, sA, sW1, sW2, Y, M, N, K, true, stream);
+}
+
+int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t, int64_t N,
+                                int64_t K, void *stream) {
+  if (K < 0 || N < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (K > kMaxDim || 2 * N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (K == 0 || N == 0) return SWIGLU_OK;
+  if (!W1t || !W2t || !Wfused_t) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(W1t) || !aligned16(W2t) || !aligned16(Wfused_t)) return SWIGLU_ERR_MISALIGNED;
+  if (K % 16 != 0) return SWIGLU_ERR_MISALIGNED;
+  const uint64_t w = uint64_t(K) * N;
+  if (overlaps(Wfused_t, 2 * w, W1t, w) || overlaps(Wfused_t, 2 * w, W2t, w))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaError_t e = launch_pack_rows_interleaved_u8(W1t, W2t, Wfused_t, N, K, st->sm_count,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
 int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved) {
   if (M < 0 || N < 0 || K < 0) return SWIGLU_VARIANT_AUTO;
   int sms = 0, dev = 0;
@@ -258,6 +363,7 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_1SM_N128: return "1sm_n128";
     case SWIGLU_VARIANT_1SM_N64: return "1sm_n64";
     case SWIGLU_VARIANT_2SM_N128: return "2sm_n128";
+    case SWIGLU_VARIANT_1SM_N32: return "1sm_n32";
     default: return "?";
   }
 }

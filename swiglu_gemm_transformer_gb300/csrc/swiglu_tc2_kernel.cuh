@@ -15,9 +15,13 @@
 //   * each CTA's TMEM receives its own 128 rows x 256 columns (gate | up, or
 //     the interleaved pairs), double-buffered, so the epilogue is local;
 //   * the even CTA owns the "full" barriers (both CTAs' TMA copies count on
-//     them) and the "accumulator empty" barriers (all eight epilogue warps
+//     them) and the "accumulator empty" barriers (all sixteen epilogue warps
 //     arrive there); MMA completion is multicast to both CTAs' "empty" and
 //     "accumulator full" barriers.
+// FP8 E4M3 operands (the page's motivation: quantisation raises tensor-core
+// density, section "Definizione del Problema") use tcgen05.mma.kind::f8f6f4
+// with K-major weights; the epilogue multiplies the gate and up accumulators
+// by sA*sW1 and sA*sW2 before SiLU.
 // Waits are bounded as in the one-CTA kernel.
 #pragma once
 
@@ -29,29 +33,39 @@
 
 namespace swiglu {
 
-template <bool INTERLEAVED_, int STAGES_>
+// FP8 = false: BF16 operands, weights MN-major ([K,N] row-major), 64 K per stage.
+// FP8 = true : E4M3 operands, weights K-major ([N,K] row-major), 128 K per stage;
+//              the epilogue applies the per-tensor scales.
+template <bool INTERLEAVED_, int STAGES_, bool FP8_ = false>
 struct PairCfg {
   static constexpr bool INTERLEAVED = INTERLEAVED_;
   static constexpr int STAGES = STAGES_;
+  static constexpr bool FP8 = FP8_;
   static constexpr int BM = 128;                 // rows per CTA (MMA M = 256 per pair)
-  static constexpr int BK = 64;
+  static constexpr int BK = FP8 ? 128 : 64;      // K per stage: 128 bytes of each A row
+  static constexpr int MMA_K = FP8 ? 32 : 16;    // K of one MMA instruction (32 bytes)
   static constexpr int MMA_M = 256;
   static constexpr int MMA_N = 256;              // gate+up columns per tile
   static constexpr int BN = 128;                 // output columns per tile
-  static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-  static constexpr int ATOM_BYTES = BK * 128;    // 64 K-rows x 64 columns
-  static constexpr int B_ATOMS = 2;              // this CTA's 128 weight columns
+  static constexpr int A_BYTES = BM * 128;       // 16 KB
+  // BF16: two 64-column MN-major boxes of 64 K-rows; FP8: one K-major box of
+  // this CTA's 128 weight rows x 128 K bytes.
+  static constexpr int ATOM_BYTES = FP8 ? 128 * 128 : 64 * 128;
+  static constexpr int B_ATOMS = FP8 ? 1 : 2;
   static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 64;
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 192;
-  static constexpr uint32_t IDESC = ptx::idesc_bf16(MMA_M, MMA_N, false, true);
+  static constexpr int PRODUCER_WARP = EPI_WARPS;
+  static constexpr int MMA_WARP = EPI_WARPS + 1;
+  static constexpr int THREADS = 32 * (EPI_WARPS + 2);
+  static constexpr uint32_t IDESC = FP8 ? ptx::idesc_e4m3(MMA_M, MMA_N, false, false)
+                                        : ptx::idesc_bf16(MMA_M, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -81,7 +95,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int cid = static_cast<int>(ptx::cluster_id_x());
   const int ncl = static_cast<int>(ptx::num_clusters_x());
 
-  if (warp == 4 && lane == 0) {
+  if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
@@ -97,7 +111,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::prefetch_tmap(rank == 0 || C::INTERLEAVED ? &tmB0 : &tmB1);
     ptx::prefetch_tmap(&tmY);
   }
-  if (warp == 5) {
+  if (warp == C::MMA_WARP) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish_pair();
   }
@@ -105,10 +119,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above overlaps the previous kernel when launched with PDL.
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
 
   const int num_tiles = p.num_m_blk * p.num_n_blk;
 
-  if (warp == 4) {
+  if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const CUtensorMap *tmB = (C::INTERLEAVED || rank == 0) ? &tmB0 : &tmB1;
@@ -118,6 +135,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int arow = mb * 2 * C::BM + static_cast<int>(rank) * C::BM;
+        // first weight column (BF16, [K,N]) or row (FP8, [N,K]) of this CTA's block
         const int bcol = C::INTERLEAVED ? nb * C::MMA_N + static_cast<int>(rank) * 128 : nb * C::BN;
         for (int kb = 0; kb < p.num_k_blk; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
@@ -130,9 +148,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
           if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
           ptx::tma_load_2d_pair(sa, &tmA, fb, kb * C::BK, arow);
+          if (C::FP8) {
+            ptx::tma_load_2d_pair(sb, tmB, fb, kb * C::BK, bcol);
+          } else {
 #pragma unroll
-          for (int j = 0; j < C::B_ATOMS; ++j)
-            ptx::tma_load_2d_pair(sb + j * C::ATOM_BYTES, tmB, fb, bcol + j * 64, kb * C::BK);
+            for (int j = 0; j < C::B_ATOMS; ++j)
+              ptx::tma_load_2d_pair(sb + j * C::ATOM_BYTES, tmB, fb, bcol + j * 64, kb * C::BK);
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -152,7 +174,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
@@ -174,11 +196,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t sa = base + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
+          for (int kk = 0; kk < C::BK / C::MMA_K; ++kk) {
+            // A: K-major, 128-byte swizzle; one MMA's K = 32 bytes along the row.
             const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
-            const uint64_t bdesc =
-                ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
-            ptx::mma_f16_pair(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if (C::FP8) {
+              // B: K-major like A.
+              const uint64_t bdesc = ptx::smem_desc(sb + kk * 32, 16, 1024, ptx::SW_128B);
+              ptx::mma_f8_pair(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            } else {
+              // B: MN-major; 64-column boxes ATOM_BYTES apart, 8-row K groups 1024
+              // bytes apart, 16 K-rows = 2048 bytes.
+              const uint64_t bdesc =
+                  ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
+              ptx::mma_f16_pair(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == C::STAGES) {
@@ -198,9 +229,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-3, both CTAs)
-    const int q = warp;
-    const uint32_t stg_base = base + C::STG_OFF + q * 2 * C::STG_BYTES;
+    // ------------------------------------------------------------ epilogue (warps 0-7, both CTAs)
+    const int q = warp & 3;   // TMEM lanes [32q, 32q+32)
+    const int h = warp >> 2;  // half of the tile's 32-column chunks
+    constexpr int NC = C::BN / 32;
+    const uint32_t stg_base = base + C::STG_OFF + warp * 2 * C::STG_BYTES;
+    float gs = 1.0f, us = 1.0f;
+    if (C::FP8) {
+      const float sa = *p.sA;
+      gs = sa * *p.sW1;
+      us = sa * *p.sW2;
+    }
     uint32_t abuf = 0, aphase = 0, it = 0;
     for (int t = cid; t < num_tiles; t += ncl) {
       int mb, nb;
@@ -212,9 +251,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
       const int row0 = mb * 2 * C::BM + static_cast<int>(rank) * C::BM + q * 32;
-      epilogue_tile<C::INTERLEAVED, C::BN>(tacc, row0, nb * C::BN, &tmY, p.M, p.N, smem, base,
-                                           stg_base, it, lane,
-                                           ptx::mapa_shared(acce_bar(abuf), 0));
+      epilogue_tile<C::INTERLEAVED, C::BN, C::FP8>(
+          tacc, row0, nb * C::BN, h * (NC / 2), (h + 1) * (NC / 2), &tmY, p.M, p.N, smem, base,
+          stg_base, it, lane, ptx::mapa_shared(acce_bar(abuf), 0), gs, us);
       if (++abuf == 2) {
         abuf = 0;
         aphase ^= 1u;
@@ -226,7 +265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   ptx::tc_fence_before();
   ptx::cluster_sync();
-  if (warp == 5) {
+  if (warp == C::MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }

@@ -1,4 +1,4 @@
-// swiglu_tc_kernel.cuh -- the fused SwiGLU tcgen05 kernel for sm_103a.
+// swiglu_tc_kernel.cuh -- the one-CTA fused SwiGLU tcgen05 kernel for sm_103a.
 //
 // Computes Y = SiLU(A x W1) (.) (A x W2) (page "Riepilogo Tecnico:
 // Sovrapposizione delle Attivazioni a Livello di Tile per l'Inferenza
@@ -10,10 +10,10 @@
 // GB300 design (the page's kernels target H100 and register accumulators):
 //   * persistent CTAs, one per SM, walk the output tiles in a grouped order so
 //     that concurrently running tiles share A rows and weight columns in L2;
-//   * warp 4 (one thread) streams A[128 x 64] and the weight tile
+//   * warp 8 (one thread) streams A[128 x 64] and the weight tile
 //     [64 x MMA_N] of every K step into a STAGES-deep shared-memory ring with
-//     TMA (128-byte swizzle), completion counted on mbarriers;
-//   * warp 5 (one thread) issues tcgen05.mma.kind::f16 M=128 x N=MMA_N x K=16.
+//     TMA (128- or 64-byte swizzle), completion counted on mbarriers;
+//   * warp 9 (one thread) issues tcgen05.mma.kind::f16 M=128 x N=MMA_N x K=16.
 //     The B operand of one MMA holds the gate columns AND the up columns of the
 //     tile side by side, so a single instruction produces both accumulators in
 //     tensor memory: separate form -> TMEM columns [0,BN) = gate, [BN,2BN) = up;
@@ -21,12 +21,17 @@
 //     PairMulStore pairing, now on adjacent TMEM columns);
 //   * the accumulators are double-buffered in TMEM (2 x MMA_N columns) so the
 //     epilogue of tile i overlaps the MMAs of tile i+1;
-//   * warps 0-3 (the epilogue) read their 32 TMEM lanes with tcgen05.ld, apply
-//     y = g * u / (1 + e^-g) in FP32, round to BF16 (RNE), stage 32x32 blocks
-//     in shared memory (64-byte swizzle, bank-conflict free) and write them
-//     with TMA stores whose completion overlaps the next block's arithmetic
-//     (the compute/store overlap of the page's Kernel-2).
+//   * warps 0-7 (the epilogue; warp w reads TMEM lanes 32*(w%4).. and half
+//     w/4 of the tile's columns) apply y = g * u / (1 + e^-g) in FP32, round
+//     to BF16 (RNE), stage 32x32 blocks in shared memory (64-byte swizzle,
+//     bank-conflict free) and write them with TMA stores whose completion
+//     overlaps the next block's arithmetic (the compute/store overlap of the
+//     page's Kernel-2).
 //   Gate and up values never leave the SM.
+//
+// Programmatic dependent launch: the prologue (barriers, TMEM, descriptor
+// prefetch) runs before griddepcontrol.wait, so it overlaps the previous
+// kernel on the stream; no global memory is touched before the wait.
 //
 // Every mbarrier wait is bounded by a time limit.  On expiry the waiting
 // thread records SWIGLU_ERR_TIMEOUT in the device error word, raises a CTA
@@ -43,29 +48,39 @@
 
 namespace swiglu {
 
-template <int NB_ATOMS_, bool INTERLEAVED_, int STAGES_>
+// NB_ATOMS weight boxes of ATOM_COLS columns make the MMA's B operand.
+//   ATOM_COLS = 64: 128-byte swizzle; ATOM_COLS = 32: 64-byte swizzle.
+template <int NB_ATOMS_, int ATOM_COLS_, bool INTERLEAVED_, int STAGES_>
 struct TileCfg {
   static constexpr int NB_ATOMS = NB_ATOMS_;
+  static constexpr int ATOM_COLS = ATOM_COLS_;
   static constexpr bool INTERLEAVED = INTERLEAVED_;
   static constexpr int STAGES = STAGES_;
   static constexpr int BM = 128;                 // rows per tile (MMA M)
-  static constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of BF16
-  static constexpr int MMA_N = NB_ATOMS * 64;    // gate+up accumulator columns per tile
+  static constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of A
+  static constexpr int MMA_N = NB_ATOMS * ATOM_COLS;  // gate+up accumulator columns per tile
   static constexpr int BN = MMA_N / 2;           // output columns per tile
   static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-  static constexpr int ATOM_BYTES = BK * 128;    // one 64-column weight box: 64 K-rows x 128 B
+  static constexpr int ROW_BYTES = ATOM_COLS * 2;          // one K-row of a weight box
+  static constexpr int ATOM_BYTES = BK * ROW_BYTES;        // one weight box
+  static constexpr uint32_t B_SWIZZLE = ATOM_COLS == 64 ? ptx::SW_128B : ptx::SW_64B;
+  static constexpr int B_SBO = 8 * ROW_BYTES;              // 8-row K group
+  static constexpr int B_KSTEP = 16 * ROW_BYTES;           // 16 K-rows = one MMA's K
   static constexpr int B_BYTES = NB_ATOMS * ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 64;      // a warp's 32 rows x 32 BF16 columns
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full[S], empty[S], acc_full[2], acc_empty[2], drain
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + slot/flag + alignment slack
-  static constexpr int TMEM_COLS = (2 * MMA_N <= 256) ? 256 : 512;
-  static constexpr int THREADS = 192;
+  static constexpr int TMEM_COLS = (2 * MMA_N <= 128) ? 128 : (2 * MMA_N <= 256) ? 256 : 512;
+  static constexpr int PRODUCER_WARP = EPI_WARPS;
+  static constexpr int MMA_WARP = EPI_WARPS + 1;
+  static constexpr int THREADS = 32 * (EPI_WARPS + 2);
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
-  static_assert(NB_ATOMS == 2 || NB_ATOMS == 4, "MMA N of 128 or 256");
+  static_assert(MMA_N % 16 == 0 && MMA_N >= 64 && MMA_N <= 256, "MMA N");
+  static_assert(INTERLEAVED || NB_ATOMS % 2 == 0, "separate form: half the boxes per weight");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -92,7 +107,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
@@ -109,7 +124,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (!C::INTERLEAVED) ptx::prefetch_tmap(&tmB1);
     ptx::prefetch_tmap(&tmY);
   }
-  if (warp == 5) {
+  if (warp == C::MMA_WARP) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -117,10 +132,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above overlaps the previous kernel when launched with PDL.
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
 
   const int num_tiles = p.num_m_blk * p.num_n_blk;
 
-  if (warp == 4) {
+  if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
@@ -143,14 +161,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (C::INTERLEAVED) {
 #pragma unroll
             for (int j = 0; j < C::NB_ATOMS; ++j)
-              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::MMA_N + j * 64,
-                               kb * C::BK);
+              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb,
+                               nb * C::MMA_N + j * C::ATOM_COLS, kb * C::BK);
           } else {
 #pragma unroll
             for (int j = 0; j < C::NB_ATOMS / 2; ++j) {
-              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::BN + j * 64, kb * C::BK);
+              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::BN + j * C::ATOM_COLS,
+                               kb * C::BK);
               ptx::tma_load_2d(sb + (C::NB_ATOMS / 2 + j) * C::ATOM_BYTES, &tmB1, fb,
-                               nb * C::BN + j * 64, kb * C::BK);
+                               nb * C::BN + j * C::ATOM_COLS, kb * C::BK);
             }
           }
           ++issued;
@@ -164,17 +183,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // Let the copies already in flight land before the CTA's shared
         // memory is released: wait for the last min(issued, STAGES) loads.
         const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
-        for (uint32_t i = issued - n; i < issued; ++i) {
-          const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1u;
-          const uint64_t t0 = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(full_bar(s), ph) &&
-                 ptx::globaltimer_ns() - t0 < p.timeout_ns) {
-          }
-        }
+        for (uint32_t i = issued - n; i < issued; ++i)
+          wait_quiet(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
@@ -199,10 +213,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             // A: K-major, 128-byte swizzle; 16 K-elements = 32 bytes along the row.
             const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
-            // B: MN-major, 128-byte swizzle; 64-column boxes ATOM_BYTES apart (LBO),
-            // 8-row K groups 1024 bytes apart (SBO); 16 K-rows = 2048 bytes.
+            // B: MN-major; weight boxes ATOM_BYTES apart (LBO), 8-row K groups
+            // B_SBO apart, one MMA's 16 K-rows = B_KSTEP bytes.
             const uint64_t bdesc =
-                ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
+                ptx::smem_desc(sb + kk * C::B_KSTEP, C::ATOM_BYTES, C::B_SBO, C::B_SWIZZLE);
             ptx::mma_f16(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(empty_bar(stage));
@@ -220,15 +234,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       // Every MMA this thread issued completes before TMEM can be freed.
       ptx::mma_commit(drain_bar);
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::globaltimer_ns() - t0 < p.timeout_ns) {
-      }
+      wait_quiet(drain_bar, 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-3)
-    const int q = warp;  // TMEM lanes [32q, 32q+32) = tile rows [32q, 32q+32)
-    const uint32_t stg_base = base + C::STG_OFF + q * 2 * C::STG_BYTES;
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    const int q = warp & 3;   // TMEM lanes [32q, 32q+32) = tile rows [32q, 32q+32)
+    const int h = warp >> 2;  // which half of the tile's 32-column chunks
+    constexpr int NC = C::BN / 32;
+    const int c_begin = NC >= 2 ? h * (NC / 2) : 0;
+    const int c_end = NC >= 2 ? (h + 1) * (NC / 2) : (h == 0 ? NC : 0);
+    const uint32_t stg_base = base + C::STG_OFF + warp * 2 * C::STG_BYTES;
     uint32_t abuf = 0, aphase = 0, it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int mb, nb;
@@ -239,8 +255,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
-      epilogue_tile<C::INTERLEAVED, C::BN>(tacc, mb * C::BM + q * 32, nb * C::BN, &tmY, p.M, p.N,
-                                           smem, base, stg_base, it, lane, acce_bar(abuf));
+      epilogue_tile<C::INTERLEAVED, C::BN>(tacc, mb * C::BM + q * 32, nb * C::BN, c_begin, c_end,
+                                           &tmY, p.M, p.N, smem, base, stg_base, it, lane,
+                                           acce_bar(abuf));
       if (++abuf == 2) {
         abuf = 0;
         aphase ^= 1u;
@@ -252,7 +269,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
   }

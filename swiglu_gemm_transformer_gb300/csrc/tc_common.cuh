@@ -30,6 +30,9 @@ struct KParams {
   int32_t pad_;
   uint64_t timeout_ns;   // limit of every mbarrier wait
   uint32_t *err;         // device error word: [0] = status, [1] = where
+  // FP8 operands only: device pointers to the per-tensor scales of A, W1, W2
+  // (the gate and up products are scaled by sA*sW1 and sA*sW2).
+  const float *sA, *sW1, *sW2;
 };
 
 // Bounded wait, slow path.  Returns false on timeout or when another role of
@@ -94,7 +97,8 @@ __device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Epilogue of one accumulator tile, for one warp (32 TMEM lanes = 32 rows).
+// Epilogue of one accumulator tile, for one warp (32 TMEM lanes = 32 rows,
+// output chunks [c_begin, c_end) of 32 columns each).
 //   tacc      : TMEM address of this warp's lanes at the tile's first column;
 //               separate form: columns [0,BN) gate, [BN,2BN) up;
 //               interleaved form: column 2j gate j, 2j+1 up j.
@@ -103,14 +107,23 @@ __device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
 //   it        : running staging-buffer counter of this warp.
 //   release   : cluster address of the barrier to arrive on once the warp has
 //               read the whole accumulator (frees the TMEM buffer for the MMA).
-template <bool INTERLEAVED, int BN>
+//   gs, us    : scales applied to the gate and up accumulators (SCALED only).
+template <bool INTERLEAVED, int BN, bool SCALED = false>
 __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, int col0,
+                                                     int c_begin, int c_end,
                                                      const CUtensorMap *tmY, int M, int N,
                                                      uint8_t *smem, uint32_t smem_base,
                                                      uint32_t stg_base, uint32_t &it, int lane,
-                                                     uint32_t release) {
+                                                     uint32_t release, float gs = 1.0f,
+                                                     float us = 1.0f) {
+  if (c_begin >= c_end) {  // nothing to read in this tile: release at once
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_cluster(release);
+    return;
+  }
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     uint32_t g[32], u[32];
     if (INTERLEAVED) {
       ptx::tmem_ld32(tacc + c * 64, g);
@@ -122,7 +135,18 @@ __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, in
     ptx::tmem_wait_ld();
     ptx::reg_fence(g);
     ptx::reg_fence(u);
-    if (c == BN / 32 - 1) {
+    if (SCALED) {
+      // separate form: g = gate columns, u = up columns; interleaved form:
+      // even registers are gate columns, odd registers up columns.
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float sg = INTERLEAVED ? ((i & 1) ? us : gs) : gs;
+        const float su = INTERLEAVED ? ((i & 1) ? us : gs) : us;
+        g[i] = __float_as_uint(__uint_as_float(g[i]) * sg);
+        u[i] = __float_as_uint(__uint_as_float(u[i]) * su);
+      }
+    }
+    if (c == c_end - 1) {
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(release);

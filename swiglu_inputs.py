@@ -56,9 +56,13 @@ def make_bf16(M: int, N: int, K: int, seed: int):
 
 
 def quantize_e4m3(x: torch.Tensor):
-    """Per-tensor amax scale and saturating RNE E4M3 codes: returns (q, s)."""
+    """Per-tensor amax scale and saturating RNE E4M3 codes: returns (q, s).
+
+    s is rounded to float32 (the type a device scale is stored in) before it
+    is used, so both sides of a comparison see the same scale value."""
+    import numpy as np
     amax = float(x.abs().max()) if x.numel() else 0.0
-    s = amax / E4M3_MAX if amax > 0 else 1.0
+    s = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
     q = (x / s).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).contiguous()
     return q, s
 

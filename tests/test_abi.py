@@ -49,7 +49,8 @@ def test_status_and_variant_strings(lib):
 
 def test_host_side_variant_choice(lib):
     # 0.5B shape, M = 64: 1 x 38 tiles of 128 columns cannot fill 152 SMs
-    assert lib.swiglu_select_variant(64, 4864, 896, 0) == sg.VARIANT_1SM_N64
+    assert lib.swiglu_select_variant(64, 4864, 896, 0) == sg.VARIANT_1SM_N32
+    assert lib.swiglu_select_variant(128, 18944, 3584, 0) == sg.VARIANT_1SM_N64
     assert lib.swiglu_select_variant(8192, 4864, 896, 0) == sg.VARIANT_2SM_N128
 
 
@@ -113,3 +114,16 @@ def test_python_binding_refuses_cpu_tensors(lib):
     A = torch.zeros(8, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         sg.swiglu_fused(A, A, A)
+
+
+def test_fp8_argument_validation(lib):
+    s = 0x50000000
+    assert lib.swiglu_fused_fp8(A_, W1_, W2_, None, s, s, Y_, 64, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_fused_fp8(A_, W1_, W2_, s, s, s, Y_, 64, 64, 40, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_fused_fp8(A_, W1_, W2_, s + 2, s, s, Y_, 64, 64, 64, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_fused_fp8(A_, W1_, W2_, s, s, s, A_, 64, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_fused_fp8(A_, W1_, W2_, s, s, s, Y_, 0, 64, 64, None) == sg.OK
+    assert lib.swiglu_fused_interleaved_fp8(A_, None, s, s, s, Y_, 64, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_pack_interleaved_fp8(W1_, W2_, Y_, 64, 24, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_pack_interleaved_fp8(W1_, W2_, W1_, 64, 64, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_pack_interleaved_fp8(W1_, W2_, Y_, 0, 64, None) == sg.OK
