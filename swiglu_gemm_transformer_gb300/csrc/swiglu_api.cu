@@ -255,18 +255,20 @@ int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, cons
 namespace swiglu {
 
 VariantGeom variant_geom(int variant, bool interleaved) {
+  // separate N32: two 32-column boxes (W1, W2); interleaved N32: one 64-column W_fused box
+  const VariantGeom n32 = interleaved ? VariantGeom{128, 32, 64, 64, 0, 128, 1, 1}
+                                      : VariantGeom{128, 32, 64, 32, 1, 128, 1, 1};
+  VariantGeom g;
   switch (variant) {
-    case SWIGLU_VARIANT_1SM_N64:
-      return {128, 64, 64, 64, 0, 128, 1};
-    case SWIGLU_VARIANT_1SM_N32:
-      // separate: two 32-column boxes (W1, W2); interleaved: one 64-column W_fused box
-      return interleaved ? VariantGeom{128, 32, 64, 64, 0, 128, 1}
-                         : VariantGeom{128, 32, 64, 32, 1, 128, 1};
-    case SWIGLU_VARIANT_2SM_N128:
-      return {256, 128, 64, 64, 0, 128, 2};
+    case SWIGLU_VARIANT_1SM_N64: return {128, 64, 64, 64, 0, 128, 1, 1};
+    case SWIGLU_VARIANT_1SM_N32: return n32;
+    case SWIGLU_VARIANT_1SM_N32_MC2: g = n32; g.mc = 2; g.box_a = 64; return g;
+    case SWIGLU_VARIANT_1SM_N32_MC4: g = n32; g.mc = 4; g.box_a = 32; return g;
+    case SWIGLU_VARIANT_1SM_N64_MC2: return {128, 64, 64, 64, 0, 64, 1, 2};
+    case SWIGLU_VARIANT_1SM_N128_MC2: return {128, 128, 64, 64, 0, 64, 1, 2};
+    case SWIGLU_VARIANT_2SM_N128: return {256, 128, 64, 64, 0, 128, 2, 1};
     case SWIGLU_VARIANT_1SM_N128:
-    default:
-      return {128, 128, 64, 64, 0, 128, 1};
+    default: return {128, 128, 64, 64, 0, 128, 1, 1};
   }
 }
 
@@ -364,6 +366,10 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_1SM_N64: return "1sm_n64";
     case SWIGLU_VARIANT_2SM_N128: return "2sm_n128";
     case SWIGLU_VARIANT_1SM_N32: return "1sm_n32";
+    case SWIGLU_VARIANT_1SM_N32_MC2: return "1sm_n32_mc2";
+    case SWIGLU_VARIANT_1SM_N32_MC4: return "1sm_n32_mc4";
+    case SWIGLU_VARIANT_1SM_N64_MC2: return "1sm_n64_mc2";
+    case SWIGLU_VARIANT_1SM_N128_MC2: return "1sm_n128_mc2";
     default: return "?";
   }
 }
