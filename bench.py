@@ -154,6 +154,33 @@ class ClockSampler:
                 "power_w_max": pmax}
 
 
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The timed region's duration as the job sees it: the slowest rank's."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step_per_rank: float, steps: int, ms_max: float, ws: int) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return ws * flops_per_step_per_rank * steps / (ms_max * 1e-3) / 1e12
+
+
+def roofline_entry(flops: float, nbytes: float, us: float, peak_tflops: float, peak_gbs: float) -> dict:
+    """Bound (tensor or HBM) of one launch and the fraction of it achieved."""
+    t_tc = flops / (peak_tflops * 1e12)
+    t_hbm = nbytes / (peak_gbs * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    return {"bound": bound,
+            "tflops": flops / (us * 1e-6) / 1e12,
+            "gbs": nbytes / (us * 1e-6) / 1e9,
+            "frac_of_roofline": max(t_tc, t_hbm) / (us * 1e-6)}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 class Workload:
@@ -383,13 +410,9 @@ def run_ours(args, ws, rank, local):
     # rotating copies of its inputs (enough copies to exceed 2.5x L2), in a graph.
     per_call_us = measure_calls(wl, stream, args.call_launches)
 
-    t_max = ms_total
-    if ws > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms_total, ws, dev)
     ms_per_step = t_max / args.steps
-    value = ws * wl.flops * args.steps / (t_max * 1e-3) / 1e12
+    value = job_tflops(wl.flops, args.steps, t_max, ws)
 
     peaks, peak_src = load_peaks()
     sustained = t_max > 1000.0
@@ -401,16 +424,13 @@ def run_ours(args, ws, rank, local):
         us = per_call_us[c]
         flops = 4 * M * wl.N * wl.K
         abytes = wl.algorithmic_bytes(M)
-        t_hbm = abytes / (peaks["hbm_gbs"] * 1e9)
-        t_tc = flops / (peak_tf * 1e12)
-        bound = "tensor" if t_tc >= t_hbm else "hbm"
-        achieved_tf = flops / (us * 1e-6) / 1e12
-        achieved_gbs = abytes / (us * 1e-6) / 1e9
+        r = roofline_entry(flops, abytes, us, peak_tf, peaks["hbm_gbs"])
+        bound, achieved_tf, achieved_gbs = r["bound"], r["tflops"], r["gbs"]
         kernels.append({
             "form": form, "M": M, "variant": "2sm_fp8" if wl.fp8 else sg.variant_name(v),
             "us": round(us, 3),
             "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
-            "frac_of_roofline": round(max(t_tc, t_hbm) / (us * 1e-6), 4),
+            "frac_of_roofline": round(r["frac_of_roofline"], 4),
             "share": 0.0,
         })
     tot_us = sum(k["us"] for k in kernels)
@@ -505,13 +525,8 @@ def run_e2e(args, wl, stream, ws):
             step()
         e1.record()
     e1.synchronize()
-    ms = e0.elapsed_time(e1)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    val = ws * wl.flops * steps / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    val = job_tflops(wl.flops, steps, ms, ws)
     return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "note": "weights resident in HBM; each step copies every call's A in and Y out (pinned host)"}
@@ -593,8 +608,8 @@ def oracle_sample(workload: str, target_s: float):
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
-    target = 12.0 / max(1, args.steps + args.warmup)
-    target = max(0.5, min(target, 6.0))
+    target = args.cpu_seconds / max(1, args.steps + args.warmup)
+    target = max(0.2, min(target, 6.0))
     import numpy as np  # noqa: F401
     vals = []
     desc = ""

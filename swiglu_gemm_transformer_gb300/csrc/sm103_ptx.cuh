@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *
       : "memory");
 }
 
+// Bring one 2-D tile into L2 only (no shared memory, no completion tracking).
+// Used once per descriptor at kernel start so the TMA unit holds the
+// descriptor before the first real copy; L2 is the coherence point of device
+// memory, so an early prefetch cannot make a later load see stale data.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

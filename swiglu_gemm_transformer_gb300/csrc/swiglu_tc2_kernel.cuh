@@ -121,6 +121,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   // Everything above overlaps the previous kernel when launched with PDL.
   ptx::grid_launch_dependents();
+  if (warp == C::PRODUCER_WARP && lane == 0) {
+    // Warm the TMA unit's descriptor cache while the previous kernel ends.
+    ptx::tma_prefetch_2d(&tmA, 0, 0);
+    ptx::tma_prefetch_2d(rank == 0 || C::INTERLEAVED ? &tmB0 : &tmB1, 0, 0);
+  }
   ptx::grid_dependency_wait();
 
   const int num_tiles = p.num_m_blk * p.num_n_blk;
@@ -259,7 +264,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         aphase ^= 1u;
       }
     }
-    if (lane == 0) ptx::bulk_wait<0>();
+    // Shared memory must not be released while a store still reads it; the
+    // stores' global writes complete before the grid does.
+    if (lane == 0) ptx::bulk_wait_read<0>();
     __syncwarp();
   }
 

@@ -151,6 +151,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   // Everything above overlaps the previous kernel when launched with PDL.
   ptx::grid_launch_dependents();
+  if (warp == C::PRODUCER_WARP && lane == 0) {
+    // Warm the TMA unit's descriptor cache while the previous kernel ends.
+    ptx::tma_prefetch_2d(&tmA, 0, 0);
+    ptx::tma_prefetch_2d(&tmB0, 0, 0);
+    if (!C::INTERLEAVED) ptx::tma_prefetch_2d(&tmB1, 0, 0);
+  }
   ptx::grid_dependency_wait();
 
   const int num_units = pc.num_m_blk * pc.num_n_blk;
@@ -298,7 +304,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         aphase ^= 1u;
       }
     }
-    if (lane == 0) ptx::bulk_wait<0>();
+    // Shared memory must not be released while a store still reads it; the
+    // stores' global writes complete before the grid does.
+    if (lane == 0) ptx::bulk_wait_read<0>();
     __syncwarp();
   }
 
