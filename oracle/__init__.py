@@ -66,6 +66,12 @@ def _load():
         lib.oracle_pack_interleaved_u8.restype = None
         lib.oracle_swiglu_interleaved_bf16.argtypes = [p, p, i64, i64, i64, p, i64, p]
         lib.oracle_swiglu_interleaved_bf16.restype = ctypes.c_int
+        lib.oracle_f64_to_bf16.argtypes = [d]
+        lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_linear_bf16.argtypes = [p, p, p, i64, i64, i64, p, i64, p]
+        lib.oracle_linear_bf16.restype = ctypes.c_int
+        lib.oracle_mlp_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, p, i64, p, p]
+        lib.oracle_mlp_bf16.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -186,6 +192,57 @@ def swiglu_interleaved_bf16(A, Wf, rows=None) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_swiglu_interleaved_bf16 failed")
     return Y
+
+
+def f64_to_bf16(x: float) -> int:
+    """Round to the nearest BF16 (ties to even); returns the 16-bit pattern."""
+    return int(_load().oracle_f64_to_bf16(float(x)))
+
+
+def linear_bf16(X, W, R=None, rows=None) -> np.ndarray:
+    """Z = X W (+ R) in double; X [M,K], W [K,N], R [M,N] as BF16 bit patterns."""
+    X, W = _u16(X), _u16(W)
+    M, K = X.shape
+    K2, N = W.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if R is not None:
+        R = _u16(R)
+        if R.shape != (M, N):
+            raise ValueError("R must be [M, N]")
+    r, nr = _rows(rows, M)
+    Z = np.empty((nr, N), dtype=np.float64)
+    rc = _load().oracle_linear_bf16(_ptr(X), _ptr(W), _ptr(R) if R is not None else None,
+                                    M, N, K, _ptr(r) if r is not None else None, nr, _ptr(Z))
+    if rc != 0:
+        raise ValueError("oracle_linear_bf16 failed")
+    return Z
+
+
+def mlp_bf16(A, W1, W2, W3, R=None, rows=None, with_y: bool = False):
+    """The SwiGLU MLP block: Y = BF16(SiLU(A W1) * (A W2)), Z = Y W3 (+ R).
+
+    A [M,H], W1/W2 [H,F], W3 [F,H], R [M,H] as BF16 bit patterns.  Returns Z
+    [nrows,H] float64, or (Z, Ybits) with the rounded Y as uint16 patterns."""
+    A, W1, W2, W3 = _u16(A), _u16(W1), _u16(W2), _u16(W3)
+    M, H = A.shape
+    H2, F = W1.shape
+    if H2 != H or W2.shape != (H, F) or W3.shape != (F, H):
+        raise ValueError("shape mismatch")
+    if R is not None:
+        R = _u16(R)
+        if R.shape != (M, H):
+            raise ValueError("R must be [M, H]")
+    r, nr = _rows(rows, M)
+    Z = np.empty((nr, H), dtype=np.float64)
+    Y = np.empty((nr, F), dtype=np.uint16) if with_y else None
+    rc = _load().oracle_mlp_bf16(_ptr(A), _ptr(W1), _ptr(W2), _ptr(W3),
+                                 _ptr(R) if R is not None else None, M, H, F,
+                                 _ptr(r) if r is not None else None, nr, _ptr(Z),
+                                 _ptr(Y) if Y is not None else None)
+    if rc != 0:
+        raise ValueError("oracle_mlp_bf16 failed")
+    return (Z, Y) if with_y else Z
 
 
 from .check import parity_report, assert_parity  # noqa: E402,F401

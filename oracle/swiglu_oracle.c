@@ -270,3 +270,148 @@ int oracle_swiglu_interleaved_bf16(const uint16_t *A, const uint16_t *Wf,
     free(wf);
     return 0;
 }
+
+/* ---- the next step of the MLP: the down projection ---------------------- */
+/*
+ * The page motivates the fused kernel by the MLP's total time (section
+ * "Definizione del Problema": gate/up materialisation is 9-37 % of MLP time);
+ * the MLP continues with a down projection Z = Y x W3 (+ residual R).  Between
+ * the two projections Y is stored in BF16, as the fused kernel writes it, so
+ * the MLP oracle rounds Y to BF16 once (round to nearest, ties to even) and
+ * multiplies the rounded values exactly.
+ */
+
+/* Round a double to the nearest BF16 value, ties to even, returning the bit
+ * pattern (no intermediate float rounding).  BF16: 1 sign, 8 exponent bits
+ * (bias 127), 7 fraction bits; subnormals below 2^-126 have spacing 2^-133. */
+uint16_t oracle_f64_to_bf16(double x)
+{
+    if (isnan(x))
+        return 0x7FC0u;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    int e;
+    frexp(a, &e);              /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    int q = e - 1;             /* a in [2^q, 2^(q+1)) */
+    if (q < -126)
+        q = -126;              /* subnormal range keeps the spacing of 2^-126's binade */
+    double ulp = ldexp(1.0, q - 7);
+    double m = nearbyint(a / ulp); /* exact division by a power of two; ties to even */
+    double r = m * ulp;
+    if (r >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80u); /* overflow to infinity */
+    /* encode r */
+    if (r < ldexp(1.0, -126)) {            /* subnormal: r = m * 2^-133 */
+        return (uint16_t)(sign | (uint16_t)m);
+    }
+    int er;
+    double fr = frexp(r, &er);             /* r = fr * 2^er, fr in [0.5, 1) */
+    int biased = er - 1 + 127;
+    uint16_t frac = (uint16_t)((fr * 2.0 - 1.0) * 128.0); /* exact: 7 fraction bits */
+    return (uint16_t)(sign | (uint16_t)(biased << 7) | frac);
+}
+
+/* Z[r,:] = X[m_r,:] W (+ R[m_r,:]) in double, X [M,K], W [K,N], R [M,N] (may be NULL). */
+int oracle_linear_bf16(const uint16_t *X, const uint16_t *W, const uint16_t *R,
+                       int64_t M, int64_t N, int64_t K,
+                       const int64_t *rows, int64_t nrows, double *Z)
+{
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        if (m < 0 || m >= M)
+            return -1;
+    }
+    double *w = decode_bf16_matrix(W, K * N);
+    if (!w)
+        return -1;
+#pragma omp parallel
+    {
+        double *x = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        double *z = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            decode_a_row(X, 0, 1.0, m, K, x);
+            for (int64_t n = 0; n < N; ++n)
+                z[n] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double xk = x[k];
+                const double *wk = w + k * N;
+                for (int64_t n = 0; n < N; ++n)
+                    z[n] += xk * wk[n];
+            }
+            for (int64_t n = 0; n < N; ++n)
+                Z[i * N + n] = z[n] + (R ? oracle_bf16_to_f64(R[m * N + n]) : 0.0);
+        }
+        free(x);
+        free(z);
+    }
+    free(w);
+    return 0;
+}
+
+/* The SwiGLU MLP block: Y = BF16(SiLU(A W1) (.) (A W2)) per row, then
+ * Z = Y W3 (+ R).  A [M,H], W1/W2 [H,F], W3 [F,H], R [M,H] (may be NULL).
+ * Writes Z [nrows,H] in double and, if Ybits is not NULL, the rounded Y
+ * [nrows,F] as BF16 bit patterns. */
+int oracle_mlp_bf16(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
+                    const uint16_t *W3, const uint16_t *R,
+                    int64_t M, int64_t H, int64_t F,
+                    const int64_t *rows, int64_t nrows, double *Z, uint16_t *Ybits)
+{
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        if (m < 0 || m >= M)
+            return -1;
+    }
+    double *w1 = decode_bf16_matrix(W1, H * F);
+    double *w2 = decode_bf16_matrix(W2, H * F);
+    double *w3 = decode_bf16_matrix(W3, F * H);
+    int rc = -1;
+    if (w1 && w2 && w3) {
+        rc = 0;
+#pragma omp parallel
+        {
+            double *a = (double *)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
+            double *g = (double *)malloc((size_t)(F > 0 ? F : 1) * sizeof(double));
+            double *u = (double *)malloc((size_t)(F > 0 ? F : 1) * sizeof(double));
+            double *y = (double *)malloc((size_t)(F > 0 ? F : 1) * sizeof(double));
+            double *z = (double *)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t i = 0; i < nrows; ++i) {
+                int64_t m = rows ? rows[i] : i;
+                decode_a_row(A, 0, 1.0, m, H, a);
+                gate_up_row(a, w1, w2, F, H, g, u);
+                for (int64_t f = 0; f < F; ++f) {
+                    uint16_t yb = oracle_f64_to_bf16(oracle_silu(g[f]) * u[f]);
+                    if (Ybits)
+                        Ybits[i * F + f] = yb;
+                    y[f] = oracle_bf16_to_f64(yb);
+                }
+                for (int64_t h = 0; h < H; ++h)
+                    z[h] = 0.0;
+                for (int64_t f = 0; f < F; ++f) {
+                    const double yf = y[f];
+                    const double *w3f = w3 + f * H;
+                    for (int64_t h = 0; h < H; ++h)
+                        z[h] += yf * w3f[h];
+                }
+                for (int64_t h = 0; h < H; ++h)
+                    Z[i * H + h] = z[h] + (R ? oracle_bf16_to_f64(R[m * H + h]) : 0.0);
+            }
+            free(a);
+            free(g);
+            free(u);
+            free(y);
+            free(z);
+        }
+    }
+    free(w1);
+    free(w2);
+    free(w3);
+    return rc;
+}

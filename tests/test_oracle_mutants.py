@@ -34,6 +34,17 @@ MUTANTS = {
     "bf16_shift": ("uint32_t w = (uint32_t)bits << 16;", "uint32_t w = (uint32_t)bits << 15;"),
 }
 
+# Planted mistakes in the MLP pieces, caught by the MLP pins below.
+MLP_MUTANTS = {
+    "round_truncates": ("double m = nearbyint(a / ulp);", "double m = floor(a / ulp);"),
+    "round_via_float": ("double m = nearbyint(a / ulp);", "double m = nearbyint((double)(float)(a / ulp));"),
+    "linear_drops_residual": ("Z[i * N + n] = z[n] + (R ? oracle_bf16_to_f64(R[m * N + n]) : 0.0);",
+                              "Z[i * N + n] = z[n];"),
+    "linear_transposed_w": ("const double *wk = w + k * N;\n                for (int64_t n = 0; n < N; ++n)\n                    z[n] += xk * wk[n];",
+                            "for (int64_t n = 0; n < N; ++n)\n                    z[n] += xk * w[n * K + k];"),
+    "mlp_skips_rounding": ("y[f] = oracle_bf16_to_f64(yb);", "y[f] = oracle_silu(g[f]) * u[f];"),
+}
+
 
 def _build(tmp_path, name, src_text):
     c = tmp_path / f"{name}.c"
@@ -49,6 +60,10 @@ def _build(tmp_path, name, src_text):
     lib.oracle_swiglu_interleaved_bf16.argtypes = [p, p, i64, i64, i64, p, i64, p]
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_to_f64.restype = d
+    lib.oracle_f64_to_bf16.argtypes = [d]
+    lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_linear_bf16.argtypes = [p, p, p, i64, i64, i64, p, i64, p]
+    lib.oracle_mlp_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, p, i64, p, p]
     return lib
 
 
@@ -116,3 +131,58 @@ def test_planted_mistake_is_caught(tmp_path, golden_dir, name):
     assert src.count(old) >= 1, f"mutation site for {name} not found in the oracle source"
     lib = _build(tmp_path, name, src.replace(old, new, 1))
     assert not _pins_pass(lib, golden_dir), f"pins did not catch mutant {name}"
+
+
+def _mlp_pins_pass(lib) -> bool:
+    # (1) BF16 rounding against torch's float conversion, including exact ties
+    rng = np.random.default_rng(1)
+    f = rng.standard_normal(4000).astype(np.float32) * np.float32(3.0)
+    ties = (rng.integers(0, 2 ** 15, size=200, dtype=np.uint64).astype(np.uint32) << 16 | 0x8000).view(np.float32)
+    f = np.concatenate([f, ties[np.isfinite(ties)]])
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([lib.oracle_f64_to_bf16(float(x)) for x in f], dtype=np.uint16)
+    if not np.array_equal(got, want):
+        return False
+    # a double just above a midpoint (not representable in float) rounds up
+    if lib.oracle_f64_to_bf16(1.0 + 2 ** -8 + 2 ** -30) != 0x3F81:
+        return False
+    # (2) linear with a residual against numpy, non-square
+    X, W, _ = si.make_bf16(13, 24, 40, seed=7)
+    R = si.make_bf16(13, 24, 8, seed=8)[0][:, :8].repeat(1, 3).contiguous()
+    x, w, r = si.bits_u16(X), si.bits_u16(W), si.bits_u16(R)
+    Z = np.empty((13, 24))
+    lib.oracle_linear_bf16(_ptr(x), _ptr(w), _ptr(r), 13, 24, 40, None, 13, _ptr(Z))
+    if not np.allclose(Z, X.double().numpy() @ W.double().numpy() + R.double().numpy(),
+                       rtol=1e-12, atol=1e-12):
+        return False
+    # (3) MLP: Y is the BF16 rounding of the SwiGLU output, Z is that Y times W3
+    A, W1, W2 = si.make_bf16(9, 32, 24, seed=3)
+    W3 = si.make_bf16(1, 24, 32, seed=4)[1]
+    a, w1, w2, w3 = (si.bits_u16(t) for t in (A, W1, W2, W3))
+    Zm = np.empty((9, 24))
+    Yb = np.empty((9, 32), dtype=np.uint16)
+    lib.oracle_mlp_bf16(_ptr(a), _ptr(w1), _ptr(w2), _ptr(w3), None, 9, 24, 32, None, 9, _ptr(Zm), _ptr(Yb))
+    g = A.double().numpy() @ W1.double().numpy()
+    u = A.double().numpy() @ W2.double().numpy()
+    y = g / (1 + np.exp(-g)) * u
+    y_torch = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if np.mean(Yb != y_torch) > 0.01:       # torch rounds through float: rare near-tie differences
+        return False
+    yd = torch.from_numpy(Yb.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    return bool(np.allclose(Zm, yd @ W3.double().numpy(), rtol=1e-12, atol=1e-12))
+
+
+def test_unmodified_oracle_passes_mlp_pins(tmp_path):
+    lib = _build(tmp_path, "orig_mlp", open(SRC).read())
+    assert _mlp_pins_pass(lib)
+
+
+@pytest.mark.parametrize("name", sorted(MLP_MUTANTS))
+def test_planted_mlp_mistake_is_caught(tmp_path, name):
+    src = open(SRC).read()
+    old, new = MLP_MUTANTS[name]
+    old = old.replace("\\n", "\n")
+    new = new.replace("\\n", "\n")
+    assert src.count(old) >= 1, f"mutation site for {name} not found in the oracle source"
+    lib = _build(tmp_path, name, src.replace(old, new, 1))
+    assert not _mlp_pins_pass(lib), f"pins did not catch mutant {name}"
