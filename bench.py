@@ -45,6 +45,9 @@ WORKLOADS = {
     "qwen2.5-7b": (3584, 18944, (256, 1024, 2048, 4096), 2),
     "qwen2.5-72b": (8192, 29568, (2048, 8192, 16384), 3),
     "qwen2.5-7b-fp8": (3584, 18944, (512, 4096), 4),
+    # the SwiGLU MLP block: (H, F, Ms, seed)
+    "qwen2.5-0.5b-mlp": (896, 4864, (128, 512, 2048, 8192), 1),
+    "qwen2.5-7b-mlp": (3584, 18944, (256, 1024, 4096), 2),
 }
 DEFAULT_WORKLOAD = "qwen2.5-0.5b"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -184,120 +187,144 @@ def roofline_entry(flops: float, nbytes: float, us: float, peak_tflops: float, p
 # ----------------------------------------------------------------------------- our arm
 
 class Workload:
-    """Device-resident inputs and the list of fused calls of one step."""
+    """Device-resident inputs and the list of calls of one step.
 
-    def __init__(self, name, dev, variant=0, forms=("separate", "interleaved"), only=None):
+    kinds: "bf16" (fused projection, separate and interleaved weights),
+    "fp8" (the same with E4M3 operands), "mlp" (the SwiGLU MLP block, fused
+    projection followed by the down projection)."""
+
+    def __init__(self, name, dev, variant=0, only=None):
         import torch
         import swiglu_gemm_transformer_gb300 as sg
         import swiglu_inputs as si
         self.sg = sg
+        self.lib = sg.lib()
         self.name = name
         K, N, Ms, seed = WORKLOADS[name]
         self.K, self.N, self.Ms, self.seed = K, N, Ms, seed
         self.dev = dev
-        self.calls = []      # (form, M, variant_resolved, fn)
-        self.bytes_touched = 0
-        self.flops = 0
-        lib = sg.lib()
-        self.fp8 = name.endswith("-fp8")
+        self.kind = "fp8" if name.endswith("-fp8") else "mlp" if name.endswith("-mlp") else "bf16"
+        self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
-        host = {}
+        forms = ("mlp",) if self.kind == "mlp" else ("separate", "interleaved")
+        self.host = {}
         for M in Ms:
             if self.fp8:
                 q, sc = si.make_e4m3(M, N, K, seed)
-                host[M] = (q[0], q[1].t().contiguous(), q[2].t().contiguous(), sc)
-            else:
+                self.host[M] = (q[0], q[1].t().contiguous(), q[2].t().contiguous(), sc)
+            elif self.kind == "mlp":   # K = H (hidden), N = F (intermediate)
                 A, W1, W2 = si.make_bf16(M, N, K, seed)
-                host[M] = (A, W1, W2)
-        self.host = host
-        self.buffers = []
+                self.host[M] = (A, W1, W2, si.make_bf16(1, K, N, seed + 100)[1])
+            else:
+                self.host[M] = si.make_bf16(M, N, K, seed)
+        self.calls, self.buffers, self.fns = [], [], []
+        self.bytes_touched = 0
+        self.flops = 0
         for form in forms:
             for M in Ms:
                 if only is not None and (form, M) not in only:
                     continue
-                if self.fp8:
-                    self._add_fp8(form, M, host[M], dev)
-                    continue
-                A, W1, W2 = host[M]
-                Ad = A.to(dev)
-                Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-                if form == "separate":
-                    W1d, W2d = W1.to(dev), W2.to(dev)
-                    v = variant or lib.swiglu_select_variant(M, N, K, 0)
-                    ptrs = (Ad.data_ptr(), W1d.data_ptr(), W2d.data_ptr(), Y.data_ptr())
-                    fn = (lambda p=ptrs, M=M, v=v: self._sep(p, M, v))
-                    self.buffers.append((Ad, W1d, W2d, Y))
-                    wbytes = 2 * K * N * 2
-                else:
-                    W1d, W2d = W1.to(dev), W2.to(dev)
-                    Wf = sg.swiglu_pack_interleaved(W1d, W2d)
-                    del W1d, W2d
-                    v = variant or lib.swiglu_select_variant(M, N, K, 1)
-                    ptrs = (Ad.data_ptr(), Wf.data_ptr(), Y.data_ptr())
-                    fn = (lambda p=ptrs, M=M, v=v: self._inter(p, M, v))
-                    self.buffers.append((Ad, Wf, Y))
-                    wbytes = 2 * K * N * 2
-                self.calls.append((form, M, v, fn))
-                self.bytes_touched += M * K * 2 + wbytes + M * N * 2
-                self.flops += 4 * M * N * K
+                v = variant or (self.lib.swiglu_select_variant(M, N, K, int(form == "interleaved"))
+                                if self.kind == "bf16" else -1)
+                bufs = self._device_buffers(form, M)
+                self.calls.append((form, M, v))
+                self.buffers.append(bufs)
+                self.fns.append(self.launcher(form, M, v, bufs))
+                self.bytes_touched += self.algorithmic_bytes(M)
+                self.flops += self.flops_of(M)
         torch.cuda.synchronize(dev)
 
-    def _add_fp8(self, form, M, h, dev):
+    # -- per-call quantities
+    def flops_of(self, M):
+        return (6 if self.kind == "mlp" else 4) * M * self.N * self.K
+
+    def algorithmic_bytes(self, M):
+        """Inputs read once and the output written once (the MLP's Y is internal)."""
+        if self.kind == "mlp":
+            return 2 * (M * self.K + 3 * self.K * self.N + M * self.K)
+        return self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
+
+    def out_shape(self, M):
+        return (M, self.K) if self.kind == "mlp" else (M, self.N)
+
+    # -- buffers and launches
+    def _device_buffers(self, form, M):
         import torch
-        sg = self.sg
-        K, N = self.K, self.N
-        Aq, W1t, W2t, sc = h
-        Ad = Aq.to(dev)
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        s = torch.tensor(list(sc), dtype=torch.float32, device=dev)
-        sp = (s.data_ptr(), s.data_ptr() + 4, s.data_ptr() + 8)
-        W1d, W2d = W1t.to(dev), W2t.to(dev)
+        dev, sg = self.dev, self.sg
+        h = self.host[M]
+        out = torch.empty(self.out_shape(M), dtype=torch.bfloat16, device=dev)
+        if self.kind == "mlp":
+            ws = torch.empty(int(self.lib.swiglu_mlp_workspace_size(M, self.K, self.N)),
+                             dtype=torch.uint8, device=dev)
+            return (h[0].to(dev), h[1].to(dev), h[2].to(dev), h[3].to(dev), out, ws)
+        if self.fp8:
+            s = torch.tensor(list(h[3]), dtype=torch.float32, device=dev)
+            if form == "separate":
+                return (h[0].to(dev), h[1].to(dev), h[2].to(dev), out, s)
+            return (h[0].to(dev), sg.swiglu_pack_interleaved_fp8(h[1].to(dev), h[2].to(dev)), out, s)
         if form == "separate":
-            ptrs = (Ad.data_ptr(), W1d.data_ptr(), W2d.data_ptr(), Y.data_ptr())
-            fn = (lambda p=ptrs, M=M: self._fp8_sep(p, sp, M))
-            self.buffers.append((Ad, W1d, W2d, Y, s))
-        else:
-            Wf = sg.swiglu_pack_interleaved_fp8(W1d, W2d)
-            del W1d, W2d
-            ptrs = (Ad.data_ptr(), Wf.data_ptr(), Y.data_ptr())
-            fn = (lambda p=ptrs, M=M: self._fp8_inter(p, sp, M))
-            self.buffers.append((Ad, Wf, Y, s))
-        self.calls.append((form, M, -1, fn))
-        self.bytes_touched += M * K + 2 * K * N + M * N * 2
-        self.flops += 4 * M * N * K
-
-    def _fp8_sep(self, p, sp, M):
-        rc = self.sg.lib().swiglu_fused_fp8(p[0], p[1], p[2], sp[0], sp[1], sp[2], p[3], M, self.N,
-                                            self.K, self._stream())
-        if rc:
-            raise self.sg.SwigluError("swiglu_fused_fp8", rc)
-
-    def _fp8_inter(self, p, sp, M):
-        rc = self.sg.lib().swiglu_fused_interleaved_fp8(p[0], p[1], sp[0], sp[1], sp[2], p[2], M,
-                                                        self.N, self.K, self._stream())
-        if rc:
-            raise self.sg.SwigluError("swiglu_fused_interleaved_fp8", rc)
+            return (h[0].to(dev), h[1].to(dev), h[2].to(dev), out)
+        return (h[0].to(dev), sg.swiglu_pack_interleaved(h[1].to(dev), h[2].to(dev)), out)
 
     def _stream(self):
         import torch
         return torch.cuda.current_stream().cuda_stream
 
-    def _sep(self, p, M, v):
-        rc = self.sg.lib().swiglu_fused_ex(p[0], p[1], p[2], p[3], M, self.N, self.K, v, self._stream())
-        if rc:
-            raise self.sg.SwigluError("swiglu_fused_ex", rc)
+    def launcher(self, form, M, v, bufs):
+        """A closure launching this call through the C ABI on the current stream."""
+        lib, N, K, sg = self.lib, self.N, self.K, self.sg
+        d = [b.data_ptr() for b in bufs]
 
-    def _inter(self, p, M, v):
-        rc = self.sg.lib().swiglu_fused_interleaved_ex(p[0], p[1], p[2], M, self.N, self.K, v, self._stream())
-        if rc:
-            raise self.sg.SwigluError("swiglu_fused_interleaved_ex", rc)
+        def check(name, rc):
+            if rc:
+                raise sg.SwigluError(name, rc)
+        if self.kind == "mlp":
+            nbytes = bufs[5].numel()
+            return lambda: check("swiglu_mlp", lib.swiglu_mlp(d[0], d[1], d[2], d[3], None, d[4],
+                                                               M, K, N, d[5], nbytes, self._stream()))
+        if self.fp8:
+            sp = (d[-1], d[-1] + 4, d[-1] + 8)
+            if form == "separate":
+                return lambda: check("swiglu_fused_fp8", lib.swiglu_fused_fp8(
+                    d[0], d[1], d[2], sp[0], sp[1], sp[2], d[3], M, N, K, self._stream()))
+            return lambda: check("swiglu_fused_interleaved_fp8", lib.swiglu_fused_interleaved_fp8(
+                d[0], d[1], sp[0], sp[1], sp[2], d[2], M, N, K, self._stream()))
+        if form == "separate":
+            return lambda: check("swiglu_fused_ex", lib.swiglu_fused_ex(
+                d[0], d[1], d[2], d[3], M, N, K, v, self._stream()))
+        return lambda: check("swiglu_fused_interleaved_ex", lib.swiglu_fused_interleaved_ex(
+            d[0], d[1], d[2], M, N, K, v, self._stream()))
+
+    def api_call(self, form, M, v, bufs):
+        """The same call through the public Python API; returns the output tensor."""
+        sg = self.sg
+        if self.kind == "mlp":
+            return sg.swiglu_mlp(bufs[0], bufs[1], bufs[2], bufs[3], None, bufs[4], workspace=bufs[5])
+        if self.fp8:
+            sc = bufs[-1]
+            s3 = (sc[0:1], sc[1:2], sc[2:3])
+            if form == "separate":
+                return sg.swiglu_fused_fp8(bufs[0], bufs[1], bufs[2], *s3, bufs[3])
+            return sg.swiglu_fused_interleaved_fp8(bufs[0], bufs[1], *s3, bufs[2])
+        if form == "separate":
+            return sg.swiglu_fused(bufs[0], bufs[1], bufs[2], bufs[3], variant=v)
+        return sg.swiglu_fused_interleaved(bufs[0], bufs[1], bufs[2], variant=v)
+
+    def launches_per_call(self, M):
+        """Kernels one call enqueues (the MLP: fused projection, down projection,
+        and the split-K reduction when the down projection splits K)."""
+        if self.kind != "mlp":
+            return 1
+        return 2 + (1 if self.lib.swiglu_linear_workspace_size(M, self.K, self.N) > 0 else 0)
+
+    def variant_label(self, v):
+        if self.kind == "mlp":
+            return "mlp"
+        return "2sm_fp8" if self.fp8 else self.sg.variant_name(v)
 
     def step(self):
-        for _, _, _, fn in self.calls:
+        for fn in self.fns:
             fn()
-
-    def algorithmic_bytes(self, M):
-        return self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
 
 
 def measure_calls(wl, stream, launches):
@@ -306,27 +333,11 @@ def measure_calls(wl, stream, launches):
     the copies together exceed 2.5x the L2 size."""
     import torch
     out = []
-    for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
+    for (form, M, v), bufs in zip(wl.calls, wl.buffers):
         per = wl.algorithmic_bytes(M)
         ncopy = max(2, min(24, math.ceil(2.5 * L2_BYTES / per)))
         copies = [bufs] + [tuple(t.clone() for t in bufs) for _ in range(ncopy - 1)]
-        fns = []
-        for cb in copies:
-            if wl.fp8:
-                sd = cb[-1].data_ptr()
-                sp = (sd, sd + 4, sd + 8)
-                if form == "separate":
-                    p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr(), cb[3].data_ptr())
-                    fns.append(lambda p=p, sp=sp, M=M: wl._fp8_sep(p, sp, M))
-                else:
-                    p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr())
-                    fns.append(lambda p=p, sp=sp, M=M: wl._fp8_inter(p, sp, M))
-            elif form == "separate":
-                p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr(), cb[3].data_ptr())
-                fns.append(lambda p=p, M=M, v=v: wl._sep(p, M, v))
-            else:
-                p = (cb[0].data_ptr(), cb[1].data_ptr(), cb[2].data_ptr())
-                fns.append(lambda p=p, M=M, v=v: wl._inter(p, M, v))
+        fns = [wl.launcher(form, M, v, cb) for cb in copies]
         reps = max(1, math.ceil(launches / ncopy))
 
         def body():
@@ -368,6 +379,8 @@ def run_ours(args, ws, rank, local):
     if args.only:
         only = {(f, int(m)) for f, m in (x.split(":") for x in args.only.split(","))}
     wl = Workload(args.workload, dev, variant=sg.VARIANTS[args.variant], only=only)
+    if not wl.calls:
+        raise SystemExit(f"no calls selected from workload {args.workload}")
     stream = torch.cuda.Stream(device=dev)
     n_calls = len(wl.calls)
 
@@ -420,14 +433,14 @@ def run_ours(args, ws, rank, local):
     if wl.fp8:
         peak_tf *= 2.0  # dense FP8 = 2x dense BF16 (nominal 4.5 vs 2.25 PFLOP/s)
     kernels = []
-    for c, (form, M, v, _) in enumerate(wl.calls):
+    for c, (form, M, v) in enumerate(wl.calls):
         us = per_call_us[c]
-        flops = 4 * M * wl.N * wl.K
+        flops = wl.flops_of(M)
         abytes = wl.algorithmic_bytes(M)
         r = roofline_entry(flops, abytes, us, peak_tf, peaks["hbm_gbs"])
         bound, achieved_tf, achieved_gbs = r["bound"], r["tflops"], r["gbs"]
         kernels.append({
-            "form": form, "M": M, "variant": "2sm_fp8" if wl.fp8 else sg.variant_name(v),
+            "form": form, "M": M, "variant": wl.variant_label(v),
             "us": round(us, 3),
             "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
             "frac_of_roofline": round(r["frac_of_roofline"], 4),
@@ -438,7 +451,7 @@ def run_ours(args, ws, rank, local):
         k["share"] = round(k["us"] / tot_us, 4)
     dom = max(range(n_calls), key=lambda i: kernels[i]["us"])
     dk = kernels[dom]
-    form, M, v, _ = wl.calls[dom]
+    form, M, v = wl.calls[dom]
     kernel_key = f"{wl.name}:{form}:M{M}:{dk['variant']}"
     if dk["bound"] == "tensor":
         roof = {"bound": "tensor", "achieved": dk["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
@@ -448,7 +461,7 @@ def run_ours(args, ws, rank, local):
                 "frac": round(dk["gbs"] / peaks["hbm_gbs"], 4)}
     roof["traffic"] = load_traffic(kernel_key)
     roof["kernel"] = kernel_key
-    roof["algorithmic_per_launch"] = (4 * M * wl.N * wl.K if dk["bound"] == "tensor"
+    roof["algorithmic_per_launch"] = (wl.flops_of(M) if dk["bound"] == "tensor"
                                       else wl.algorithmic_bytes(M))
     roof["peak_source"] = (f"{peak_src} ({'sustained' if sustained and dk['bound'] == 'tensor' else 'burst'})"
                            + (", x2 for FP8" if wl.fp8 and dk["bound"] == "tensor" else ""))
@@ -460,8 +473,11 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic",
         "impl": "ours",
         "config": {
-            "workload": f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
-                        f"separate and interleaved weights, seed {wl.seed}",
+            "workload": (f"{wl.name} SwiGLU MLP block H={wl.K} F={wl.N} M={list(wl.Ms)} "
+                         f"(fused gate/up projection + down projection), seed {wl.seed}"
+                         if wl.kind == "mlp" else
+                         f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
+                         f"separate and interleaved weights, seed {wl.seed}"),
             "calls_per_step": n_calls,
             "l2": f"inputs larger than L2: each call has its own A, weights and Y; "
                   f"{wl.bytes_touched / 2**20:.0f} MiB per step vs {L2_BYTES / 2**20:.0f} MiB L2",
@@ -470,7 +486,7 @@ def run_ours(args, ws, rank, local):
                       "back-to-back launches of that call on rotating input copies",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
-        "gpu_launches": n_calls * args.steps,
+        "gpu_launches": sum(wl.launches_per_call(M) for (_, M, _) in wl.calls) * args.steps,
         "roofline": roof,
         "clocks": clocks,
         "kernels": kernels,
@@ -490,9 +506,9 @@ def run_e2e(args, wl, stream, ws):
     dev = wl.dev
     host_a, host_y = [], []
     h2d = d2h = 0
-    for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
+    for (form, M, v), bufs in zip(wl.calls, wl.buffers):
         A_host = wl.host[M][0].pin_memory()
-        Y_host = torch.empty((M, wl.N), dtype=torch.bfloat16).pin_memory()
+        Y_host = torch.empty(wl.out_shape(M), dtype=torch.bfloat16).pin_memory()
         host_a.append(A_host)
         host_y.append(Y_host)
         h2d += A_host.numel() * wl.eb
@@ -505,7 +521,7 @@ def run_e2e(args, wl, stream, ws):
     y_free = [torch.cuda.Event() for _ in range(n)]
 
     def step():
-        for i, ((form, M, v, _), bufs) in enumerate(zip(wl.calls, wl.buffers)):
+        for i, ((form, M, v), bufs) in enumerate(zip(wl.calls, wl.buffers)):
             Ad = bufs[0]
             with torch.cuda.stream(s_in):
                 s_in.wait_event(a_free[i])          # the previous step's kernel has read A
@@ -514,17 +530,7 @@ def run_e2e(args, wl, stream, ws):
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(a_ready[i])
                 s_cmp.wait_event(y_free[i])         # the previous step's Y has been copied out
-                if wl.fp8:
-                    sc = bufs[-1]
-                    s3 = (sc[0:1], sc[1:2], sc[2:3])
-                    if form == "separate":
-                        Y = sg.swiglu_fused_fp8(Ad, bufs[1], bufs[2], *s3, bufs[3])
-                    else:
-                        Y = sg.swiglu_fused_interleaved_fp8(Ad, bufs[1], *s3, bufs[2])
-                elif form == "separate":
-                    Y = sg.swiglu_fused(Ad, bufs[1], bufs[2], bufs[3], variant=v)
-                else:
-                    Y = sg.swiglu_fused_interleaved(Ad, bufs[1], bufs[2], variant=v)
+                Y = wl.api_call(form, M, v, bufs)
                 a_free[i].record()
                 y_ready[i].record()
             with torch.cuda.stream(s_out):
@@ -554,18 +560,20 @@ def run_e2e(args, wl, stream, ws):
 
 
 def run_unfused_context(wl, stream, steps):
-    """Context only: the unfused eager path (two cuBLAS GEMMs, SiLU, multiply) on the same inputs."""
+    """Context only: the unfused eager path (cuBLAS GEMMs, SiLU, multiply) on the same inputs."""
     import torch
     import torch.nn.functional as F
     if wl.fp8:
         return None
 
     def step():
-        for (form, M, v, _), bufs in zip(wl.calls, wl.buffers):
-            if form != "separate":
-                continue
-            A, W1, W2, Y = bufs
-            torch.mul(F.silu(A @ W1), A @ W2, out=Y)
+        for (form, M, v), bufs in zip(wl.calls, wl.buffers):
+            if wl.kind == "mlp":
+                A, W1, W2, W3, Z = bufs[:5]
+                torch.matmul(F.silu(A @ W1) * (A @ W2), W3, out=Z)
+            elif form == "separate":
+                A, W1, W2, Y = bufs
+                torch.mul(F.silu(A @ W1), A @ W2, out=Y)
     with torch.cuda.stream(stream):
         for _ in range(3):
             step()
@@ -580,49 +588,61 @@ def run_unfused_context(wl, stream, steps):
         e1.record()
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    flops = sum(4 * M * wl.N * wl.K for (f, M, _, _) in wl.calls if f == "separate")
-    return {"what": "torch eager: A@W1, A@W2 (cuBLAS), silu, mul; separate-weight calls only",
-            "ms_per_step": round(ms, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
+    flops = sum(wl.flops_of(M) for (f, M, _) in wl.calls if f in ("separate", "mlp"))
+    what = ("torch eager: (silu(A@W1) * (A@W2)) @ W3 (cuBLAS)" if wl.kind == "mlp" else
+            "torch eager: A@W1, A@W2 (cuBLAS), silu, mul; separate-weight calls only")
+    return {"what": what, "ms_per_step": round(ms, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 
 def oracle_sample(workload: str, target_s: float):
     """Time the CPU oracle on a bounded sample of the workload: for every call
-    (form, M) of the step, the same number of seeded rows.  Returns
-    (TFLOP/s, threads, description, seconds)."""
+    of the step, the same number of seeded rows.  Returns (TFLOP/s, threads,
+    description, seconds)."""
     import numpy as np
     import oracle
     import swiglu_inputs as si
     K, N, Ms, seed = WORKLOADS[workload]
     oracle.build()
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    _, W1, W2 = si.make_bf16(1, N, K, seed)
-    w1, w2 = si.bits_u16(W1), si.bits_u16(W2)
-    wf = oracle.pack_interleaved(w1, w2)
     rng = np.random.default_rng(seed)
-    A = si.bits_u16(si.make_bf16(max(Ms), N, K, seed)[0])
+    mlp = workload.endswith("-mlp")
+    fp8 = workload.endswith("-fp8")
+    if fp8:
+        (Aq, W1q, W2q), sc = si.make_e4m3(max(Ms), N, K, seed)
+        a8, w18, w28 = si.bits_u8(Aq), si.bits_u8(W1q), si.bits_u8(W2q)
+    else:
+        A, W1, W2 = si.make_bf16(max(Ms), N, K, seed)
+        a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
+        wf = oracle.pack_interleaved(w1, w2)
+        w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
+    forms = ("mlp",) if mlp else ("separate", "interleaved")
+    per_row = (6 if mlp else 4) * N * K
 
     def one(rows_per_call):
         t0 = time.perf_counter()
         flops = 0
-        for form in ("separate", "interleaved"):
+        for form in forms:
             for M in Ms:
                 rows = np.sort(rng.integers(0, M, size=rows_per_call))
-                if form == "separate":
-                    oracle.swiglu_bf16(A[:M], w1, w2, rows=rows)
+                if mlp:
+                    oracle.mlp_bf16(a[:M], w1, w2, w3, rows=rows)
+                elif fp8:
+                    oracle.swiglu_e4m3(a8[:M], w18, w28, *sc, rows=rows)
+                elif form == "separate":
+                    oracle.swiglu_bf16(a[:M], w1, w2, rows=rows)
                 else:
-                    oracle.swiglu_interleaved_bf16(A[:M], wf, rows=rows)
-                flops += 4 * rows_per_call * N * K
+                    oracle.swiglu_interleaved_bf16(a[:M], wf, rows=rows)
+                flops += per_row * rows_per_call
         return flops, time.perf_counter() - t0
 
     f0, s0 = one(max(1, threads))               # calibration
     rate = f0 / s0
-    per_row = 4 * N * K * 2 * len(Ms)
-    rows = max(1, int(target_s * rate / per_row))
+    rows = max(1, int(target_s * rate / (per_row * len(forms) * len(Ms))))
     flops, secs = one(rows)
-    desc = (f"{rows} seeded rows of each of the {2 * len(Ms)} calls (M in {list(Ms)}, separate and "
-            f"interleaved), all N={N} columns, K={K}: {flops / 1e9:.1f} GFLOP in {secs:.1f} s")
+    desc = (f"{rows} seeded rows of each of the {len(forms) * len(Ms)} calls (M in {list(Ms)}, "
+            f"{'/'.join(forms)}), all output columns, K={K}: {flops / 1e9:.1f} GFLOP in {secs:.1f} s")
     return flops / secs / 1e12, threads, desc, secs
 
 

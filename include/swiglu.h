@@ -144,6 +144,41 @@ int swiglu_fused_interleaved_fp8(const void *Aq, const void *Wfused_t, const flo
 int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t, int64_t N,
                                 int64_t K, void *stream);
 
+/*
+ * The down projection that completes the MLP block the page studies (section
+ * "Definizione del Problema": the gate/up materialisation is 9-37 % of MLP
+ * time; the MLP ends with a product by the down-projection weight):
+ *     Z[M,N] = X[M,K] x W[K,N] (+ R[M,N]),   BF16 in, FP32 accumulate, BF16 out.
+ *   X : device, BF16 [M,K] row-major (read)
+ *   W : device, BF16 [K,N] row-major (read)
+ *   R : device, BF16 [M,N] row-major residual (read), or NULL; may equal Z
+ *   Z : device, BF16 [M,N] row-major (written)
+ *   workspace : device scratch of workspace_bytes (caller-owned, 16-byte
+ *       aligned) used for split-K partial sums when the product has too few
+ *       output tiles to occupy the GPU (small M); swiglu_linear_workspace_size()
+ *       gives the bytes wanted.  NULL or too small is valid: the product then
+ *       runs without splitting K (same result up to summation order).
+ * K and N multiples of 8; other rules as above.
+ */
+uint64_t swiglu_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+int swiglu_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, int64_t N,
+                  int64_t K, void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
+ * The SwiGLU MLP block built from the two entry points above:
+ *     Y = BF16(SiLU(A W1) (.) (A W2)),   Z = Y W3 (+ R)
+ *   A  : BF16 [M,H]; W1, W2: BF16 [H,F]; W3: BF16 [F,H]; R: BF16 [M,H] or NULL; Z: BF16 [M,H]
+ *   workspace : caller-owned device scratch, at least M*F*2 bytes (Y lives in
+ *       its first M*F*2 bytes, rounded up to 256), preferably
+ *       swiglu_mlp_workspace_size() bytes (room for split-K partial sums).
+ * Two kernels on `stream`; the second starts its set-up while the first ends
+ * (programmatic dependent launch) and reads Y while it is still in L2.
+ */
+uint64_t swiglu_mlp_workspace_size(int64_t M, int64_t H, int64_t F);
+int swiglu_mlp(const void *A, const void *W1, const void *W2, const void *W3, const void *R,
+               void *Z, int64_t M, int64_t H, int64_t F, void *workspace,
+               uint64_t workspace_bytes, void *stream);
+
 /* swiglu_fused / swiglu_fused_interleaved with an explicit variant
  * (SWIGLU_VARIANT_*) instead of the library's choice; for sweeps and tests. */
 int swiglu_fused_ex(const void *A, const void *W1, const void *W2, void *Y,

@@ -12,6 +12,14 @@ that it is meaningful near zero, where a relative error is undefined:
   (2) no element with |ref| > 1e-2 * rms(ref) has |y - ref| / |ref| > 1e-2.
 
 Non-finite values anywhere in y fail (1).
+
+For a result that passes through an intermediate BF16 rounding (the MLP block:
+Y is rounded to BF16 before the down projection), the kernel rounds Y from an
+FP32 value and the oracle from the exact value, so the two may pick
+neighbouring BF16 numbers for a value near a rounding midpoint; both are
+correct roundings.  Such results use (1) unchanged and replace (2) by a bound
+on the fraction of significant elements more than 1 % off
+(``max_sig_mismatch_frac``).
 """
 from __future__ import annotations
 
@@ -22,7 +30,7 @@ ABS_OF_MAX = 1e-3    # absolute floor as a fraction of max|ref|
 SIG_OF_RMS = 1e-2    # "significant" elements: |ref| above this fraction of rms(ref)
 
 
-def parity_report(y, ref) -> dict:
+def parity_report(y, ref, max_sig_mismatch_frac: float = 0.0) -> dict:
     """Compare y (any float array) with ref (float64) element by element."""
     y = np.asarray(y, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -58,7 +66,8 @@ def parity_report(y, ref) -> dict:
         "rms_ref": rms_ref,
         "max_rel_err_sig": float(rel_sig.max()) if rel_sig.size else 0.0,
     }
-    rep["ok"] = rep["n_over_bound"] == 0 and n_rel_sig == 0
+    rep["ok"] = (rep["n_over_bound"] == 0 and
+                 n_rel_sig <= max_sig_mismatch_frac * max(1, rep["n_significant"]))
     if not rep["ok"]:
         idx = np.unravel_index(int(np.argmax(np.where(over, err - bound, -np.inf))), ref.shape)
         rep["worst_index"] = [int(i) for i in idx]
@@ -67,8 +76,8 @@ def parity_report(y, ref) -> dict:
     return rep
 
 
-def assert_parity(y, ref, what: str = "") -> dict:
-    rep = parity_report(y, ref)
+def assert_parity(y, ref, what: str = "", max_sig_mismatch_frac: float = 0.0) -> dict:
+    rep = parity_report(y, ref, max_sig_mismatch_frac)
     if not rep["ok"]:
         raise AssertionError(f"parity failed {what}: {rep}")
     return rep

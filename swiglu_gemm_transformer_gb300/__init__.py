@@ -36,6 +36,10 @@ EXPORTS = {
     "swiglu_fused_fp8": ("ppp ppp p lll p", ctypes.c_int),
     "swiglu_fused_interleaved_fp8": ("pp ppp p lll p", ctypes.c_int),
     "swiglu_pack_interleaved_fp8": ("ppp ll p", ctypes.c_int),
+    "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
+    "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
+    "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
+    "swiglu_mlp": ("ppppp p lll pQ p", ctypes.c_int),
     "swiglu_select_variant": ("lll i", ctypes.c_int),
     "swiglu_variant_name": ("i", ctypes.c_char_p),
     "swiglu_status_string": ("i", ctypes.c_char_p),
@@ -245,6 +249,69 @@ def swiglu_pack_interleaved_fp8(W1t, W2t, Wfused_t=None, *, stream=None):
                                            N, K, _stream(stream))
     _check("swiglu_pack_interleaved_fp8", rc)
     return Wfused_t
+
+
+def _workspace(nbytes, device, workspace):
+    import torch
+    if workspace is None:
+        if nbytes == 0:
+            return None, 0
+        workspace = torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def swiglu_linear(X, W, R=None, Z=None, *, workspace=None, stream=None):
+    """Z = X @ W (+ R); X [M,K], W [K,N], R [M,N] or None; BF16.
+
+    ``workspace`` (a CUDA tensor) holds split-K partial sums for small M; when
+    None, one of swiglu_linear_workspace_size() bytes is allocated here."""
+    import torch
+    bf = torch.bfloat16
+    _need(X, "X", bf), _need(W, "W", bf)
+    M, K = X.shape
+    if W.shape[0] != K:
+        raise ValueError(f"shape mismatch: X {tuple(X.shape)}, W {tuple(W.shape)}")
+    N = W.shape[1]
+    if R is not None:
+        _need(R, "R", bf)
+        if tuple(R.shape) != (M, N):
+            raise ValueError("R must be [M, N]")
+    if Z is None:
+        Z = torch.empty((M, N), dtype=bf, device=X.device)
+    else:
+        _need(Z, "Z", bf)
+        if tuple(Z.shape) != (M, N):
+            raise ValueError("Z must be [M, N]")
+    ws, nbytes = _workspace(lib().swiglu_linear_workspace_size(M, N, K), X.device, workspace)
+    rc = lib().swiglu_linear(X.data_ptr(), W.data_ptr(), R.data_ptr() if R is not None else None,
+                             Z.data_ptr(), M, N, K, ws.data_ptr() if ws is not None else None,
+                             nbytes, _stream(stream))
+    _check("swiglu_linear", rc)
+    return Z
+
+
+def swiglu_mlp(A, W1, W2, W3, R=None, Z=None, *, workspace=None, stream=None):
+    """Z = BF16(SiLU(A @ W1) * (A @ W2)) @ W3 (+ R); A [M,H], W1/W2 [H,F], W3 [F,H]."""
+    import torch
+    bf = torch.bfloat16
+    for t, n in ((A, "A"), (W1, "W1"), (W2, "W2"), (W3, "W3")):
+        _need(t, n, bf)
+    M, H = A.shape
+    F = W1.shape[1]
+    if W1.shape != (H, F) or W2.shape != (H, F) or W3.shape != (F, H):
+        raise ValueError("shape mismatch: A [M,H], W1/W2 [H,F], W3 [F,H]")
+    if R is not None:
+        _need(R, "R", bf)
+        if tuple(R.shape) != (M, H):
+            raise ValueError("R must be [M, H]")
+    if Z is None:
+        Z = torch.empty((M, H), dtype=bf, device=A.device)
+    ws, nbytes = _workspace(lib().swiglu_mlp_workspace_size(M, H, F), A.device, workspace)
+    rc = lib().swiglu_mlp(A.data_ptr(), W1.data_ptr(), W2.data_ptr(), W3.data_ptr(),
+                          R.data_ptr() if R is not None else None, Z.data_ptr(), M, H, F,
+                          ws.data_ptr() if ws is not None else None, nbytes, _stream(stream))
+    _check("swiglu_mlp", rc)
+    return Z
 
 
 def swiglu_select_variant(M: int, N: int, K: int, interleaved: bool = False) -> int:

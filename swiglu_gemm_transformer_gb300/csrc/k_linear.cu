@@ -1,0 +1,67 @@
+// k_linear.cu -- the linear (down-projection) instantiations of the CTA-pair
+// kernel and the split-K reduction kernel.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
+#include "launch_tc.cuh"
+
+namespace swiglu {
+
+cudaError_t launch_linear(int lin_n, const LaunchArgs &la) {
+  return lin_n == 256 ? launch_pair<PairCfg<true, 6, false, true, 256>>(la)
+                      : launch_pair<PairCfg<true, 8, false, true, 128>>(la);
+}
+
+// Z = BF16(sum_s ws[s] + R): four columns per thread (N is a multiple of 8),
+// one pass over the FP32 partial sums; memory-bound, grid-stride, with the
+// slices' loads unrolled so they are in flight together.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ ws,
+                                                            int splits, int64_t slice_vec4,
+                                                            const uint2 *__restrict__ R,
+                                                            uint2 *__restrict__ Z, int64_t n_vec4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_vec4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (R != nullptr) {
+      const uint2 r = __ldg(R + i);
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+      acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    int s = 0;
+    for (; s + 4 <= splits; s += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __ldg(ws + (s + j) * slice_vec4 + i);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+      }
+    }
+    for (; s < splits; ++s) {
+      const float4 v = __ldg(ws + s * slice_vec4 + i);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t *>(&lo);
+    o.y = *reinterpret_cast<const uint32_t *>(&hi);
+    Z[i] = o;
+  }
+}
+
+cudaError_t launch_splitk_reduce(const float *ws, int splits, const void *R, void *Z, int64_t M,
+                                 int64_t N, int sm_count, cudaStream_t s) {
+  const int64_t n_vec4 = M * N / 4;
+  if (n_vec4 == 0) return cudaSuccess;
+  const int threads = 256;
+  const int grid = (int)std::min<int64_t>((n_vec4 + threads - 1) / threads, (int64_t)sm_count * 8);
+  splitk_reduce_kernel<<<grid, threads, 0, s>>>(reinterpret_cast<const float4 *>(ws), splits,
+                                                 M * N / 4, static_cast<const uint2 *>(R),
+                                                 static_cast<uint2 *>(Z), n_vec4);
+  return cudaGetLastError();
+}
+
+}  // namespace swiglu

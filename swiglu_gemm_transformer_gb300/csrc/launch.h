@@ -37,6 +37,9 @@ cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf
                                         int sm_count, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t *err, cudaStream_t s);
 cudaError_t launch_fp8(bool interleaved, const LaunchArgs &la);
+cudaError_t launch_linear(int lin_n, const LaunchArgs &la);
+cudaError_t launch_splitk_reduce(const float *ws, int splits, const void *R, void *Z, int64_t M,
+                                 int64_t N, int sm_count, cudaStream_t s);
 cudaError_t launch_pack_rows_interleaved_u8(const void *W1t, const void *W2t, void *Wft,
                                             int64_t N, int64_t K, int sm_count, cudaStream_t s);
 

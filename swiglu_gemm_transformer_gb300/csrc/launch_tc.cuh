@@ -96,7 +96,9 @@ cudaError_t launch_pair(const LaunchArgs &la) {
     max_clusters[la.device & 63] = n;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int64_t tiles = int64_t(la.p.num_m_blk) * la.p.num_n_blk;
+  // work units: output tiles x K slices
+  const int64_t tiles =
+      int64_t(la.p.num_m_blk) * la.p.num_n_blk * (la.p.k_splits > 1 ? la.p.k_splits : 1);
   const int n = max_clusters[la.device & 63];
   const int clusters = int(tiles < n ? tiles : n);
   cfg.gridDim = dim3(2 * clusters, 1, 1);

@@ -5,8 +5,10 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -32,6 +34,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+// Down-projection tile width: 0 = chosen by shape; 128 or 256 forces it (the
+// SWIGLU_LINEAR_N environment variable, read once, sets it for tuning sweeps).
+std::atomic<int> g_linear_n{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int device_state(DeviceState **out, int *dev_out) {
@@ -71,6 +76,10 @@ int device_state(DeviceState **out, int *dev_out) {
     }
     st.sm_count = sms;
     st.ready = true;
+    if (const char *e = std::getenv("SWIGLU_LINEAR_N")) {
+      const long v = std::strtol(e, nullptr, 10);
+      if (v == 128 || v == 256) g_linear_n.store(int(v), std::memory_order_relaxed);
+    }
   }
   *out = &st;
   *dev_out = dev;
@@ -172,6 +181,8 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   p.group_m = p.num_m_blk < gm ? p.num_m_blk : gm;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blk;
   const int64_t tiles = int64_t(p.num_m_blk) * p.num_n_blk;
   if (tiles > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   la.grid = int(tiles < st->sm_count ? tiles : st->sm_count);  // one-CTA kernels
@@ -244,11 +255,124 @@ int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, cons
   p.sA = sA;
   p.sW1 = sW1;
   p.sW2 = sW2;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blk;
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
   la.stream = s;
   return launch_fp8(interleaved, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
+
+
+// ---- the down projection: Z = X W (+ R) ----------------------------------------
+
+struct LinearPlan {
+  int lin_n;       // output columns per CTA-pair tile (256 or 128)
+  int k_splits;    // K slices (1 = no split)
+  int kb_per;      // 64-deep K steps per slice
+  uint64_t ws_bytes;
+};
+
+LinearPlan plan_linear(int64_t M, int64_t N, int64_t K, int sm_count) {
+  LinearPlan pl;
+  const int forced = g_linear_n.load(std::memory_order_relaxed);
+  // 256-column tiles (the pair's weight halves of 128 columns, 32 KB per CTA
+  // per K step) keep the tensor pipe fed; measured faster than 128 even when
+  // the last tile is half empty (N = 896: 50 us vs 70 us at M = 8192).
+  // Very few output tiles (small M and N): 128-column tiles give more of them
+  // before K is split (0.5B, M = 128: 14.0 us vs 16.7 us).
+  if (!forced) pl.lin_n = (N <= 128 || cdiv(M, 256) * cdiv(N, 256) < 8) ? 128 : 256;
+  else pl.lin_n = forced;
+  const int64_t nk = cdiv(K, 64);
+  const int64_t tiles = cdiv(M, 256) * cdiv(N, pl.lin_n);
+  const int64_t pairs = sm_count / 2;
+  int64_t ks = 1;
+  // Few output tiles (small M): split K so that every CTA pair has work; each
+  // slice keeps at least four K steps.
+  if (tiles * 2 <= pairs) ks = std::min<int64_t>({pairs / tiles, nk / 4, 16});
+  if (ks < 2) ks = 1;
+  pl.kb_per = int(cdiv(nk, ks));
+  pl.k_splits = int(cdiv(nk, pl.kb_per));
+  pl.ws_bytes = pl.k_splits > 1 ? uint64_t(pl.k_splits) * M * N * 4 : 0;
+  return pl;
+}
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;  // GB300's SM count, for host-only planning without a device
+  }
+  return sms;
+}
+
+int run_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, int64_t N,
+               int64_t K, void *ws, uint64_t ws_bytes, void *stream) {
+  if (M < 0 || N < 0 || K < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SWIGLU_OK;
+  if (!Z || (K > 0 && (!X || !W))) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(Z) || (R && !aligned16(R)) || (K > 0 && (!aligned16(X) || !aligned16(W))))
+    return SWIGLU_ERR_MISALIGNED;
+  if (N % 8 != 0 || K % 8 != 0) return SWIGLU_ERR_MISALIGNED;
+  const uint64_t z_bytes = uint64_t(M) * N * 2;
+  if (overlaps(Z, z_bytes, X, uint64_t(M) * K * 2) || overlaps(Z, z_bytes, W, uint64_t(K) * N * 2))
+    return SWIGLU_ERR_INVALID_ARG;
+  if (R && R != Z && overlaps(Z, z_bytes, R, z_bytes)) return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {  // Z = R (or zeros)
+    cudaError_t e = R ? (R == Z ? cudaSuccess
+                                : cudaMemcpyAsync(Z, R, z_bytes, cudaMemcpyDeviceToDevice, s))
+                      : cudaMemsetAsync(Z, 0, z_bytes, s);
+    return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  }
+  LinearPlan pl = plan_linear(M, N, K, st->sm_count);
+  if (pl.k_splits > 1 &&
+      (ws == nullptr || ws_bytes < pl.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 15u) ||
+       overlaps(ws, pl.ws_bytes, Z, z_bytes) || overlaps(ws, pl.ws_bytes, X, uint64_t(M) * K * 2))) {
+    pl.k_splits = 1;  // no usable workspace: one K slice (correct, fewer busy SMs)
+    pl.kb_per = int(cdiv(K, 64));
+  }
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof la);
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  rc = encode_2d(&la.a, BF16, X, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == SWIGLU_OK)
+    rc = encode_2d(&la.b0, BF16, W, N, K, 2 * N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  la.b1 = la.b0;
+  if (rc == SWIGLU_OK)
+    rc = encode_2d(&la.y, BF16, Z, N, M, 2 * N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc != SWIGLU_OK) return rc;
+  KParams &p = la.p;
+  p.M = int32_t(M);
+  p.N = int32_t(N);
+  p.K = int32_t(K);
+  p.num_m_blk = int32_t(cdiv(M, 256));
+  p.num_n_blk = int32_t(cdiv(N, pl.lin_n));
+  p.num_k_blk = int32_t(cdiv(K, 64));
+  p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.err = st->err;
+  p.R = R;
+  p.ws = pl.k_splits > 1 ? static_cast<float *>(ws) : nullptr;
+  p.k_splits = pl.k_splits;
+  p.kb_per_split = pl.kb_per;
+  if (int64_t(p.num_m_blk) * p.num_n_blk * p.k_splits > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  la.device = dev;
+  la.stream = s;
+  if (launch_linear(pl.lin_n, la) != cudaSuccess) return SWIGLU_ERR_CUDA;
+  if (pl.k_splits > 1 &&
+      launch_splitk_reduce(p.ws, pl.k_splits, R, Z, M, N, st->sm_count, s) != cudaSuccess)
+    return SWIGLU_ERR_CUDA;
+  return SWIGLU_OK;
+}
+
+uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255u); }
 
 }  // namespace
 
@@ -346,6 +470,42 @@ int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t
   cudaError_t e = launch_pack_rows_interleaved_u8(W1t, W2t, Wfused_t, N, K, st->sm_count,
                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+uint64_t swiglu_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return plan_linear(M, N, K, device_sm_count()).ws_bytes;
+}
+
+int swiglu_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, int64_t N,
+                  int64_t K, void *workspace, uint64_t workspace_bytes, void *stream) {
+  return run_linear(X, W, R, Z, M, N, K, workspace, workspace_bytes, stream);
+}
+
+uint64_t swiglu_mlp_workspace_size(int64_t M, int64_t H, int64_t F) {
+  if (M <= 0 || H <= 0 || F <= 0) return 0;
+  return align256(uint64_t(M) * F * 2) + swiglu_linear_workspace_size(M, H, F);
+}
+
+int swiglu_mlp(const void *A, const void *W1, const void *W2, const void *W3, const void *R,
+               void *Z, int64_t M, int64_t H, int64_t F, void *workspace, uint64_t workspace_bytes,
+               void *stream) {
+  if (M < 0 || H < 0 || F < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M == 0 || H == 0) return SWIGLU_OK;
+  if (F == 0) return run_linear(nullptr, nullptr, R, Z, M, H, 0, nullptr, 0, stream);
+  const uint64_t y_bytes = align256(uint64_t(M) * F * 2);
+  if (!workspace || workspace_bytes < uint64_t(M) * F * 2) return SWIGLU_ERR_INVALID_ARG;
+  if (!A || !W3 || !Z) return SWIGLU_ERR_INVALID_ARG;
+  if (overlaps(workspace, workspace_bytes, Z, uint64_t(M) * H * 2) ||
+      overlaps(workspace, workspace_bytes, A, uint64_t(M) * H * 2) ||
+      (R && overlaps(workspace, workspace_bytes, R, uint64_t(M) * H * 2)))
+    return SWIGLU_ERR_INVALID_ARG;
+  void *Y = workspace;
+  int rc = run_bf16(A, W1, W2, Y, M, F, H, SWIGLU_VARIANT_AUTO, false, stream);
+  if (rc != SWIGLU_OK) return rc;
+  char *rest = static_cast<char *>(workspace) + y_bytes;
+  const uint64_t rest_bytes = workspace_bytes > y_bytes ? workspace_bytes - y_bytes : 0;
+  return run_linear(Y, W3, R, Z, M, H, F, rest_bytes ? rest : nullptr, rest_bytes, stream);
 }
 
 int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved) {

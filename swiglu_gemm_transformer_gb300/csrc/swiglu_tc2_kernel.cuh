@@ -36,22 +36,31 @@ namespace swiglu {
 // FP8 = false: BF16 operands, weights MN-major ([K,N] row-major), 64 K per stage.
 // FP8 = true : E4M3 operands, weights K-major ([N,K] row-major), 128 K per stage;
 //              the epilogue applies the per-tensor scales.
-template <bool INTERLEAVED_, int STAGES_, bool FP8_ = false>
+// LINEAR = false: the fused SwiGLU epilogue (MMA N = 256 = 128 gate + 128 up
+//                 columns, 128 output columns per tile).
+// LINEAR = true : a plain product Z = X W (+ R) with LIN_N output columns per
+//                 tile (MMA N = LIN_N = 256 or 128); the weight block of one
+//                 tile is split between the two CTAs like the interleaved form.
+template <bool INTERLEAVED_, int STAGES_, bool FP8_ = false, bool LINEAR_ = false,
+          int LIN_N = 256>
 struct PairCfg {
-  static constexpr bool INTERLEAVED = INTERLEAVED_;
+  static constexpr bool LINEAR = LINEAR_;
+  static constexpr bool INTERLEAVED = INTERLEAVED_ || LINEAR_;  // one weight matrix
   static constexpr int STAGES = STAGES_;
   static constexpr bool FP8 = FP8_;
   static constexpr int BM = 128;                 // rows per CTA (MMA M = 256 per pair)
   static constexpr int BK = FP8 ? 128 : 64;      // K per stage: 128 bytes of each A row
   static constexpr int MMA_K = FP8 ? 32 : 16;    // K of one MMA instruction (32 bytes)
   static constexpr int MMA_M = 256;
-  static constexpr int MMA_N = 256;              // gate+up columns per tile
-  static constexpr int BN = 128;                 // output columns per tile
+  static constexpr int MMA_N = LINEAR ? LIN_N : 256;  // accumulator columns per tile
+  static constexpr int BN = LINEAR ? LIN_N : 128;     // output columns per tile
   static constexpr int A_BYTES = BM * 128;       // 16 KB
-  // BF16: two 64-column MN-major boxes of 64 K-rows; FP8: one K-major box of
-  // this CTA's 128 weight rows x 128 K bytes.
+  // BF16: MN-major boxes of 64 columns x 64 K-rows (MMA_N/128 of them per
+  // CTA); FP8: one K-major box of this CTA's 128 weight rows x 128 K bytes.
   static constexpr int ATOM_BYTES = FP8 ? 128 * 128 : 64 * 128;
-  static constexpr int B_ATOMS = FP8 ? 1 : 2;
+  static constexpr int B_ATOMS = FP8 ? 1 : MMA_N / 128;
+  static_assert(!(LINEAR && FP8), "linear mode is BF16");
+  static_assert(LIN_N == 256 || LIN_N == 128, "linear tile width");
   static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
   static constexpr int EPI_WARPS = 8;
@@ -60,7 +69,7 @@ struct PairCfg {
   static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
-  static constexpr int TMEM_COLS = 512;
+  static constexpr int TMEM_COLS = 2 * MMA_N;
   static constexpr int PRODUCER_WARP = EPI_WARPS;
   static constexpr int MMA_WARP = EPI_WARPS + 1;
   static constexpr int THREADS = 32 * (EPI_WARPS + 2);
@@ -124,11 +133,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (warp == C::PRODUCER_WARP && lane == 0) {
     // Warm the TMA unit's descriptor cache while the previous kernel ends.
     ptx::tma_prefetch_2d(&tmA, 0, 0);
-    ptx::tma_prefetch_2d(rank == 0 || C::INTERLEAVED ? &tmB0 : &tmB1, 0, 0);
+    ptx::tma_prefetch_2d(rank == 0 || C::INTERLEAVED ? &tmB0 : &tmB1, 0, 0);  // descriptor warm-up
   }
   ptx::grid_dependency_wait();
 
-  const int num_tiles = p.num_m_blk * p.num_n_blk;
+  // work units: output tiles x K slices (k_splits == 1 unless split-K)
+  const int num_tiles = p.num_m_blk * p.num_n_blk * p.k_splits;
+  auto unit_coords = [&](int t, int &mb, int &nb, int &ks, int &kb0, int &kb1) {
+    ks = t % p.k_splits;
+    tile_coords(t / p.k_splits, p, mb, nb);
+    kb0 = ks * p.kb_per_split;
+    kb1 = min(p.num_k_blk, kb0 + p.kb_per_split);
+  };
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -137,12 +153,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       for (int t = cid; ok && t < num_tiles; t += ncl) {
-        int mb, nb;
-        tile_coords(t, p, mb, nb);
+        int mb, nb, ks, kb0, kb1;
+        unit_coords(t, mb, nb, ks, kb0, kb1);
         const int arow = mb * 2 * C::BM + static_cast<int>(rank) * C::BM;
         // first weight column (BF16, [K,N]) or row (FP8, [N,K]) of this CTA's block
-        const int bcol = C::INTERLEAVED ? nb * C::MMA_N + static_cast<int>(rank) * 128 : nb * C::BN;
-        for (int kb = 0; kb < p.num_k_blk; ++kb) {
+        const int bcol = C::INTERLEAVED ? nb * C::MMA_N + static_cast<int>(rank) * (C::MMA_N / 2)
+                                        : nb * C::BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
                         WAIT_PRODUCER_EMPTY)) {
             ok = false;
@@ -185,6 +202,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
       bool ok = true;
       for (int t = cid; ok && t < num_tiles; t += ncl) {
+        int mb, nb, ks, kb0, kb1;
+        unit_coords(t, mb, nb, ks, kb0, kb1);
         if (!wait_bar(acce_bar(abuf), aphase ^ 1u, p.timeout_ns, abort_flag, p.err,
                       WAIT_MMA_ACC_EMPTY)) {
           ok = false;
@@ -192,7 +211,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + abuf * C::MMA_N;
-        for (int kb = 0; kb < p.num_k_blk; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
             ok = false;
             break;
@@ -207,13 +226,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (C::FP8) {
               // B: K-major like A.
               const uint64_t bdesc = ptx::smem_desc(sb + kk * 32, 16, 1024, ptx::SW_128B);
-              ptx::mma_f8_pair(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+              ptx::mma_f8_pair(d, adesc, bdesc, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
             } else {
               // B: MN-major; 64-column boxes ATOM_BYTES apart, 8-row K groups 1024
               // bytes apart, 16 K-rows = 2048 bytes.
               const uint64_t bdesc =
                   ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
-              ptx::mma_f16_pair(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+              ptx::mma_f16_pair(d, adesc, bdesc, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
           }
           ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
@@ -247,8 +266,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     uint32_t abuf = 0, aphase = 0, it = 0;
     for (int t = cid; t < num_tiles; t += ncl) {
-      int mb, nb;
-      tile_coords(t, p, mb, nb);
+      int mb, nb, ks, kb0, kb1;
+      unit_coords(t, mb, nb, ks, kb0, kb1);
       bool ok = wait_bar(accf_bar(abuf), aphase, p.timeout_ns, abort_flag, p.err,
                          WAIT_EPI_ACC_FULL);
       ok = __all_sync(0xffffffffu, ok);
@@ -256,9 +275,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::MMA_N;
       const int row0 = mb * 2 * C::BM + static_cast<int>(rank) * C::BM + q * 32;
-      epilogue_tile<C::INTERLEAVED, C::BN, C::FP8>(
-          tacc, row0, nb * C::BN, h * (NC / 2), (h + 1) * (NC / 2), &tmY, p.M, p.N, smem, base,
-          stg_base, it, lane, ptx::mapa_shared(acce_bar(abuf), 0), gs, us);
+      if (C::LINEAR)
+        epilogue_tile_linear<C::BN>(tacc, row0, nb * C::BN, h * (NC / 2), (h + 1) * (NC / 2), &tmY,
+                                    p, ks, smem, base, stg_base, it, lane,
+                                    ptx::mapa_shared(acce_bar(abuf), 0));
+      else
+        epilogue_tile<C::INTERLEAVED, C::BN, C::FP8>(
+            tacc, row0, nb * C::BN, h * (NC / 2), (h + 1) * (NC / 2), &tmY, p.M, p.N, smem, base,
+            stg_base, it, lane, ptx::mapa_shared(acce_bar(abuf), 0), gs, us);
       if (++abuf == 2) {
         abuf = 0;
         aphase ^= 1u;

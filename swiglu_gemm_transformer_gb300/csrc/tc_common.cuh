@@ -33,6 +33,12 @@ struct KParams {
   // FP8 operands only: device pointers to the per-tensor scales of A, W1, W2
   // (the gate and up products are scaled by sA*sW1 and sA*sW2).
   const float *sA, *sW1, *sW2;
+  // Linear mode only (Z = X W + R): the residual R [M,N] BF16 (or null), and
+  // split-K: k_splits slices of kb_per_split K steps each; with k_splits > 1
+  // every slice writes FP32 partial sums to ws[slice][M][N] instead of Z.
+  const void *R;
+  float *ws;
+  int32_t k_splits, kb_per_split;
 };
 
 // Bounded wait, slow path.  Returns false on timeout or when another role of
@@ -186,6 +192,84 @@ __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, in
     __syncwarp();
     if (lane == 0) {
       if (row0 < M && ccol < N) ptx::tma_store_2d(tmY, stg, ccol, row0);
+      ptx::bulk_commit();
+    }
+    ++it;
+  }
+}
+
+// Linear-mode epilogue of one accumulator tile for one warp: Z = acc (+ R),
+// rounded to BF16 and stored through the staging buffers with TMA (k_splits
+// == 1), or the FP32 partial sums written to the workspace slice (k_splits > 1).
+template <int BN>
+__device__ __forceinline__ static void epilogue_tile_linear(uint32_t tacc, int row0, int col0,
+                                                            int c_begin, int c_end,
+                                                            const CUtensorMap *tmZ, const KParams &p,
+                                                            int split, uint8_t *smem,
+                                                            uint32_t smem_base, uint32_t stg_base,
+                                                            uint32_t &it, int lane,
+                                                            uint32_t release) {
+  if (c_begin >= c_end) {
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_cluster(release);
+    return;
+  }
+  const int row = row0 + lane;
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; ++c) {
+    const int ccol = col0 + c * 32;
+    // residual for this thread's row, 8 columns per 16-byte load (N % 8 == 0)
+    uint4 rv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                   make_uint4(0, 0, 0, 0)};
+    if (p.R != nullptr && p.k_splits == 1 && row < p.M) {
+      const uint4 *rp = reinterpret_cast<const uint4 *>(
+          static_cast<const __nv_bfloat16 *>(p.R) + static_cast<int64_t>(row) * p.N + ccol);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (ccol + 8 * j < p.N) rv[j] = __ldg(rp + j);
+    }
+    uint32_t v[32];
+    ptx::tmem_ld32(tacc + c * 32, v);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(v);
+    if (c == c_end - 1) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(release);
+    }
+    if (p.k_splits > 1) {
+      if (row < p.M) {
+        float4 *wp = reinterpret_cast<float4 *>(
+            p.ws + (static_cast<int64_t>(split) * p.M + row) * p.N + ccol);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (ccol + 4 * j < p.N)
+            wp[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+      }
+      continue;
+    }
+    uint32_t packed[16];
+    const __nv_bfloat162 *r2 = reinterpret_cast<const __nv_bfloat162 *>(rv);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 rf = __bfloat1622float2(r2[i]);
+      packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]) + rf.x, __uint_as_float(v[2 * i + 1]) + rf.y);
+    }
+    const uint32_t stg = stg_base + (it & 1u) * 2048u;
+    if (lane == 0) ptx::bulk_wait_read<1>();
+    __syncwarp();
+    uint4 *rowp = reinterpret_cast<uint4 *>(smem + (stg - smem_base) + lane * 64);
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      rowp[i ^ sw] =
+          make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (row0 < p.M && ccol < p.N) ptx::tma_store_2d(tmZ, stg, ccol, row0);
       ptx::bulk_commit();
     }
     ++it;

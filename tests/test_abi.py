@@ -127,3 +127,25 @@ def test_fp8_argument_validation(lib):
     assert lib.swiglu_pack_interleaved_fp8(W1_, W2_, Y_, 64, 24, None) == sg.ERR_MISALIGNED
     assert lib.swiglu_pack_interleaved_fp8(W1_, W2_, W1_, 64, 64, None) == sg.ERR_INVALID_ARG
     assert lib.swiglu_pack_interleaved_fp8(W1_, W2_, Y_, 0, 64, None) == sg.OK
+
+
+def test_linear_and_mlp_validation(lib):
+    ws = 0x60000000
+    assert lib.swiglu_linear(A_, W1_, None, Y_, -1, 64, 64, None, 0, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_linear(A_, W1_, None, Y_, 64, 60, 64, None, 0, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_linear(A_, W1_, None, A_ + 32, 64, 64, 64, None, 0, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_linear(A_, W1_, Y_ + 64, Y_, 64, 64, 64, None, 0, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_linear(A_, W1_, None, Y_, 0, 64, 64, None, 0, None) == sg.OK
+    assert lib.swiglu_mlp(A_, W1_, W2_, W1_, None, Y_, 64, 64, 64, None, 0, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_mlp(A_, W1_, W2_, W1_, None, Y_, 64, 64, 64, ws, 100, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_mlp(A_, W1_, W2_, W1_, None, Y_, 64, 64, 64, Y_, 1 << 20, None) == sg.ERR_INVALID_ARG
+
+
+def test_workspace_sizes(lib):
+    # 0.5B down projection, M = 128: 7 tiles of 128 columns -> split K over the 76 CTA pairs
+    n = lib.swiglu_linear_workspace_size(128, 896, 4864)
+    assert n > 0 and n % (128 * 896 * 4) == 0
+    assert lib.swiglu_linear_workspace_size(8192, 896, 4864) == 0      # enough tiles: no split
+    assert lib.swiglu_linear_workspace_size(128, 896, 4864) % (128 * 896 * 4 * 2) == 0
+    assert lib.swiglu_mlp_workspace_size(128, 896, 4864) == 128 * 4864 * 2 + n
+    assert lib.swiglu_linear_workspace_size(0, 896, 4864) == 0

@@ -253,3 +253,12 @@ def test_parity_report_flags_errors():
     nan = ref.copy()
     nan[3] = np.nan
     assert not oracle.parity_report(nan, ref)["ok"]
+
+
+def test_parity_report_mismatch_fraction():
+    ref = np.linspace(1, 2, 1000)
+    y = ref.copy()
+    y[:2] *= 1.011              # 2 of 1000 significant elements 1.1 % off, inside bound (1)
+    assert not oracle.parity_report(y, ref)["ok"]
+    assert not oracle.parity_report(y, ref, max_sig_mismatch_frac=1e-3)["ok"]
+    assert oracle.parity_report(y, ref, max_sig_mismatch_frac=2e-3)["ok"]
