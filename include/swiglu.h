@@ -179,6 +179,35 @@ int swiglu_mlp(const void *A, const void *W1, const void *W2, const void *W3, co
                void *Z, int64_t M, int64_t H, int64_t F, void *workspace,
                uint64_t workspace_bytes, void *stream);
 
+/*
+ * swiglu_mlp for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this entry point; it is a convenience of this library.
+ * Some code may not call cudaMalloc or any allocating routine: a plugin that
+ * is handed only the tensors it reads and writes, or a runtime whose device
+ * memory is planned before it runs and that forbids allocations while it
+ * executes.  This entry point takes only the inputs and the output and uses a
+ * scratch area kept inside the library:
+ *   - the area is a fixed 32 MiB of device memory
+ *     (swiglu_mlp_noalloc_scratch_bytes()), present on every GPU the library
+ *     is used on and held until the process exits;
+ *   - Y (M*F BF16 values) must fit in it: M*F*2 > 32 MiB is rejected with
+ *     SWIGLU_ERR_UNSUPPORTED before anything is enqueued; what is left of the
+ *     area holds the down projection's split-K partial sums when they fit,
+ *     and otherwise the down projection runs without splitting K;
+ *   - the first call on a device looks up the area's device address, a
+ *     host-side set-up step; make that first call before any stream capture
+ *     that would include it;
+ *   - all calls on a device share the one area, which keeps what the last call
+ *     left in it; nothing in it needs to start at zero (each call writes all
+ *     it later reads), but calls whose GPU work overlaps in time (unordered
+ *     streams, several host threads) race on it and must be serialised by the
+ *     caller.
+ * Arguments, layouts and the result are those of swiglu_mlp.
+ */
+uint64_t swiglu_mlp_noalloc_scratch_bytes(void);
+int swiglu_mlp_noalloc(const void *A, const void *W1, const void *W2, const void *W3,
+                       const void *R, void *Z, int64_t M, int64_t H, int64_t F, void *stream);
+
 /* swiglu_fused / swiglu_fused_interleaved with an explicit variant
  * (SWIGLU_VARIANT_*) instead of the library's choice; for sweeps and tests. */
 int swiglu_fused_ex(const void *A, const void *W1, const void *W2, void *Y,

@@ -40,6 +40,8 @@ EXPORTS = {
     "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
     "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
     "swiglu_mlp": ("ppppp p lll pQ p", ctypes.c_int),
+    "swiglu_mlp_noalloc_scratch_bytes": ("", ctypes.c_uint64),
+    "swiglu_mlp_noalloc": ("ppppp p lll p", ctypes.c_int),
     "swiglu_select_variant": ("lll i", ctypes.c_int),
     "swiglu_variant_name": ("i", ctypes.c_char_p),
     "swiglu_status_string": ("i", ctypes.c_char_p),
@@ -311,6 +313,26 @@ def swiglu_mlp(A, W1, W2, W3, R=None, Z=None, *, workspace=None, stream=None):
                           R.data_ptr() if R is not None else None, Z.data_ptr(), M, H, F,
                           ws.data_ptr() if ws is not None else None, nbytes, _stream(stream))
     _check("swiglu_mlp", rc)
+    return Z
+
+
+def swiglu_mlp_noalloc(A, W1, W2, W3, R, Z, *, stream=None):
+    """swiglu_mlp without any device allocation, for callers that may not
+    allocate: Y lives in the library's fixed 32 MiB scratch area.  Z must be
+    given; calls on one device whose GPU work overlaps must be serialised."""
+    bf = __import__("torch").bfloat16
+    for t, n in ((A, "A"), (W1, "W1"), (W2, "W2"), (W3, "W3"), (Z, "Z")):
+        _need(t, n, bf)
+    M, H = A.shape
+    F = W1.shape[1]
+    if W1.shape != (H, F) or W2.shape != (H, F) or W3.shape != (F, H) or tuple(Z.shape) != (M, H):
+        raise ValueError("shape mismatch: A [M,H], W1/W2 [H,F], W3 [F,H], Z [M,H]")
+    if R is not None:
+        _need(R, "R", bf)
+    rc = lib().swiglu_mlp_noalloc(A.data_ptr(), W1.data_ptr(), W2.data_ptr(), W3.data_ptr(),
+                                  R.data_ptr() if R is not None else None, Z.data_ptr(), M, H, F,
+                                  _stream(stream))
+    _check("swiglu_mlp_noalloc", rc)
     return Z
 
 
