@@ -72,6 +72,14 @@ def _load():
         lib.oracle_linear_bf16.restype = ctypes.c_int
         lib.oracle_mlp_bf16.argtypes = [p, p, p, p, p, i64, i64, i64, p, i64, p, p]
         lib.oracle_mlp_bf16.restype = ctypes.c_int
+        lib.oracle_f64_to_e4m3.argtypes = [d]
+        lib.oracle_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_f64_to_e4m3_n.argtypes = [p, i64, p]
+        lib.oracle_f64_to_e4m3_n.restype = None
+        lib.oracle_rmsnorm_bf16.argtypes = [p, p, d, i64, i64, p]
+        lib.oracle_rmsnorm_bf16.restype = ctypes.c_int
+        lib.oracle_quant_e4m3.argtypes = [p, i64, p, p]
+        lib.oracle_quant_e4m3.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -246,3 +254,47 @@ def mlp_bf16(A, W1, W2, W3, R=None, rows=None, with_y: bool = False):
 
 
 from .check import parity_report, assert_parity  # noqa: E402,F401
+
+
+# ---- the producer: RMSNorm and per-tensor E4M3 quantisation ----------------
+
+def f64_to_e4m3(x) -> np.ndarray:
+    """Round each value to FP8 E4M3 (ties to even, saturating at +-448);
+    returns the codes as uint8 with the input's shape."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    q = np.empty(a.shape, dtype=np.uint8)
+    _load().oracle_f64_to_e4m3_n(_ptr(a), a.size, _ptr(q))
+    return q
+
+
+def rmsnorm_bf16(X, gamma=None, eps: float = 1e-6) -> np.ndarray:
+    """a[m,k] = x[m,k] * gamma[k] / sqrt(mean_k x[m,k]^2 + eps), in double.
+    X [M,K] and gamma [K] are BF16 bit patterns (gamma None = all ones)."""
+    X = _u16(X)
+    M, K = X.shape
+    g = None if gamma is None else _u16(gamma)
+    if g is not None and g.shape != (K,):
+        raise ValueError("gamma must have K elements")
+    A = np.empty((M, K), dtype=np.float64)
+    rc = _load().oracle_rmsnorm_bf16(_ptr(X), _ptr(g) if g is not None else None, float(eps),
+                                     M, K, _ptr(A))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_bf16 failed (K = 0 or eps < 0)")
+    return A
+
+
+def quant_e4m3(a):
+    """Per-tensor quantisation: returns (scale, codes) with scale =
+    float32(max|a| / 448) and codes = E4M3(a / scale) (all zero if scale is 0)."""
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    q = np.empty(a.shape, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.float32)
+    rc = _load().oracle_quant_e4m3(_ptr(a), a.size, _ptr(s), _ptr(q))
+    if rc != 0:
+        raise ValueError("oracle_quant_e4m3 failed (NaN input)")
+    return float(s[0]), q
+
+
+def rmsnorm_quant_e4m3(X, gamma=None, eps: float = 1e-6):
+    """RMSNorm then per-tensor E4M3 quantisation: returns (scale, codes [M,K])."""
+    return quant_e4m3(rmsnorm_bf16(X, gamma, eps))

@@ -415,3 +415,99 @@ int oracle_mlp_bf16(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
     free(w3);
     return rc;
 }
+
+/* ---- the producer: RMSNorm and per-tensor FP8 quantisation of A --------
+ *
+ * The step that feeds the FP8 form of the projection.  The page names FP8
+ * quantisation as what raises the tensor cores' arithmetic density (section
+ * "Definizione del Problema") but defines neither the normalisation nor the
+ * scaling, so these follow the plainest readings, listed in the design notes:
+ *   - RMSNorm (root-mean-square layer normalisation, Zhang and Sennrich 2019):
+ *     a[m,k] = x[m,k] * gamma[k] / sqrt(mean over k of x[m,k]^2 + eps);
+ *   - one scale for the whole tensor: s = max|a| / 448 (448 = the largest
+ *     finite E4M3 value), rounded once to binary32 because the projection
+ *     takes its scales as floats; s = 0 when every a is zero;
+ *   - q = E4M3(a / s): round to nearest, ties to even, saturating at +-448;
+ *     all codes are 0 when s = 0.
+ */
+
+/* Round a double to FP8 E4M3 ("fn" variant, see oracle_e4m3_to_f64), ties to
+ * even, clamping magnitudes beyond the finite range to 448.  Returns the bit
+ * pattern.  Normal values in [2^q, 2^(q+1)) have spacing 2^(q-3); below 2^-6
+ * the subnormals keep the spacing 2^-9 of the first binade. */
+uint8_t oracle_f64_to_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int e;
+    frexp(a, &e);              /* a in [2^(e-1), 2^e) */
+    int q = e - 1;
+    if (q < -6)
+        q = -6;
+    double ulp = ldexp(1.0, q - 3);
+    double m = nearbyint(a / ulp); /* exact division by a power of two; ties to even */
+    double r = m * ulp;            /* a < 448 = 14 * 2^5, so r <= 448 */
+    if (r < ldexp(1.0, -6))        /* subnormal: r = m * 2^-9, m in 0..7 */
+        return (uint8_t)(sign | (uint8_t)m);
+    int er;
+    double fr = frexp(r, &er);     /* r = fr * 2^er, fr in [0.5, 1) */
+    int biased = er - 1 + 7;
+    uint8_t mant = (uint8_t)((fr * 2.0 - 1.0) * 8.0); /* exact: 3 fraction bits */
+    return (uint8_t)(sign | (uint8_t)(biased << 3) | mant);
+}
+
+void oracle_f64_to_e4m3_n(const double *x, int64_t n, uint8_t *q)
+{
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = oracle_f64_to_e4m3(x[i]);
+}
+
+/* RMSNorm of every row of X [M,K] (BF16) in double; gamma [K] (BF16) may be
+ * NULL, meaning all ones.  Writes A [M,K]. */
+int oracle_rmsnorm_bf16(const uint16_t *X, const uint16_t *gamma, double eps,
+                        int64_t M, int64_t K, double *A)
+{
+    if (M < 0 || K <= 0 || eps < 0.0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double x = oracle_bf16_to_f64(X[m * K + k]);
+            ss += x * x;
+        }
+        double rms = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k) {
+            double g = gamma ? oracle_bf16_to_f64(gamma[k]) : 1.0;
+            A[m * K + k] = oracle_bf16_to_f64(X[m * K + k]) * g / rms;
+        }
+    }
+    return 0;
+}
+
+/* Per-tensor E4M3 quantisation of n values: *scale = (float)(max|a| / 448),
+ * q[i] = E4M3(a[i] / scale), all zero when the scale is zero. */
+int oracle_quant_e4m3(const double *a, int64_t n, float *scale, uint8_t *q)
+{
+    if (n < 0)
+        return -1;
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double v = fabs(a[i]);
+        if (isnan(v))
+            return -1;
+        if (v > amax)
+            amax = v;
+    }
+    float s = (float)(amax / 448.0);
+    *scale = s;
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = s > 0.0f ? oracle_f64_to_e4m3(a[i] / (double)s) : 0;
+    return 0;
+}

@@ -186,3 +186,50 @@ def test_planted_mlp_mistake_is_caught(tmp_path, name):
     assert src.count(old) >= 1, f"mutation site for {name} not found in the oracle source"
     lib = _build(tmp_path, name, src.replace(old, new, 1))
     assert not _mlp_pins_pass(lib), f"pins did not catch mutant {name}"
+
+
+# Planted mistakes in the producer (RMSNorm and E4M3 quantisation), caught by
+# the producer pins of test_oracle_producer_pins.py.
+PRODUCER_MUTANTS = {
+    "eps_outside_sqrt": ("double rms = sqrt(ss / (double)K + eps);", "double rms = sqrt(ss / (double)K) + eps;"),
+    "mean_over_k_minus_1": ("double rms = sqrt(ss / (double)K + eps);", "double rms = sqrt(ss / (double)(K - 1) + eps);"),
+    "drops_gamma": ("double g = gamma ? oracle_bf16_to_f64(gamma[k]) : 1.0;", "double g = 1.0;"),
+    "e4m3_truncates": ("double m = nearbyint(a / ulp); /* exact division by a power of two; ties to even */\n    double r = m * ulp;            /* a < 448",
+                       "double m = floor(a / ulp); /* exact division by a power of two; ties to even */\n    double r = m * ulp;            /* a < 448"),
+    "e4m3_ties_away": ("double m = nearbyint(a / ulp); /* exact division by a power of two; ties to even */\n    double r = m * ulp;            /* a < 448",
+                       "double m = round(a / ulp); /* exact division by a power of two; ties to even */\n    double r = m * ulp;            /* a < 448"),
+    "e4m3_no_saturation": ("if (a >= 448.0)\n        return (uint8_t)(sign | 0x7E);", ""),
+    "e4m3_subnormal_spacing": ("if (q < -6)\n        q = -6;", "if (q < -7)\n        q = -7;"),
+    "scale_not_448": ("float s = (float)(amax / 448.0);", "float s = (float)(amax / 240.0);"),
+    "quant_drops_sign": ("oracle_f64_to_e4m3(a[i] / (double)s)", "oracle_f64_to_e4m3(fabs(a[i]) / (double)s)"),
+}
+
+
+def _build_producer(tmp_path, name, src_text):
+    lib = _build(tmp_path, name, src_text)
+    p, i64, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+    lib.oracle_f64_to_e4m3_n.argtypes = [p, i64, p]
+    lib.oracle_f64_to_e4m3_n.restype = None
+    lib.oracle_rmsnorm_bf16.argtypes = [p, p, d, i64, i64, p]
+    lib.oracle_quant_e4m3.argtypes = [p, i64, p, p]
+    return lib
+
+
+def test_unmodified_oracle_passes_producer_pins(tmp_path):
+    from test_oracle_producer_pins import producer_pin_failures
+    lib = _build_producer(tmp_path, "orig_producer", open(SRC).read())
+    assert producer_pin_failures(lib) == []
+
+
+@pytest.mark.parametrize("name", sorted(PRODUCER_MUTANTS))
+def test_planted_producer_mistake_is_caught(tmp_path, name):
+    from test_oracle_producer_pins import producer_pin_failures
+    src = open(SRC).read()
+    old, new = PRODUCER_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique in the oracle source"
+    lib = _build_producer(tmp_path, name, src.replace(old, new, 1))
+    try:
+        failures = producer_pin_failures(lib)
+    except AssertionError:      # the mutant broke a call outright
+        failures = ["call failed"]
+    assert failures, f"pins did not catch mutant {name}"
