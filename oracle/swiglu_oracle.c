@@ -423,7 +423,8 @@ int oracle_mlp_bf16(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
  * "Definizione del Problema") but defines neither the normalisation nor the
  * scaling, so these follow the plainest readings, listed in the design notes:
  *   - RMSNorm (root-mean-square layer normalisation, Zhang and Sennrich 2019):
- *     a[m,k] = x[m,k] * gamma[k] / sqrt(mean over k of x[m,k]^2 + eps);
+ *     a[m,k] = x[m,k] * gamma[k] / sqrt(mean over k of x[m,k]^2 + eps); a row
+ *     of zeros with eps = 0, where that is 0/0, normalises to zeros;
  *   - one scale for the whole tensor: s = max|a| / 448 (448 = the largest
  *     finite E4M3 value), rounded once to binary32 because the projection
  *     takes its scales as floats; s = 0 when every a is zero;
@@ -485,7 +486,7 @@ int oracle_rmsnorm_bf16(const uint16_t *X, const uint16_t *gamma, double eps,
         double rms = sqrt(ss / (double)K + eps);
         for (int64_t k = 0; k < K; ++k) {
             double g = gamma ? oracle_bf16_to_f64(gamma[k]) : 1.0;
-            A[m * K + k] = oracle_bf16_to_f64(X[m * K + k]) * g / rms;
+            A[m * K + k] = rms > 0.0 ? oracle_bf16_to_f64(X[m * K + k]) * g / rms : 0.0;
         }
     }
     return 0;

@@ -15,7 +15,9 @@ than itself:
   routine) on random float32 values in range;
 * RMSNorm closed forms: a constant row normalises to +-gamma, a one-hot row
   to sqrt(K) gamma_j, mean(a^2) = 1 for gamma = 1 and eps = 0, invariance under
-  scaling x by a power of two, linearity in gamma, rows independent;
+  scaling x by a power of two, linearity in gamma, rows independent, and a
+  zero row with eps = 0 (0/0) normalises to zeros, the reading the oracle and
+  the kernels share;
 * quantisation: the largest |a| maps to code +-448, every code is the nearest
   one (the error is at most half the local spacing), an all-zero input gives
   scale 0 and zero codes.
@@ -146,6 +148,9 @@ def producer_pin_failures(lib):
     if not (np.allclose(Ag2, 2 * Ag, rtol=1e-15, atol=0)
             and np.allclose(Ag, A * gam.double().numpy(), rtol=1e-14, atol=1e-15)):
         bad.append("gamma is not a per-column factor")
+    z = _rms(lib, _bits(np.zeros((2, K))), None, 0.0)
+    if not (np.all(z == 0) and not np.signbit(z).any()):
+        bad.append("zero row with eps = 0 does not normalise to +0")
     perm = np.random.default_rng(2).permutation(11)
     if not np.array_equal(_rms(lib, np.ascontiguousarray(xb[perm]), None, 1e-3), _rms(lib, xb, None, 1e-3)[perm]):
         bad.append("rows not independent")
