@@ -78,9 +78,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_digest() -> str:
+def source_digest(files=None) -> str:
+    """Hash of the kernel sources a capture was taken on: the named files of
+    the CUDA source folder, or all of them."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in sorted(files or os.listdir(CSRC)):
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -95,7 +97,7 @@ def load_traffic(kernel_key: str):
     except Exception:
         return None
     ent = d.get(kernel_key)
-    if not ent or ent.get("source_digest") != source_digest():
+    if not ent or ent.get("source_digest") != source_digest(ent.get("sources")):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -327,17 +329,19 @@ class Workload:
             fn()
 
 
-def measure_calls(wl, stream, launches):
+def measure_calls(wl, stream, launches, factory=None):
     """Average duration (us) of each call of the step, launched alone and back
     to back inside a CUDA graph, rotating over copies of its inputs so that
-    the copies together exceed 2.5x the L2 size."""
+    the copies together exceed 2.5x the L2 size.  ``factory(form, M, v, bufs)``
+    builds the launch closure (default: the fused call through the C ABI)."""
     import torch
+    factory = factory or wl.launcher
     out = []
     for (form, M, v), bufs in zip(wl.calls, wl.buffers):
         per = wl.algorithmic_bytes(M)
         ncopy = max(2, min(24, math.ceil(2.5 * L2_BYTES / per)))
         copies = [bufs] + [tuple(t.clone() for t in bufs) for _ in range(ncopy - 1)]
-        fns = [wl.launcher(form, M, v, cb) for cb in copies]
+        fns = [factory(form, M, v, cb) for cb in copies]
         reps = max(1, math.ceil(launches / ncopy))
 
         def body():
@@ -345,6 +349,8 @@ def measure_calls(wl, stream, launches):
                 for f in fns:
                     f()
         with torch.cuda.stream(stream):
+            for f in fns:       # first calls outside the capture (module loads, compilation)
+                f()
             g = capture(body, stream)
             g.replay()
             e0 = torch.cuda.Event(enable_timing=True)
@@ -559,24 +565,78 @@ def run_e2e(args, wl, stream, ws):
                     "(pinned host memory), copies and kernels pipelined over three streams"}
 
 
-def run_unfused_context(wl, stream, steps):
-    """Context only: the unfused eager path (cuBLAS GEMMs, SiLU, multiply) on the same inputs."""
+def unfused_fn(wl, form):
+    """The unfused computation of one call in plain torch: the gate and up
+    products as separate cuBLAS GEMMs (one GEMM on W_fused for the
+    interleaved form), then SiLU and the product as separate kernels."""
     import torch
     import torch.nn.functional as F
+    if wl.kind == "mlp":
+        return lambda A, W1, W2, W3: (F.silu(A @ W1) * (A @ W2)) @ W3
+    if form == "separate":
+        return lambda A, W1, W2: F.silu(A @ W1) * (A @ W2)
+
+    def interleaved(A, Wf):
+        D = A @ Wf
+        return F.silu(D[:, 0::2]) * D[:, 1::2]
+    return interleaved
+
+
+def unfused_factory(wl, compiled=False):
+    """Launch-closure factory for measure_calls running the unfused path
+    (eager, or the torch.compile'd version of the same function).  The result
+    goes to a tensor the graph's memory pool provides, as in a model."""
+    import torch
+    fns = {}
+
+    def factory(form, M, v, bufs):
+        if form not in fns:
+            f = unfused_fn(wl, form)
+            fns[form] = torch.compile(f, dynamic=False, fullgraph=True) if compiled else f
+        f = fns[form]
+        ins = bufs[:4] if wl.kind == "mlp" else bufs[:3] if form == "separate" else bufs[:2]
+        return lambda: f(*ins)
+    return factory
+
+
+def fusion_report(wl, fused_us, eager_us, hbm_gbs):
+    """Fusion efficiency per call: the time fusion actually saved against the
+    eager unfused path, over the time the eliminated intermediate traffic
+    would take at the measured HBM bandwidth.  The eliminated traffic is the
+    gate and up tensors written and read once each (8·M·N bytes in BF16; for
+    the interleaved form the [M, 2N] product, the same bytes).  Also the
+    arithmetic-intensity increase: unfused bytes over fused bytes, minus one."""
+    rows = []
+    for (form, M, v), tf, te in zip(wl.calls, fused_us, eager_us):
+        saved_bytes = 8 * M * wl.N
+        t_theory = saved_bytes / (hbm_gbs * 1e9) * 1e6
+        fb = wl.algorithmic_bytes(M)
+        rows.append({"form": form, "M": M, "fused_us": round(tf, 3), "eager_us": round(te, 3),
+                     "speedup": round(te / tf, 3),
+                     "bytes_eliminated": saved_bytes, "t_eliminated_theory_us": round(t_theory, 3),
+                     "fusion_efficiency": round((te - tf) / t_theory, 3),
+                     "ai_increase": round((fb + saved_bytes) / fb - 1.0, 3)})
+    return rows
+
+
+def run_context(args, wl, stream, fused_us, hbm_gbs):
+    """Context only: the unfused eager path (cuBLAS GEMMs, SiLU, multiply) on
+    the same inputs, per call and as one step; fusion efficiency per call;
+    optionally the same function under torch.compile."""
+    import torch
     if wl.fp8:
         return None
+    factory = unfused_factory(wl)
+    eager_us = measure_calls(wl, stream, args.call_launches, factory)
+
+    fns = [factory(form, M, v, bufs) for (form, M, v), bufs in zip(wl.calls, wl.buffers)]
 
     def step():
-        for (form, M, v), bufs in zip(wl.calls, wl.buffers):
-            if wl.kind == "mlp":
-                A, W1, W2, W3, Z = bufs[:5]
-                torch.matmul(F.silu(A @ W1) * (A @ W2), W3, out=Z)
-            elif form == "separate":
-                A, W1, W2, Y = bufs
-                torch.mul(F.silu(A @ W1), A @ W2, out=Y)
+        for f in fns:
+            f()
+    steps = min(args.steps, 200)
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
+        step()
         g = capture(step, stream)
         for _ in range(3):
             g.replay()
@@ -588,10 +648,34 @@ def run_unfused_context(wl, stream, steps):
         e1.record()
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    flops = sum(wl.flops_of(M) for (f, M, _) in wl.calls if f in ("separate", "mlp"))
     what = ("torch eager: (silu(A@W1) * (A@W2)) @ W3 (cuBLAS)" if wl.kind == "mlp" else
-            "torch eager: A@W1, A@W2 (cuBLAS), silu, mul; separate-weight calls only")
-    return {"what": what, "ms_per_step": round(ms, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
+            "torch eager: A@W1, A@W2 (cuBLAS; one A@W_fused GEMM for the interleaved form), "
+            "silu, mul")
+    out = {"eager": {"what": what, "ms_per_step": round(ms, 5),
+                     "tflops": round(wl.flops / (ms * 1e-3) / 1e12, 2),
+                     "per_call_us": [round(u, 3) for u in eager_us]},
+           "fusion": fusion_report(wl, fused_us, eager_us, hbm_gbs)}
+    if args.compile_context:
+        out["compile"] = run_compile_context(args, wl, stream, fused_us)
+    return out
+
+
+def run_compile_context(args, wl, stream, fused_us):
+    """The same unfused function under torch.compile (default mode, static
+    shapes), timed per call like the fused calls."""
+    import torch
+    if "TRITON_PTXAS_PATH" not in os.environ and os.path.exists("/usr/local/cuda/bin/ptxas"):
+        os.environ["TRITON_PTXAS_PATH"] = "/usr/local/cuda/bin/ptxas"
+    t0 = time.time()
+    try:
+        comp_us = measure_calls(wl, stream, args.call_launches, unfused_factory(wl, compiled=True))
+    except Exception as e:  # report, do not fail the benchmark line
+        return {"error": f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"}
+    return {"what": f"torch.compile(fullgraph=True, dynamic=False) of the eager function, "
+                    f"torch {torch.__version__}",
+            "compile_and_time_s": round(time.time() - t0, 1),
+            "per_call_us": [round(u, 3) for u in comp_us],
+            "fused_speedup_vs_compile": [round(c / f, 3) for c, f in zip(comp_us, fused_us)]}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
@@ -689,7 +773,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", default="auto",
                     choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n32_mc2",
-                             "1sm_n32_mc4", "1sm_n64_mc2", "1sm_n128_mc2"))
+                             "1sm_n32_mc4", "1sm_n64_mc2", "1sm_n128_mc2", "1sm_n64_sk2"))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--call-launches", type=int, default=96,
                     help="launches per call when timing calls one by one")
@@ -698,6 +782,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--compile-context", action="store_true",
+                    help="also time the unfused function under torch.compile (context)")
     ap.add_argument("--only", default="",
                     help="restrict the step to calls FORM:M[,FORM:M...] (profiling a single kernel)")
     args = ap.parse_args()
@@ -719,7 +805,9 @@ def main():
         out, wl, stream = run_ours(args, ws, rank, local)
         out["e2e"] = None if args.no_e2e else run_e2e(args, wl, stream, ws)
         if not args.no_context:
-            out["context_unfused_torch"] = run_unfused_context(wl, stream, min(args.steps, 200))
+            peaks, _ = load_peaks()
+            out["context"] = run_context(args, wl, stream, [k["us"] for k in out["kernels"]],
+                                         peaks["hbm_gbs"])
         if rank == 0:
             if args.no_cpu_baseline or ws > 1:
                 out["cpu_baseline"] = None

@@ -74,7 +74,12 @@ typedef enum {
     SWIGLU_VARIANT_1SM_N32_MC4 = 6,
     SWIGLU_VARIANT_1SM_N64_MC2 = 7,
     SWIGLU_VARIANT_1SM_N128_MC2 = 8,
-    SWIGLU_VARIANT_COUNT_ = 9
+    /* split-K over a cluster of 2 CTAs (small M): each CTA multiplies half of
+       the K steps of one 128-row x 64-column tile and the two partial gate/up
+       accumulators are summed through distributed shared memory before the
+       activation; all of a CTA's weight and A bytes fit in flight at once */
+    SWIGLU_VARIANT_1SM_N64_SK2 = 9,
+    SWIGLU_VARIANT_COUNT_ = 10
 } swiglu_variant;
 
 /*
@@ -143,6 +148,40 @@ int swiglu_fused_interleaved_fp8(const void *Aq, const void *Wfused_t, const flo
  * in transposed storage).  W1t, W2t: E4M3 [N,K]; Wfused_t: E4M3 [2N,K]. */
 int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t, int64_t N,
                                 int64_t K, void *stream);
+
+/*
+ * The producer of the FP8 form's A operand: RMSNorm of each row of X followed
+ * by per-tensor E4M3 quantisation (FP8 quantisation is what the page's
+ * section "Definizione del Problema" names as raising tensor-core density; the
+ * page defines neither step, so both follow the standard definitions):
+ *     a[m,k] = x[m,k] * gamma[k] / sqrt(mean_k x[m,k]^2 + eps)
+ *     *sA    = max|a| / 448          (448 = largest finite E4M3 value)
+ *     Aq     = E4M3(a / *sA)         (round to nearest even, saturating)
+ * A row whose mean square plus eps is zero gives zeros; *sA = 0 gives all-zero
+ * codes.  Arithmetic is FP32; a code may differ from the exactly rounded one
+ * only where a / *sA lies within FP32 rounding of a midpoint between codes.
+ *   X     : device, BF16 [M,K] row-major (read)
+ *   gamma : device, BF16 [K] (read), or NULL for all ones
+ *   eps   : finite, >= 0
+ *   Aq    : device, E4M3 [M,K] row-major (written), the Aq of swiglu_fused_fp8
+ *   sA    : device, one float (written), the sA of swiglu_fused_fp8
+ * K must be a positive multiple of 16; X, gamma and Aq 16-byte aligned.
+ * Enqueues a 4-byte memset of *sA and two kernels on `stream` (the second
+ * waits for the first through programmatic dependent launch); no host sync.
+ * Aq and *sA must not overlap X or gamma.  M = 0 writes *sA = 0 only.
+ */
+int swiglu_rmsnorm_quant_fp8(const void *X, const void *gamma, float eps, void *Aq, float *sA,
+                             int64_t M, int64_t K, void *stream);
+
+/*
+ * Per-tensor E4M3 quantisation without normalisation, for weights:
+ *     *s = max|x| / 448,   Xq = E4M3(x / *s)
+ * with the rounding and zero rules of swiglu_rmsnorm_quant_fp8.  X: device,
+ * BF16 [M,K]; Xq: device, E4M3 [M,K]; s: device float.  For the FP8 entry
+ * points' K-major weights pass the [N,K] transpose of W (rows of K).  K a
+ * positive multiple of 16, X and Xq 16-byte aligned.
+ */
+int swiglu_quant_fp8(const void *X, void *Xq, float *s, int64_t M, int64_t K, void *stream);
 
 /*
  * The down projection that completes the MLP block the page studies (section
@@ -238,6 +277,19 @@ int swiglu_device_status(void *stream, uint32_t *detail);
 /* Time limit of every device-side wait, in nanoseconds (default 2e9, i.e. two
  * seconds; minimum 1e6).  Applies to launches enqueued after the call. */
 int swiglu_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Promise about the weights of later calls (default 0 = no promise).  With
+ * on = 1 the caller guarantees that no work enqueued on a stream before a
+ * call writes that call's weight matrices (true of model parameters loaded
+ * once); the BF16 kernels may then start loading the weights of their first
+ * K steps while the preceding kernel on the stream is still finishing
+ * (programmatic dependent launch), and load A and write Y only after it has
+ * completed.  With on = 0 every load waits for the preceding kernel.  A call
+ * that breaks the promise may read stale weights.  Process-wide; applies to
+ * calls made after it.  Returns SWIGLU_ERR_INVALID_ARG unless on is 0 or 1.
+ */
+int swiglu_set_weights_read_only(int32_t on);
 
 /*
  * Failure-detection self test: enqueues one small kernel whose single wait

@@ -20,11 +20,13 @@ LIB_PATH = os.path.join(_HERE, "libswiglu_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
 (VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64, VARIANT_2SM_N128, VARIANT_1SM_N32,
- VARIANT_1SM_N32_MC2, VARIANT_1SM_N32_MC4, VARIANT_1SM_N64_MC2, VARIANT_1SM_N128_MC2) = range(9)
+ VARIANT_1SM_N32_MC2, VARIANT_1SM_N32_MC4, VARIANT_1SM_N64_MC2, VARIANT_1SM_N128_MC2,
+ VARIANT_1SM_N64_SK2) = range(10)
 VARIANTS = {"auto": VARIANT_AUTO, "1sm_n128": VARIANT_1SM_N128, "1sm_n64": VARIANT_1SM_N64,
             "2sm_n128": VARIANT_2SM_N128, "1sm_n32": VARIANT_1SM_N32,
             "1sm_n32_mc2": VARIANT_1SM_N32_MC2, "1sm_n32_mc4": VARIANT_1SM_N32_MC4,
-            "1sm_n64_mc2": VARIANT_1SM_N64_MC2, "1sm_n128_mc2": VARIANT_1SM_N128_MC2}
+            "1sm_n64_mc2": VARIANT_1SM_N64_MC2, "1sm_n128_mc2": VARIANT_1SM_N128_MC2,
+            "1sm_n64_sk2": VARIANT_1SM_N64_SK2}
 
 EXPORTS = {
     # name: (argtypes, restype)
@@ -36,6 +38,8 @@ EXPORTS = {
     "swiglu_fused_fp8": ("ppp ppp p lll p", ctypes.c_int),
     "swiglu_fused_interleaved_fp8": ("pp ppp p lll p", ctypes.c_int),
     "swiglu_pack_interleaved_fp8": ("ppp ll p", ctypes.c_int),
+    "swiglu_rmsnorm_quant_fp8": ("pp f pp ll p", ctypes.c_int),
+    "swiglu_quant_fp8": ("ppp ll p", ctypes.c_int),
     "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
     "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
     "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
@@ -47,9 +51,10 @@ EXPORTS = {
     "swiglu_status_string": ("i", ctypes.c_char_p),
     "swiglu_device_status": ("p P", ctypes.c_int),
     "swiglu_set_wait_timeout_ns": ("Q", ctypes.c_int),
+    "swiglu_set_weights_read_only": ("i", ctypes.c_int),
     "swiglu_selftest_wait_timeout": ("I p", ctypes.c_int),
 }
-_CT = {"p": ctypes.c_void_p, "l": ctypes.c_int64, "i": ctypes.c_int32, "Q": ctypes.c_uint64,
+_CT = {"p": ctypes.c_void_p, "l": ctypes.c_int64, "f": ctypes.c_float, "i": ctypes.c_int32, "Q": ctypes.c_uint64,
        "I": ctypes.c_uint32, "P": ctypes.POINTER(ctypes.c_uint32)}
 
 _lock = threading.Lock()
@@ -253,6 +258,48 @@ def swiglu_pack_interleaved_fp8(W1t, W2t, Wfused_t=None, *, stream=None):
     return Wfused_t
 
 
+def _quant_outputs(X, Xq, s):
+    import torch
+    if Xq is None:
+        Xq = torch.empty(X.shape, dtype=torch.float8_e4m3fn, device=X.device)
+    else:
+        _fp8(Xq, "Xq")
+        if Xq.shape != X.shape:
+            raise ValueError("the codes must have the shape of X")
+    if s is None:
+        s = torch.empty(1, dtype=torch.float32, device=X.device)
+    return Xq, s
+
+
+def swiglu_rmsnorm_quant_fp8(X, gamma=None, eps: float = 1e-6, Aq=None, sA=None, *, stream=None):
+    """RMSNorm of the rows of X (BF16 [M,K], gamma BF16 [K] or None) then
+    per-tensor E4M3 quantisation; returns (Aq, sA) for swiglu_fused_fp8."""
+    import torch
+    _need(X, "X", torch.bfloat16)
+    M, K = X.shape
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, ndim=1)
+        if gamma.numel() != K:
+            raise ValueError("gamma must have K elements")
+    Aq, sA = _quant_outputs(X, Aq, sA)
+    rc = lib().swiglu_rmsnorm_quant_fp8(X.data_ptr(), gamma.data_ptr() if gamma is not None else None,
+                                        float(eps), Aq.data_ptr(), _scale(sA, "sA"), M, K,
+                                        _stream(stream))
+    _check("swiglu_rmsnorm_quant_fp8", rc)
+    return Aq, sA
+
+
+def swiglu_quant_fp8(X, Xq=None, s=None, *, stream=None):
+    """Per-tensor E4M3 quantisation of a BF16 [M,K] matrix; returns (Xq, s)."""
+    import torch
+    _need(X, "X", torch.bfloat16)
+    M, K = X.shape
+    Xq, s = _quant_outputs(X, Xq, s)
+    rc = lib().swiglu_quant_fp8(X.data_ptr(), Xq.data_ptr(), _scale(s, "s"), M, K, _stream(stream))
+    _check("swiglu_quant_fp8", rc)
+    return Xq, s
+
+
 def _workspace(nbytes, device, workspace):
     import torch
     if workspace is None:
@@ -349,6 +396,13 @@ def swiglu_device_status(stream=None):
 
 def swiglu_set_wait_timeout_ns(ns: int):
     _check("swiglu_set_wait_timeout_ns", lib().swiglu_set_wait_timeout_ns(int(ns)))
+
+
+def swiglu_set_weights_read_only(on: bool):
+    """Promise that no earlier work on a stream writes a later call's weights
+    (model parameters): lets the kernels start streaming weights before the
+    preceding kernel finishes."""
+    _check("swiglu_set_weights_read_only", lib().swiglu_set_weights_read_only(1 if on else 0))
 
 
 def swiglu_selftest_wait_timeout(timeout_us: int, stream=None):

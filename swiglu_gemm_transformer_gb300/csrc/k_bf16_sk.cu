@@ -1,0 +1,45 @@
+// k_bf16_sk.cu -- the split-K cluster kernel for small M, both weight forms.
+#include <atomic>
+
+#include "launch.h"
+#include "swiglu_sk_kernel.cuh"
+
+namespace swiglu {
+namespace {
+
+template <class C>
+cudaError_t launch_sk(const LaunchArgs &la) {
+  static std::atomic<uint64_t> configured{0};
+  const uint64_t bit = 1ull << (la.device & 63);
+  auto kern = swiglu_bf16_sk_kernel<C>;
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  const int64_t tiles = int64_t(la.p.num_m_blk) * la.p.num_n_blk;  // one tile per cluster
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * tiles), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = la.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
+}
+
+}  // namespace
+
+cudaError_t launch_bf16_sk(bool interleaved, const LaunchArgs &la) {
+  return interleaved ? launch_sk<SkCfg<true>>(la) : launch_sk<SkCfg<false>>(la);
+}
+
+}  // namespace swiglu

@@ -34,6 +34,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_weights_read_only{0};
 // Down-projection tile width: 0 = chosen by shape; 128 or 256 forces it (the
 // SWIGLU_LINEAR_N environment variable, read once, sets it for tuning sweeps).
 std::atomic<int> g_linear_n{0};
@@ -183,13 +184,15 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   p.err = st->err;
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blk;
+  p.w_early = g_weights_read_only.load(std::memory_order_relaxed);
   const int64_t tiles = int64_t(p.num_m_blk) * p.num_n_blk;
   if (tiles > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   la.grid = int(tiles < st->sm_count ? tiles : st->sm_count);  // one-CTA kernels
   la.device = dev;
   la.stream = s;
-  cudaError_t e = interleaved ? launch_bf16_interleaved(variant, la)
-                              : launch_bf16_separate(variant, la);
+  cudaError_t e = variant == SWIGLU_VARIANT_1SM_N64_SK2 ? launch_bf16_sk(interleaved, la)
+                  : interleaved ? launch_bf16_interleaved(variant, la)
+                                : launch_bf16_separate(variant, la);
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
@@ -391,6 +394,7 @@ VariantGeom variant_geom(int variant, bool interleaved) {
     case SWIGLU_VARIANT_1SM_N64_MC2: return {128, 64, 64, 64, 0, 64, 1, 2};
     case SWIGLU_VARIANT_1SM_N128_MC2: return {128, 128, 64, 64, 0, 64, 1, 2};
     case SWIGLU_VARIANT_2SM_N128: return {256, 128, 64, 64, 0, 128, 2, 1};
+    case SWIGLU_VARIANT_1SM_N64_SK2: return {128, 64, 64, 64, 0, 128, 2, 1};
     case SWIGLU_VARIANT_1SM_N128:
     default: return {128, 128, 64, 64, 0, 128, 1, 1};
   }
@@ -530,6 +534,7 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_1SM_N32_MC4: return "1sm_n32_mc4";
     case SWIGLU_VARIANT_1SM_N64_MC2: return "1sm_n64_mc2";
     case SWIGLU_VARIANT_1SM_N128_MC2: return "1sm_n128_mc2";
+    case SWIGLU_VARIANT_1SM_N64_SK2: return "1sm_n64_sk2";
     default: return "?";
   }
 }
@@ -575,6 +580,12 @@ int swiglu_device_status(void *stream, uint32_t *detail) {
 int swiglu_set_wait_timeout_ns(uint64_t ns) {
   if (ns < 1000000ull) return SWIGLU_ERR_INVALID_ARG;
   g_timeout_ns.store(ns, std::memory_order_relaxed);
+  return SWIGLU_OK;
+}
+
+int swiglu_set_weights_read_only(int32_t on) {
+  if (on != 0 && on != 1) return SWIGLU_ERR_INVALID_ARG;
+  g_weights_read_only.store(on, std::memory_order_relaxed);
   return SWIGLU_OK;
 }
 

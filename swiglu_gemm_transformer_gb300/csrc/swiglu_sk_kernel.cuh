@@ -1,0 +1,382 @@
+// swiglu_sk_kernel.cuh -- split-K fused SwiGLU kernel for small M on sm_103a.
+//
+// Same result as the other kernels, Y = SiLU(A x W1) (.) (A x W2) (page
+// "Riepilogo Tecnico: Sovrapposizione delle Attivazioni a Livello di Tile per
+// l'Inferenza Efficiente di LLM", section "Definizione del Problema"), in either
+// weight form (section "Metodologia", items 1 and 2).
+//
+// Why a separate kernel: with M <= 128 the call is a stream of the weights
+// (2*K*N*2 bytes, 17.4 MB for the Qwen-2.5-0.5B MLP), and what limits it is how
+// much of that stream each SM keeps in flight.  A one-CTA tile needs all of A
+// (M x K) next to its weight columns, so a 128-row tile of 32 columns on every
+// SM holds only 8 of its 14 K steps in shared memory and waits a second DRAM
+// round trip for the rest.  Here a CLUSTER OF TWO CTAs computes one 128 x 64
+// output tile and each CTA takes half of the K steps:
+//   * per CTA: A[128 x K/2] and the tile's 64 gate + 64 up weight columns over
+//     K/2 -- half the A bytes of a one-CTA tile, and all of them in flight;
+//   * warp 4 streams its K half into a 6-stage ring (TMA, 128-byte swizzle);
+//     warp 5 issues tcgen05.mma M=128 x N=128 (gate and up side by side in
+//     TMEM, as in the one-CTA kernel) over that half;
+//   * the two partial accumulators are summed through distributed shared
+//     memory: CTA r keeps output rows [64r, 64r+64); eight epilogue warps
+//     (four TMEM lane groups x two column halves) split the work: those on
+//     the other 64 lanes send their rows' partial columns to the peer with
+//     st.async (16 bytes per store, counted on the peer's receive mbarrier);
+//     those on the kept lanes wait for the peer's half, add it to their own
+//     accumulator, apply y = g * u / (1 + e^-g) in FP32, round to BF16 and
+//     store 32 x 32 blocks through 64-byte-swizzled staging buffers with TMA.
+// Gate and up values never reach global memory.  One tile per cluster (no
+// persistent loop): the launcher sizes the grid to two CTAs per output tile.
+//
+// Every wait is bounded as in the other kernels (timeout -> error word, abort
+// flag, drain, TMEM freed).  A CTA leaves only once everything its peer
+// sends it has arrived (or, after a timeout, once late stores have had time
+// to land), so no store targets a CTA that has left.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+#include "tc_common.cuh"
+
+namespace swiglu {
+
+enum : uint32_t { WAIT_SK_RECV = 7 };
+
+template <bool INTERLEAVED_>
+struct SkCfg {
+  static constexpr bool INTERLEAVED = INTERLEAVED_;
+  static constexpr int BM = 128;                 // rows per tile (MMA M)
+  static constexpr int BK = 64;                  // K per stage
+  static constexpr int BN = 64;                  // output columns per tile
+  static constexpr int MMA_N = 2 * BN;           // gate + up accumulator columns
+  static constexpr int ATOM_COLS = 64;           // one weight box: 64 columns, 128-byte swizzle
+  static constexpr int NB_ATOMS = 2;
+  static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+  static constexpr int ROW_BYTES = ATOM_COLS * 2;
+  static constexpr int ATOM_BYTES = BK * ROW_BYTES;  // 8 KB
+  static constexpr int B_SBO = 8 * ROW_BYTES;
+  static constexpr int B_KSTEP = 16 * ROW_BYTES;
+  static constexpr int B_BYTES = NB_ATOMS * ATOM_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+  static constexpr int STAGES = 6;
+  static constexpr int HALF_ROWS = BM / 2;
+  // Receive buffer: the peer's partial accumulator for the 64 kept rows,
+  // 128 FP32 columns each, stored as [column / 4][row][4] so that a warp's 32
+  // rows read or write 512 contiguous bytes per 16-byte access.
+  static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
+  static constexpr int RECV_BYTES = HALF_ROWS * MMA_N * 4;  // 32 KB
+  static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], acc_full, recv, drain
+  static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
+  static constexpr int EPI_WARPS = 8;            // 4 TMEM lane groups x 2 column halves
+  static constexpr int PRODUCER_WARP = 8;
+  static constexpr int MMA_WARP = 9;
+  static constexpr int THREADS = 32 * 10;
+  static constexpr int TMEM_COLS = 128;
+  static constexpr int STG_BYTES = 32 * 64;      // a warp's 32 rows x 32 BF16 columns
+  static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(4 * STG_BYTES <= RECV_OFF, "staging reuses the ring");
+};
+
+// Epilogue of the kept half for one warp: 32 rows (TMEM lanes of `tacc`) x
+// the 32 output columns of chunk `c`; adds the peer's partial sums from `recv`
+// (this thread's row is receive row `rloc`), then stores Y through the 2 KB
+// staging buffer at `stg` (shared::cta address) with TMA.
+template <class C>
+__device__ __forceinline__ static void sk_epilogue_keep(uint32_t tacc, bool have_acc,
+                                                        const float4 *recv, int rloc, int c,
+                                                        int row0, int col0,
+                                                        const CUtensorMap *tmY, int M, int N,
+                                                        uint8_t *smem, uint32_t smem_base,
+                                                        uint32_t stg, int lane) {
+  // TMEM columns of this chunk's gate and up values
+  const int cg = C::INTERLEAVED ? c * 64 : c * 32;
+  const int cu = C::INTERLEAVED ? c * 64 + 32 : C::BN + c * 32;
+  uint32_t g[32], u[32];
+  if (have_acc) {
+    ptx::tmem_ld32(tacc + cg, g);
+    ptx::tmem_ld32(tacc + cu, u);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(g);
+    ptx::reg_fence(u);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 pg = recv[(cg / 4 + j) * C::HALF_ROWS + rloc];
+    const float4 pu = recv[(cu / 4 + j) * C::HALF_ROWS + rloc];
+    g[4 * j + 0] = __float_as_uint(__uint_as_float(g[4 * j + 0]) + pg.x);
+    g[4 * j + 1] = __float_as_uint(__uint_as_float(g[4 * j + 1]) + pg.y);
+    g[4 * j + 2] = __float_as_uint(__uint_as_float(g[4 * j + 2]) + pg.z);
+    g[4 * j + 3] = __float_as_uint(__uint_as_float(g[4 * j + 3]) + pg.w);
+    u[4 * j + 0] = __float_as_uint(__uint_as_float(u[4 * j + 0]) + pu.x);
+    u[4 * j + 1] = __float_as_uint(__uint_as_float(u[4 * j + 1]) + pu.y);
+    u[4 * j + 2] = __float_as_uint(__uint_as_float(u[4 * j + 2]) + pu.z);
+    u[4 * j + 3] = __float_as_uint(__uint_as_float(u[4 * j + 3]) + pu.w);
+  }
+  uint32_t packed[16];
+  if (C::INTERLEAVED) {
+    // g: (gate, up) pairs of outputs 32c..32c+15; u: outputs 32c+16..32c+31
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      packed[i] =
+          pack_bf16x2(silu_mul(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1])),
+                      silu_mul(__uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3])));
+      packed[8 + i] =
+          pack_bf16x2(silu_mul(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1])),
+                      silu_mul(__uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] =
+          pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                      silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+  }
+  const int ccol = col0 + c * 32;
+  uint4 *rowp = reinterpret_cast<uint4 *>(smem + (stg - smem_base) + lane * 64);
+  const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk i -> i ^ ((row >> 1) & 3)
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    rowp[i ^ sw] =
+        make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (row0 < M && ccol < N) ptx::tma_store_2d(tmY, stg, ccol, row0);
+    ptx::bulk_commit();
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    swiglu_bf16_sk_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB0,  // W1, or W_fused
+                          const __grid_constant__ CUtensorMap tmB1,  // W2 (separate form only)
+                          const __grid_constant__ CUtensorMap tmY, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw);
+
+  const uint32_t bars = base + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  const uint32_t accf_bar = bars + 8u * (2 * C::STAGES);
+  const uint32_t recv_bar = bars + 8u * (2 * C::STAGES + 1);
+  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 2);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());  // which half of K
+  const int peer = rank ^ 1;
+  int mb, nb;
+  tile_coords(static_cast<int>(ptx::cluster_id_x()), p, mb, nb);
+  const int half = (p.num_k_blk + 1) / 2;
+  const int kb0 = rank ? half : 0;
+  const int kb1 = rank ? p.num_k_blk : half;
+  const bool have_acc = kb1 > kb0;
+  // Epilogue warp q reads TMEM lanes (tile rows) [32q, 32q+32); it is live
+  // when those rows exist.  CTA r keeps rows [64r, 64r+64); the peer's warps
+  // with the same q send them, so the bytes to expect are 16 KB per live kept warp.
+  auto live = [&](int q) { return mb * C::BM + q * 32 < p.M; };
+  const uint32_t recv_bytes =
+      (live(2 * rank) ? 16384u : 0u) + (live(2 * rank + 1) ? 16384u : 0u);
+
+  if (warp == C::PRODUCER_WARP && lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    ptx::mbar_init(accf_bar, 1);
+    ptx::mbar_init(recv_bar, 1);
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    if (recv_bytes) ptx::mbar_arrive_expect_tx(recv_bar, recv_bytes);
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB0);
+    if (!C::INTERLEAVED) ptx::prefetch_tmap(&tmB1);
+    ptx::prefetch_tmap(&tmY);
+  }
+  if (warp == C::MMA_WARP) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // the peer's receive barrier is armed before any store to it
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  ptx::grid_launch_dependents();
+  auto load_w = [&](uint32_t sb, uint32_t fb, int kb) {
+    if (C::INTERLEAVED) {
+      ptx::tma_load_2d(sb, &tmB0, fb, nb * C::MMA_N, kb * C::BK);
+      ptx::tma_load_2d(sb + C::ATOM_BYTES, &tmB0, fb, nb * C::MMA_N + C::ATOM_COLS, kb * C::BK);
+    } else {
+      ptx::tma_load_2d(sb, &tmB0, fb, nb * C::BN, kb * C::BK);
+      ptx::tma_load_2d(sb + C::ATOM_BYTES, &tmB1, fb, nb * C::BN, kb * C::BK);
+    }
+  };
+  // Weights known to be unwritten by earlier work: the first stages' weight
+  // boxes go out before the dependency wait, their A boxes after it.
+  uint32_t pre = 0;
+  if (warp == C::PRODUCER_WARP && p.w_early) {
+    pre = static_cast<uint32_t>(kb1 - kb0 < C::STAGES ? kb1 - kb0 : C::STAGES);
+    if (lane == 0)
+      for (uint32_t s = 0; s < pre; ++s) {
+        ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+        load_w(base + s * C::STAGE_BYTES + C::A_BYTES, full_bar(s), kb0 + (int)s);
+      }
+    __syncwarp();
+  }
+  ptx::grid_dependency_wait();
+
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const bool early = issued < pre;  // weights already on their way
+        if (!early && !wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
+                                WAIT_PRODUCER_EMPTY)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = base + stage * C::STAGE_BYTES;
+        const uint32_t sb = sa + C::A_BYTES;
+        const uint32_t fb = full_bar(stage);
+        if (!early) ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
+        if (!early) load_w(sb, fb, kb);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // let the copies in flight land before shared memory is released
+        const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
+        for (uint32_t i = issued - n; i < issued; ++i)
+          wait_quiet(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t sa = base + stage * C::STAGE_BYTES;
+        const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk) {
+          const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
+          const uint64_t bdesc =
+              ptx::smem_desc(sb + kk * C::B_KSTEP, C::ATOM_BYTES, C::B_SBO, ptx::SW_128B);
+          ptx::mma_f16(tmem_base, adesc, bdesc, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(empty_bar(stage));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) ptx::mma_commit(accf_bar);
+      ptx::mma_commit(drain_bar);
+      wait_quiet(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    const int q = warp & 3;   // TMEM lanes (tile rows) [32q, 32q+32)
+    const int h = warp >> 2;  // column half: outputs [32h, 32h+32), TMEM columns [64h, 64h+64)
+    const bool keeper = (q >> 1) == rank;
+    const int rloc = (q & 1) * 32 + lane;  // row within the kept half
+    bool ok = wait_bar(accf_bar, 0, p.timeout_ns, abort_flag, p.err, WAIT_EPI_ACC_FULL);
+    ok = __all_sync(0xffffffffu, ok);
+    ptx::tc_fence_after();
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    if (ok && live(q)) {
+      if (!keeper) {
+        // send this warp's 32 rows x 64 partial columns to the peer
+        const uint32_t recv_local = base + C::RECV_OFF + static_cast<uint32_t>(rloc) * 16u;
+        const uint32_t dst = ptx::mapa_shared(recv_local, static_cast<uint32_t>(peer));
+        const uint32_t rbar = ptx::mapa_shared(recv_bar, static_cast<uint32_t>(peer));
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * h + cc;  // TMEM columns [32c, 32c+32)
+          uint32_t v[32];
+          if (have_acc) {
+            ptx::tmem_ld32(tacc + c * 32, v);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ptx::st_async_v4(dst + static_cast<uint32_t>((c * 8 + j) * C::HALF_ROWS * 16),
+                             v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3], rbar);
+        }
+      } else {
+        // wait for the peer's half of the K steps, then finish the kept rows
+        bool got = true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait_cluster(recv_bar, 0)) {
+          if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+            got = false;
+            break;
+          }
+        }
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            if (atomicCAS(p.err, 0u, kErrTimeout) == 0u) atomicExch(p.err + 1, WAIT_SK_RECV);
+            __threadfence();
+          }
+          // stores from a late peer land within microseconds; let them in
+          // before this CTA's shared memory is released
+          spin_ns(100000);
+        } else {
+          const float4 *recv = reinterpret_cast<const float4 *>(smem + C::RECV_OFF);
+          // staging: this warp's 2 KB buffer in the (now idle) ring
+          const uint32_t stg = base + static_cast<uint32_t>(((q & 1) * 2 + h) * C::STG_BYTES);
+          sk_epilogue_keep<C>(tacc, have_acc, recv, rloc, h, mb * C::BM + q * 32, nb * C::BN,
+                              &tmY, p.M, p.N, smem, base, stg, lane);
+          if (lane == 0) ptx::bulk_wait_read<0>();
+          __syncwarp();
+        }
+      }
+    }
+  }
+
+  // No cluster barrier at the end: a CTA leaves only after its kept warps
+  // have received every byte the peer sends it (or have given up and waited
+  // for late stores), and a CTA's own stores target only the peer.
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace swiglu

@@ -157,9 +157,41 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::tma_prefetch_2d(&tmB0, 0, 0);
     if (!C::INTERLEAVED) ptx::tma_prefetch_2d(&tmB1, 0, 0);
   }
-  ptx::grid_dependency_wait();
-
   const int num_units = pc.num_m_blk * pc.num_n_blk;
+  // The weight boxes of one stage (K step kb of column block nb).
+  auto load_w = [&](uint32_t sb, uint32_t fb, int nb, int kb) {
+    if (C::INTERLEAVED) {
+#pragma unroll
+      for (int j = 0; j < C::NB_ATOMS; ++j)
+        ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::MMA_N + j * C::ATOM_COLS,
+                         kb * C::BK);
+    } else {
+#pragma unroll
+      for (int j = 0; j < C::NB_ATOMS / 2; ++j) {
+        ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::BN + j * C::ATOM_COLS,
+                         kb * C::BK);
+        ptx::tma_load_2d(sb + (C::NB_ATOMS / 2 + j) * C::ATOM_BYTES, &tmB1, fb,
+                         nb * C::BN + j * C::ATOM_COLS, kb * C::BK);
+      }
+    }
+  };
+  // Weights known to be unwritten by earlier work: the first tile's first
+  // stages of weight boxes go out before the dependency wait (the stages are
+  // fresh, so no empty-barrier wait is needed); their A boxes follow after it.
+  uint32_t pre = 0;
+  if (warp == C::PRODUCER_WARP && p.w_early && unit0 < num_units) {
+    pre = p.num_k_blk < C::STAGES ? p.num_k_blk : C::STAGES;
+    if (lane == 0) {
+      int mb, ng;
+      tile_coords(unit0, pc, mb, ng);
+      for (uint32_t s = 0; s < pre; ++s) {
+        ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+        load_w(base + s * C::STAGE_BYTES + C::A_BYTES, full_bar(s), ng * C::MC + rank, (int)s);
+      }
+    }
+    __syncwarp();
+  }
+  ptx::grid_dependency_wait();
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
@@ -172,34 +204,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tile_coords(t, pc, mb, ng);
         const int nb = ng * C::MC + rank;
         for (int kb = 0; kb < p.num_k_blk; ++kb) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
-                        WAIT_PRODUCER_EMPTY)) {
+          const bool early = issued < pre;  // weights already on their way
+          if (!early && !wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
+                                  WAIT_PRODUCER_EMPTY)) {
             ok = false;
             break;
           }
           const uint32_t sa = base + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const uint32_t fb = full_bar(stage);
-          ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          if (!early) ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           if (C::MC > 1)
             ptx::tma_load_2d_mc(sa + rank * C::A_PIECE_ROWS * 128, &tmA, fb, kb * C::BK,
                                 mb * C::BM + rank * C::A_PIECE_ROWS, kMask);
           else
             ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
-          if (C::INTERLEAVED) {
-#pragma unroll
-            for (int j = 0; j < C::NB_ATOMS; ++j)
-              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb,
-                               nb * C::MMA_N + j * C::ATOM_COLS, kb * C::BK);
-          } else {
-#pragma unroll
-            for (int j = 0; j < C::NB_ATOMS / 2; ++j) {
-              ptx::tma_load_2d(sb + j * C::ATOM_BYTES, &tmB0, fb, nb * C::BN + j * C::ATOM_COLS,
-                               kb * C::BK);
-              ptx::tma_load_2d(sb + (C::NB_ATOMS / 2 + j) * C::ATOM_BYTES, &tmB1, fb,
-                               nb * C::BN + j * C::ATOM_COLS, kb * C::BK);
-            }
-          }
+          if (!early) load_w(sb, fb, nb, kb);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;

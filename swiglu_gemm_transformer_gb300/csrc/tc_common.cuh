@@ -27,7 +27,10 @@ struct KParams {
   int32_t M, N, K;
   int32_t num_m_blk, num_n_blk, num_k_blk;
   int32_t group_m;       // grouped raster: this many m-blocks walk the n-blocks together
-  int32_t pad_;
+  // 1: the weights are not written by any earlier work on the stream, so the
+  // producer may load the first stages' weight boxes before the dependency
+  // wait of programmatic dependent launch (A is always loaded after it).
+  int32_t w_early;
   uint64_t timeout_ns;   // limit of every mbarrier wait
   uint32_t *err;         // device error word: [0] = status, [1] = where
   // FP8 operands only: device pointers to the per-tensor scales of A, W1, W2

@@ -100,3 +100,13 @@ def sample_rows(M: int, tile_m: int, n_random: int, seed: int):
     if n_random > 0 and M > 0:
         rows.update(int(r) for r in rng.integers(0, M, size=n_random))
     return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
+
+
+def make_producer_inputs(M: int, K: int, seed: int):
+    """Inputs of the RMSNorm + E4M3 producer: X [M,K] ~ N(0,1) (the
+    distribution of A before quantisation) and gamma [K] = 1 + 0.1 N(0,1), both
+    BF16 on the CPU.  gamma is drawn first, then X."""
+    g = torch.Generator().manual_seed(seed)
+    gamma = (1.0 + 0.1 * torch.randn(K, generator=g)).to(torch.bfloat16)
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16).contiguous()
+    return X, gamma

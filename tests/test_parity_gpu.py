@@ -57,7 +57,7 @@ def _check(Y, A, W1, W2, rows=None, what=""):
 
 FORMS = ["separate", "interleaved"]
 VARIANTS = ["1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n32_mc2", "1sm_n32_mc4",
-            "1sm_n64_mc2", "1sm_n128_mc2"]
+            "1sm_n64_mc2", "1sm_n128_mc2", "1sm_n64_sk2"]
 
 SMALL_SHAPES = [
     # (M, N, K): tails in every dimension, several tiles
@@ -180,3 +180,21 @@ def test_bounded_wait_reports_timeout_and_context_survives(sg):
     A, W1, W2 = si.make_bf16(70, 72, 64, seed=1)
     Y = _run(sg, "separate", A, W1, W2, sg.VARIANT_AUTO)
     _check(Y, A, W1, W2, what="after timeout")
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("variant", ["1sm_n32", "1sm_n64", "1sm_n128", "1sm_n32_mc2", "1sm_n64_sk2"])
+def test_weights_read_only_mode(sg, form, variant):
+    """With the read-only-weights promise the kernels load the first weight
+    stages before the dependency wait; results must not change.  Calls run
+    back to back on one stream with different weights, so an early load that
+    raced a previous call would show up as a wrong tile."""
+    sg.swiglu_set_weights_read_only(True)
+    try:
+        for shape, seed in [((128, 4864, 896), 1), ((63, 264, 136), 2), ((200, 520, 72), 3)]:
+            M, N, K = shape
+            A, W1, W2 = si.make_bf16(M, N, K, seed=seed)
+            Y = _run(sg, form, A, W1, W2, sg.VARIANTS[variant])
+            _check(Y, A, W1, W2, what=f"read-only weights {form} {variant} {shape}")
+    finally:
+        sg.swiglu_set_weights_read_only(False)
