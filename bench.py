@@ -655,7 +655,7 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
                      "tflops": round(wl.flops / (ms * 1e-3) / 1e12, 2),
                      "per_call_us": [round(u, 3) for u in eager_us]},
            "fusion": fusion_report(wl, fused_us, eager_us, hbm_gbs)}
-    if args.compile_context:
+    if not args.no_compile_context:
         out["compile"] = run_compile_context(args, wl, stream, fused_us)
     return out
 
@@ -782,8 +782,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--compile-context", action="store_true",
-                    help="also time the unfused function under torch.compile (context)")
+    ap.add_argument("--no-compile-context", action="store_true",
+                    help="skip timing the unfused function under torch.compile (context)")
     ap.add_argument("--only", default="",
                     help="restrict the step to calls FORM:M[,FORM:M...] (profiling a single kernel)")
     args = ap.parse_args()

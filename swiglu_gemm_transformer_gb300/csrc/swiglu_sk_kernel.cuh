@@ -18,13 +18,16 @@
 //     warp 5 issues tcgen05.mma M=128 x N=128 (gate and up side by side in
 //     TMEM, as in the one-CTA kernel) over that half;
 //   * the two partial accumulators are summed through distributed shared
-//     memory: CTA r keeps output rows [64r, 64r+64); eight epilogue warps
-//     (four TMEM lane groups x two column halves) split the work: those on
-//     the other 64 lanes send their rows' partial columns to the peer with
-//     st.async (16 bytes per store, counted on the peer's receive mbarrier);
-//     those on the kept lanes wait for the peer's half, add it to their own
-//     accumulator, apply y = g * u / (1 + e^-g) in FP32, round to BF16 and
-//     store 32 x 32 blocks through 64-byte-swizzled staging buffers with TMA.
+//     memory: CTA r keeps output columns [32r, 32r+32) of the tile for all
+//     rows.  Eight epilogue warps (four TMEM lane groups x two 16-column
+//     halves, so all four SM sub-partitions share the work) each send the
+//     peer their partial gate/up sums of 16 of the peer's columns with
+//     st.async (16 bytes per store, counted on the peer's receive mbarrier),
+//     then wait for the peer's sums of their own 16 columns, add them, apply
+//     y = g * u / (1 + e^-g) in FP32 with one special-function operation per
+//     element, round to BF16 and store their 32 bytes of each row directly.
+//     With few rows this epilogue is not hidden behind MMAs, so its length
+//     is what the special-function unit and the exchange take.
 // Gate and up values never reach global memory.  One tile per cluster (no
 // persistent loop): the launcher sizes the grid to two CTAs per output tile.
 //
@@ -62,12 +65,14 @@ struct SkCfg {
   static constexpr int B_BYTES = NB_ATOMS * ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
   static constexpr int STAGES = 6;
-  static constexpr int HALF_ROWS = BM / 2;
-  // Receive buffer: the peer's partial accumulator for the 64 kept rows,
-  // 128 FP32 columns each, stored as [column / 4][row][4] so that a warp's 32
-  // rows read or write 512 contiguous bytes per 16-byte access.
+  // Receive buffer: the peer's partial gate and up sums of the 32 output
+  // columns this CTA keeps, for all 128 rows: value v (v < 32: gate of kept
+  // output v; v >= 32: up of kept output v - 32) of row i at
+  // [v / 4][i][v % 4], so a warp's 32 rows read or write 512 contiguous bytes
+  // per 16-byte access.
+  static constexpr int KEEP = BN / 2;            // output columns kept per CTA
   static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
-  static constexpr int RECV_BYTES = HALF_ROWS * MMA_N * 4;  // 32 KB
+  static constexpr int RECV_BYTES = BM * 2 * KEEP * 4;  // 32 KB
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], acc_full, recv, drain
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
@@ -76,81 +81,42 @@ struct SkCfg {
   static constexpr int MMA_WARP = 9;
   static constexpr int THREADS = 32 * 10;
   static constexpr int TMEM_COLS = 128;
-  static constexpr int STG_BYTES = 32 * 64;      // a warp's 32 rows x 32 BF16 columns
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(4 * STG_BYTES <= RECV_OFF, "staging reuses the ring");
 };
 
-// Epilogue of the kept half for one warp: 32 rows (TMEM lanes of `tacc`) x
-// the 32 output columns of chunk `c`; adds the peer's partial sums from `recv`
-// (this thread's row is receive row `rloc`), then stores Y through the 2 KB
-// staging buffer at `stg` (shared::cta address) with TMA.
+// This warp's 32 rows x 16 outputs starting at tile output `o0`: gate and up
+// partial sums from TMEM (zeros when the CTA had no K steps).
 template <class C>
-__device__ __forceinline__ static void sk_epilogue_keep(uint32_t tacc, bool have_acc,
-                                                        const float4 *recv, int rloc, int c,
-                                                        int row0, int col0,
-                                                        const CUtensorMap *tmY, int M, int N,
-                                                        uint8_t *smem, uint32_t smem_base,
-                                                        uint32_t stg, int lane) {
-  // TMEM columns of this chunk's gate and up values
-  const int cg = C::INTERLEAVED ? c * 64 : c * 32;
-  const int cu = C::INTERLEAVED ? c * 64 + 32 : C::BN + c * 32;
-  uint32_t g[32], u[32];
-  if (have_acc) {
-    ptx::tmem_ld32(tacc + cg, g);
-    ptx::tmem_ld32(tacc + cu, u);
+__device__ __forceinline__ static void sk_load16(uint32_t tacc, bool have_acc, int o0,
+                                                 float (&g)[16], float (&u)[16]) {
+  if (!have_acc) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = u[i] = 0.0f;
+    return;
+  }
+  if (C::INTERLEAVED) {  // columns 2o (gate), 2o+1 (up)
+    uint32_t v[32];
+    ptx::tmem_ld32(tacc + 2 * o0, v);
     ptx::tmem_wait_ld();
-    ptx::reg_fence(g);
-    ptx::reg_fence(u);
-  } else {
+    ptx::reg_fence(v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float4 pg = recv[(cg / 4 + j) * C::HALF_ROWS + rloc];
-    const float4 pu = recv[(cu / 4 + j) * C::HALF_ROWS + rloc];
-    g[4 * j + 0] = __float_as_uint(__uint_as_float(g[4 * j + 0]) + pg.x);
-    g[4 * j + 1] = __float_as_uint(__uint_as_float(g[4 * j + 1]) + pg.y);
-    g[4 * j + 2] = __float_as_uint(__uint_as_float(g[4 * j + 2]) + pg.z);
-    g[4 * j + 3] = __float_as_uint(__uint_as_float(g[4 * j + 3]) + pg.w);
-    u[4 * j + 0] = __float_as_uint(__uint_as_float(u[4 * j + 0]) + pu.x);
-    u[4 * j + 1] = __float_as_uint(__uint_as_float(u[4 * j + 1]) + pu.y);
-    u[4 * j + 2] = __float_as_uint(__uint_as_float(u[4 * j + 2]) + pu.z);
-    u[4 * j + 3] = __float_as_uint(__uint_as_float(u[4 * j + 3]) + pu.w);
-  }
-  uint32_t packed[16];
-  if (C::INTERLEAVED) {
-    // g: (gate, up) pairs of outputs 32c..32c+15; u: outputs 32c+16..32c+31
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      packed[i] =
-          pack_bf16x2(silu_mul(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1])),
-                      silu_mul(__uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3])));
-      packed[8 + i] =
-          pack_bf16x2(silu_mul(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1])),
-                      silu_mul(__uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
+    for (int i = 0; i < 16; ++i) {
+      g[i] = __uint_as_float(v[2 * i]);
+      u[i] = __uint_as_float(v[2 * i + 1]);
     }
-  } else {
+  } else {  // columns o (gate), BN + o (up)
+    uint32_t a[16], b[16];
+    ptx::tmem_ld16(tacc + o0, a);
+    ptx::tmem_ld16(tacc + C::BN + o0, b);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(a);
+    ptx::reg_fence(b);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      packed[i] =
-          pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                      silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-  }
-  const int ccol = col0 + c * 32;
-  uint4 *rowp = reinterpret_cast<uint4 *>(smem + (stg - smem_base) + lane * 64);
-  const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk i -> i ^ ((row >> 1) & 3)
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    rowp[i ^ sw] =
-        make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-  ptx::fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    if (row0 < M && ccol < N) ptx::tma_store_2d(tmY, stg, ccol, row0);
-    ptx::bulk_commit();
+    for (int i = 0; i < 16; ++i) {
+      g[i] = __uint_as_float(a[i]);
+      u[i] = __uint_as_float(b[i]);
+    }
   }
 }
 
@@ -184,12 +150,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int kb0 = rank ? half : 0;
   const int kb1 = rank ? p.num_k_blk : half;
   const bool have_acc = kb1 > kb0;
-  // Epilogue warp q reads TMEM lanes (tile rows) [32q, 32q+32); it is live
-  // when those rows exist.  CTA r keeps rows [64r, 64r+64); the peer's warps
-  // with the same q send them, so the bytes to expect are 16 KB per live kept warp.
+  // Epilogue warps on TMEM lanes (tile rows) [32q, 32q+32) are live when
+  // those rows exist; the peer's live warps send what this CTA keeps.
   auto live = [&](int q) { return mb * C::BM + q * 32 < p.M; };
-  const uint32_t recv_bytes =
-      (live(2 * rank) ? 16384u : 0u) + (live(2 * rank + 1) ? 16384u : 0u);
+  // the peer's two warps of each live lane group send 4 KB each
+  const uint32_t recv_bytes = (live(0) ? 8192u : 0u) + (live(1) ? 8192u : 0u) +
+                              (live(2) ? 8192u : 0u) + (live(3) ? 8192u : 0u);
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -304,65 +270,79 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-7)
-    const int q = warp & 3;   // TMEM lanes (tile rows) [32q, 32q+32)
-    const int h = warp >> 2;  // column half: outputs [32h, 32h+32), TMEM columns [64h, 64h+64)
-    const bool keeper = (q >> 1) == rank;
-    const int rloc = (q & 1) * 32 + lane;  // row within the kept half
+    // CTA r keeps tile outputs [32r, 32r+32) for all rows; warp (q, h) owns
+    // rows [32q, 32q+32) (its TMEM lanes) and, of both the kept and the sent
+    // outputs, the 16 starting at 16h: it sends the peer its partial sums of
+    // the peer's 16, then finishes its own 16 with the peer's partial sums.
+    const int q = warp & 3;
+    const int h = warp >> 2;
+    const int row = q * 32 + lane;  // tile row of this thread
     bool ok = wait_bar(accf_bar, 0, p.timeout_ns, abort_flag, p.err, WAIT_EPI_ACC_FULL);
     ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     if (ok && live(q)) {
-      if (!keeper) {
-        // send this warp's 32 rows x 64 partial columns to the peer
-        const uint32_t recv_local = base + C::RECV_OFF + static_cast<uint32_t>(rloc) * 16u;
+      {  // send: the peer keeps outputs [32 peer, 32 peer + 32)
+        float g[16], u[16];
+        sk_load16<C>(tacc, have_acc, C::KEEP * peer + 16 * h, g, u);
+        const uint32_t recv_local = base + C::RECV_OFF + static_cast<uint32_t>(row) * 16u;
         const uint32_t dst = ptx::mapa_shared(recv_local, static_cast<uint32_t>(peer));
         const uint32_t rbar = ptx::mapa_shared(recv_bar, static_cast<uint32_t>(peer));
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * h + cc;  // TMEM columns [32c, 32c+32)
-          uint32_t v[32];
-          if (have_acc) {
-            ptx::tmem_ld32(tacc + c * 32, v);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence(v);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ptx::st_async_v4(dst + static_cast<uint32_t>((c * 8 + j) * C::HALF_ROWS * 16),
-                             v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3], rbar);
+        for (int k = 0; k < 4; ++k) {
+          // gate values 16h + 4k .. +3 -> group 4h + k; up values -> group 8 + 4h + k
+          ptx::st_async_v4(dst + static_cast<uint32_t>((4 * h + k) * C::BM * 16),
+                           __float_as_uint(g[4 * k]), __float_as_uint(g[4 * k + 1]),
+                           __float_as_uint(g[4 * k + 2]), __float_as_uint(g[4 * k + 3]), rbar);
+          ptx::st_async_v4(dst + static_cast<uint32_t>((8 + 4 * h + k) * C::BM * 16),
+                           __float_as_uint(u[4 * k]), __float_as_uint(u[4 * k + 1]),
+                           __float_as_uint(u[4 * k + 2]), __float_as_uint(u[4 * k + 3]), rbar);
         }
+      }
+      float g[16], u[16];
+      sk_load16<C>(tacc, have_acc, C::KEEP * rank + 16 * h, g, u);
+      // wait for the peer's partial sums of the kept outputs
+      bool got = true;
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait_cluster(recv_bar, 0)) {
+        if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+          got = false;
+          break;
+        }
+      }
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          if (atomicCAS(p.err, 0u, kErrTimeout) == 0u) atomicExch(p.err + 1, WAIT_SK_RECV);
+          __threadfence();
+        }
+        // stores from a late peer land within microseconds; let them in
+        // before this CTA's shared memory is released
+        spin_ns(100000);
       } else {
-        // wait for the peer's half of the K steps, then finish the kept rows
-        bool got = true;
-        const uint64_t t0 = ptx::globaltimer_ns();
-        while (!ptx::mbar_try_wait_cluster(recv_bar, 0)) {
-          if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-            got = false;
-            break;
-          }
+        const float4 *recv = reinterpret_cast<const float4 *>(smem + C::RECV_OFF);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 pg = recv[(4 * h + k) * C::BM + row];
+          const float4 pu = recv[(8 + 4 * h + k) * C::BM + row];
+          g[4 * k] += pg.x; g[4 * k + 1] += pg.y; g[4 * k + 2] += pg.z; g[4 * k + 3] += pg.w;
+          u[4 * k] += pu.x; u[4 * k + 1] += pu.y; u[4 * k + 2] += pu.z; u[4 * k + 3] += pu.w;
         }
-        got = __all_sync(0xffffffffu, got);
-        if (!got) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            if (atomicCAS(p.err, 0u, kErrTimeout) == 0u) atomicExch(p.err + 1, WAIT_SK_RECV);
-            __threadfence();
-          }
-          // stores from a late peer land within microseconds; let them in
-          // before this CTA's shared memory is released
-          spin_ns(100000);
-        } else {
-          const float4 *recv = reinterpret_cast<const float4 *>(smem + C::RECV_OFF);
-          // staging: this warp's 2 KB buffer in the (now idle) ring
-          const uint32_t stg = base + static_cast<uint32_t>(((q & 1) * 2 + h) * C::STG_BYTES);
-          sk_epilogue_keep<C>(tacc, have_acc, recv, rloc, h, mb * C::BM + q * 32, nb * C::BN,
-                              &tmY, p.M, p.N, smem, base, stg, lane);
-          if (lane == 0) ptx::bulk_wait_read<0>();
-          __syncwarp();
+        uint32_t packed[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          packed[i] = pack_bf16x2(silu_mul_1sfu(g[2 * i], u[2 * i]),
+                                  silu_mul_1sfu(g[2 * i + 1], u[2 * i + 1]));
+        // 32 bytes of this row of Y; N is a multiple of 8, so each 16-byte
+        // half is wholly inside or wholly outside the matrix
+        const int yrow = mb * C::BM + row;
+        const int ycol = nb * C::BN + C::KEEP * rank + 16 * h;
+        if (yrow < p.M) {
+          uint4 *yp = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) +
+                                                static_cast<int64_t>(yrow) * p.N + ycol);
+          if (ycol < p.N) yp[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          if (ycol + 8 < p.N) yp[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
       }
     }

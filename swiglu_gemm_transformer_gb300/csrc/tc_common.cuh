@@ -42,6 +42,8 @@ struct KParams {
   const void *R;
   float *ws;
   int32_t k_splits, kb_per_split;
+  // Y itself (the split-K small-M kernel stores its few rows directly).
+  void *Y;
 };
 
 // Bounded wait, slow path.  Returns false on timeout or when another role of
@@ -99,6 +101,25 @@ __device__ __forceinline__ static void tile_coords(int t, const KParams &p, int 
 // SiLU(g) * u = g * u / (1 + e^-g), FP32.
 __device__ __forceinline__ static float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// The same with one special-function-unit operation instead of two, for
+// epilogues that are not hidden behind MMAs (few rows): e^-g = 2^(-g log2 e)
+// by ex2.approx, then the reciprocal of d = 1 + e^-g (d >= 1, capped at 1e30
+// so that it stays finite) on the FMA pipe: the classic bit-level first guess
+// (subtracting the float's bits from a constant, which roughly negates the
+// exponent; relative error below 6 %) refined by three Newton-Raphson steps
+// r <- r (2 - d r), each of which squares the relative error (< 1e-7 after
+// three).
+__device__ __forceinline__ static float silu_mul_1sfu(float g, float u) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
+  const float d = 1.0f + fminf(e, 1e30f);
+  float r = __uint_as_float(0x7EF311C3u - __float_as_uint(d));
+  r = r * fmaf(-d, r, 2.0f);
+  r = r * fmaf(-d, r, 2.0f);
+  r = r * fmaf(-d, r, 2.0f);
+  return g * r * u;
 }
 
 __device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
