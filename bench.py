@@ -45,11 +45,15 @@ WORKLOADS = {
     "qwen2.5-7b": (3584, 18944, (256, 1024, 2048, 4096), 2),
     "qwen2.5-72b": (8192, 29568, (2048, 8192, 16384), 3),
     "qwen2.5-7b-fp8": (3584, 18944, (512, 4096), 4),
+    # the FP8 projection fed by its producer (RMSNorm of the hidden state X and
+    # per-tensor E4M3 quantisation of A), timed together
+    "qwen2.5-7b-fp8-rmsnorm": (3584, 18944, (512, 4096), 4),
     # the SwiGLU MLP block: (H, F, Ms, seed)
     "qwen2.5-0.5b-mlp": (896, 4864, (128, 512, 2048, 8192), 1),
     "qwen2.5-7b-mlp": (3584, 18944, (256, 1024, 4096), 2),
 }
 DEFAULT_WORKLOAD = "qwen2.5-0.5b"
+RMS_EPS = 1e-6   # RMSNorm epsilon of the producer workload (Qwen-2.5's value)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CSRC = os.path.join(ROOT, "swiglu_gemm_transformer_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -205,13 +209,19 @@ class Workload:
         K, N, Ms, seed = WORKLOADS[name]
         self.K, self.N, self.Ms, self.seed = K, N, Ms, seed
         self.dev = dev
-        self.kind = "fp8" if name.endswith("-fp8") else "mlp" if name.endswith("-mlp") else "bf16"
+        self.producer = name.endswith("-fp8-rmsnorm")
+        self.kind = ("fp8" if name.endswith("-fp8") or self.producer else
+                     "mlp" if name.endswith("-mlp") else "bf16")
         self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
         forms = ("mlp",) if self.kind == "mlp" else ("separate", "interleaved")
         self.host = {}
         for M in Ms:
-            if self.fp8:
+            if self.producer:   # X and gamma in BF16; the FP8 weights of the same recipe
+                q, sc = si.make_e4m3(1, N, K, seed)
+                X, gamma = si.make_producer_inputs(M, K, seed)
+                self.host[M] = (X, q[1].t().contiguous(), q[2].t().contiguous(), sc, gamma)
+            elif self.fp8:
                 q, sc = si.make_e4m3(M, N, K, seed)
                 self.host[M] = (q[0], q[1].t().contiguous(), q[2].t().contiguous(), sc)
             elif self.kind == "mlp":   # K = H (hidden), N = F (intermediate)
@@ -241,10 +251,18 @@ class Workload:
         return (6 if self.kind == "mlp" else 4) * M * self.N * self.K
 
     def algorithmic_bytes(self, M):
-        """Inputs read once and the output written once (the MLP's Y is internal)."""
+        """Inputs read once and the output written once (the MLP's Y is internal;
+        with the producer, A's codes are written once and read once more)."""
         if self.kind == "mlp":
             return 2 * (M * self.K + 3 * self.K * self.N + M * self.K)
-        return self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
+        b = self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
+        if self.producer:
+            b += self.producer_bytes(M)
+        return b
+
+    def producer_bytes(self, M):
+        """RMSNorm + quantisation: X read (BF16), gamma read, codes written."""
+        return 2 * M * self.K + 2 * self.K + M * self.K
 
     def out_shape(self, M):
         return (M, self.K) if self.kind == "mlp" else (M, self.N)
@@ -261,9 +279,13 @@ class Workload:
             return (h[0].to(dev), h[1].to(dev), h[2].to(dev), h[3].to(dev), out, ws)
         if self.fp8:
             s = torch.tensor(list(h[3]), dtype=torch.float32, device=dev)
+            extra = ()
+            if self.producer:   # (X, gamma, Aq): the producer writes Aq and s[0]
+                extra = (h[4].to(dev), torch.empty(M, self.K, dtype=torch.float8_e4m3fn, device=dev))
             if form == "separate":
-                return (h[0].to(dev), h[1].to(dev), h[2].to(dev), out, s)
-            return (h[0].to(dev), sg.swiglu_pack_interleaved_fp8(h[1].to(dev), h[2].to(dev)), out, s)
+                return (h[0].to(dev), h[1].to(dev), h[2].to(dev), out, s) + extra
+            return (h[0].to(dev), sg.swiglu_pack_interleaved_fp8(h[1].to(dev), h[2].to(dev)), out,
+                    s) + extra
         if form == "separate":
             return (h[0].to(dev), h[1].to(dev), h[2].to(dev), out)
         return (h[0].to(dev), sg.swiglu_pack_interleaved(h[1].to(dev), h[2].to(dev)), out)
@@ -272,7 +294,7 @@ class Workload:
         import torch
         return torch.cuda.current_stream().cuda_stream
 
-    def launcher(self, form, M, v, bufs):
+    def launcher(self, form, M, v, bufs, with_producer=True):
         """A closure launching this call through the C ABI on the current stream."""
         lib, N, K, sg = self.lib, self.N, self.K, self.sg
         d = [b.data_ptr() for b in bufs]
@@ -285,17 +307,45 @@ class Workload:
             return lambda: check("swiglu_mlp", lib.swiglu_mlp(d[0], d[1], d[2], d[3], None, d[4],
                                                                M, K, N, d[5], nbytes, self._stream()))
         if self.fp8:
-            sp = (d[-1], d[-1] + 4, d[-1] + 8)
+            ns = 4 if form == "separate" else 3        # index of the scales
+            sp = (d[ns], d[ns] + 4, d[ns] + 8)
+            a = d[0]
+            prod = None
+            if self.producer:
+                a = d[ns + 2]                          # the codes the producer writes
+                if with_producer:
+                    prod = self.producer_launcher(form, M, v, bufs)
             if form == "separate":
-                return lambda: check("swiglu_fused_fp8", lib.swiglu_fused_fp8(
-                    d[0], d[1], d[2], sp[0], sp[1], sp[2], d[3], M, N, K, self._stream()))
-            return lambda: check("swiglu_fused_interleaved_fp8", lib.swiglu_fused_interleaved_fp8(
-                d[0], d[1], sp[0], sp[1], sp[2], d[2], M, N, K, self._stream()))
+                f = lambda: check("swiglu_fused_fp8", lib.swiglu_fused_fp8(
+                    a, d[1], d[2], sp[0], sp[1], sp[2], d[3], M, N, K, self._stream()))
+            else:
+                f = lambda: check("swiglu_fused_interleaved_fp8", lib.swiglu_fused_interleaved_fp8(
+                    a, d[1], sp[0], sp[1], sp[2], d[2], M, N, K, self._stream()))
+            if prod is None:
+                return f
+            return lambda: (prod(), f())
         if form == "separate":
             return lambda: check("swiglu_fused_ex", lib.swiglu_fused_ex(
                 d[0], d[1], d[2], d[3], M, N, K, v, self._stream()))
         return lambda: check("swiglu_fused_interleaved_ex", lib.swiglu_fused_interleaved_ex(
             d[0], d[1], d[2], M, N, K, v, self._stream()))
+
+    def gemm_launcher(self, form, M, v, bufs):
+        """The FP8 projection alone, on the codes the producer left in the buffers."""
+        return self.launcher(form, M, v, bufs, with_producer=False)
+
+    def producer_launcher(self, form, M, v, bufs):
+        """The producer alone: RMSNorm of X and E4M3 quantisation into Aq, s[0]."""
+        lib, K, sg = self.lib, self.K, self.sg
+        ns = 4 if form == "separate" else 3
+        X, s, gamma, Aq = bufs[0], bufs[ns], bufs[ns + 1], bufs[ns + 2]
+        px, pg, pq, ps = X.data_ptr(), gamma.data_ptr(), Aq.data_ptr(), s.data_ptr()
+
+        def run():
+            rc = lib.swiglu_rmsnorm_quant_fp8(px, pg, RMS_EPS, pq, ps, M, K, self._stream())
+            if rc:
+                raise sg.SwigluError("swiglu_rmsnorm_quant_fp8", rc)
+        return run
 
     def api_call(self, form, M, v, bufs):
         """The same call through the public Python API; returns the output tensor."""
@@ -303,11 +353,15 @@ class Workload:
         if self.kind == "mlp":
             return sg.swiglu_mlp(bufs[0], bufs[1], bufs[2], bufs[3], None, bufs[4], workspace=bufs[5])
         if self.fp8:
-            sc = bufs[-1]
+            ns = 4 if form == "separate" else 3
+            sc = bufs[ns]
             s3 = (sc[0:1], sc[1:2], sc[2:3])
+            a = bufs[0]
+            if self.producer:
+                a, _ = sg.swiglu_rmsnorm_quant_fp8(bufs[0], bufs[ns + 1], RMS_EPS, bufs[ns + 2], s3[0])
             if form == "separate":
-                return sg.swiglu_fused_fp8(bufs[0], bufs[1], bufs[2], *s3, bufs[3])
-            return sg.swiglu_fused_interleaved_fp8(bufs[0], bufs[1], *s3, bufs[2])
+                return sg.swiglu_fused_fp8(a, bufs[1], bufs[2], *s3, bufs[3])
+            return sg.swiglu_fused_interleaved_fp8(a, bufs[1], *s3, bufs[2])
         if form == "separate":
             return sg.swiglu_fused(bufs[0], bufs[1], bufs[2], bufs[3], variant=v)
         return sg.swiglu_fused_interleaved(bufs[0], bufs[1], bufs[2], variant=v)
@@ -315,6 +369,8 @@ class Workload:
     def launches_per_call(self, M):
         """Kernels one call enqueues (the MLP: fused projection, down projection,
         and the split-K reduction when the down projection splits K)."""
+        if self.producer:
+            return 3   # amax pass, quantise pass, FP8 projection
         if self.kind != "mlp":
             return 1
         return 2 + (1 if self.lib.swiglu_linear_workspace_size(M, self.K, self.N) > 0 else 0)
@@ -322,6 +378,8 @@ class Workload:
     def variant_label(self, v):
         if self.kind == "mlp":
             return "mlp"
+        if self.producer:
+            return "rmsnorm_quant+2sm_fp8"
         return "2sm_fp8" if self.fp8 else self.sg.variant_name(v)
 
     def step(self):
@@ -439,25 +497,42 @@ def run_ours(args, ws, rank, local):
     if wl.fp8:
         peak_tf *= 2.0  # dense FP8 = 2x dense BF16 (nominal 4.5 vs 2.25 PFLOP/s)
     kernels = []
+    chain = None
+    if wl.producer:
+        # the two kernels of each call timed alone: the FP8 projection (on the
+        # codes the producer wrote during warm-up) and the producer
+        gemm_us = measure_calls(wl, stream, args.call_launches, wl.gemm_launcher)
+        prod_us = measure_calls(wl, stream, args.call_launches, wl.producer_launcher)
+        chain = [{"form": f, "M": M, "us": round(per_call_us[c], 3),
+                  "tflops": round(wl.flops_of(M) / (per_call_us[c] * 1e-6) / 1e12, 1)}
+                 for c, (f, M, v) in enumerate(wl.calls)]
     for c, (form, M, v) in enumerate(wl.calls):
-        us = per_call_us[c]
+        us = gemm_us[c] if wl.producer else per_call_us[c]
         flops = wl.flops_of(M)
-        abytes = wl.algorithmic_bytes(M)
+        abytes = wl.algorithmic_bytes(M) - (wl.producer_bytes(M) if wl.producer else 0)
         r = roofline_entry(flops, abytes, us, peak_tf, peaks["hbm_gbs"])
         bound, achieved_tf, achieved_gbs = r["bound"], r["tflops"], r["gbs"]
         kernels.append({
-            "form": form, "M": M, "variant": wl.variant_label(v),
+            "form": form, "M": M, "variant": "2sm_fp8" if wl.producer else wl.variant_label(v),
             "us": round(us, 3),
             "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
             "frac_of_roofline": round(r["frac_of_roofline"], 4),
             "share": 0.0,
         })
+        if wl.producer:
+            pb = wl.producer_bytes(M)
+            gbs = pb / (prod_us[c] * 1e-6) / 1e9
+            kernels.append({
+                "form": form, "M": M, "variant": "rmsnorm_quant", "us": round(prod_us[c], 3),
+                "tflops": 0.0, "gbs": round(gbs, 1), "bound": "hbm",
+                "frac_of_roofline": round(gbs / peaks["hbm_gbs"], 4), "share": 0.0,
+            })
     tot_us = sum(k["us"] for k in kernels)
     for k in kernels:
         k["share"] = round(k["us"] / tot_us, 4)
-    dom = max(range(n_calls), key=lambda i: kernels[i]["us"])
+    dom = max(range(len(kernels)), key=lambda i: kernels[i]["us"])
     dk = kernels[dom]
-    form, M, v = wl.calls[dom]
+    form, M = dk["form"], dk["M"]
     kernel_key = f"{wl.name}:{form}:M{M}:{dk['variant']}"
     if dk["bound"] == "tensor":
         roof = {"bound": "tensor", "achieved": dk["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
@@ -468,6 +543,7 @@ def run_ours(args, ws, rank, local):
     roof["traffic"] = load_traffic(kernel_key)
     roof["kernel"] = kernel_key
     roof["algorithmic_per_launch"] = (wl.flops_of(M) if dk["bound"] == "tensor"
+                                      else wl.producer_bytes(M) if dk["variant"] == "rmsnorm_quant"
                                       else wl.algorithmic_bytes(M))
     roof["peak_source"] = (f"{peak_src} ({'sustained' if sustained and dk['bound'] == 'tensor' else 'burst'})"
                            + (", x2 for FP8" if wl.fp8 and dk["bound"] == "tensor" else ""))
@@ -482,6 +558,10 @@ def run_ours(args, ws, rank, local):
             "workload": (f"{wl.name} SwiGLU MLP block H={wl.K} F={wl.N} M={list(wl.Ms)} "
                          f"(fused gate/up projection + down projection), seed {wl.seed}"
                          if wl.kind == "mlp" else
+                         f"{wl.name} FP8 projection K={wl.K} N={wl.N} M={list(wl.Ms)} fed by its "
+                         f"producer (RMSNorm of X, eps {RMS_EPS}, per-tensor E4M3 quantisation), "
+                         f"separate and interleaved weights, seed {wl.seed}"
+                         if wl.producer else
                          f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
                          f"separate and interleaved weights, seed {wl.seed}"),
             "calls_per_step": n_calls,
@@ -497,6 +577,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "kernels": kernels,
         "timing_check": {"sum_of_call_ms": round(sum(per_call_us) / 1e3, 5)},
+        "calls": chain,
     }
     return out, wl, stream
 
@@ -517,7 +598,7 @@ def run_e2e(args, wl, stream, ws):
         Y_host = torch.empty(wl.out_shape(M), dtype=torch.bfloat16).pin_memory()
         host_a.append(A_host)
         host_y.append(Y_host)
-        h2d += A_host.numel() * wl.eb
+        h2d += A_host.numel() * A_host.element_size()
         d2h += Y_host.numel() * 2
     n = len(wl.calls)
     s_in, s_cmp, s_out = torch.cuda.Stream(device=dev), stream, torch.cuda.Stream(device=dev)
@@ -693,7 +774,12 @@ def oracle_sample(workload: str, target_s: float):
     rng = np.random.default_rng(seed)
     mlp = workload.endswith("-mlp")
     fp8 = workload.endswith("-fp8")
-    if fp8:
+    prod = workload.endswith("-fp8-rmsnorm")
+    if prod:   # the producer's inputs per M, the FP8 weights of the same recipe
+        (_, W1q, W2q), sc = si.make_e4m3(1, N, K, seed)
+        w18, w28 = si.bits_u8(W1q), si.bits_u8(W2q)
+        xg = {M: tuple(si.bits_u16(t) for t in si.make_producer_inputs(M, K, seed)) for M in Ms}
+    elif fp8:
         (Aq, W1q, W2q), sc = si.make_e4m3(max(Ms), N, K, seed)
         a8, w18, w28 = si.bits_u8(Aq), si.bits_u8(W1q), si.bits_u8(W2q)
     else:
@@ -710,7 +796,10 @@ def oracle_sample(workload: str, target_s: float):
         for form in forms:
             for M in Ms:
                 rows = np.sort(rng.integers(0, M, size=rows_per_call))
-                if mlp:
+                if prod:   # RMSNorm and quantisation of all of A (the scale needs every row)
+                    sA, aq = oracle.rmsnorm_quant_e4m3(xg[M][0], xg[M][1], RMS_EPS)
+                    oracle.swiglu_e4m3(aq, w18, w28, sA, sc[1], sc[2], rows=rows)
+                elif mlp:
                     oracle.mlp_bf16(a[:M], w1, w2, w3, rows=rows)
                 elif fp8:
                     oracle.swiglu_e4m3(a8[:M], w18, w28, *sc, rows=rows)

@@ -166,8 +166,10 @@ int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t
  *   Aq    : device, E4M3 [M,K] row-major (written), the Aq of swiglu_fused_fp8
  *   sA    : device, one float (written), the sA of swiglu_fused_fp8
  * K must be a positive multiple of 16; X, gamma and Aq 16-byte aligned.
- * Enqueues a 4-byte memset of *sA and two kernels on `stream` (the second
- * waits for the first through programmatic dependent launch); no host sync.
+ * Enqueues three kernels on `stream` (one that zeroes *sA, then an amax
+ * pass and a quantise pass, each waiting for its predecessor through
+ * programmatic dependent launch; rows longer than 25600 elements use a
+ * memset and two loop kernels instead); no host sync.
  * Aq and *sA must not overlap X or gamma.  M = 0 writes *sA = 0 only.
  */
 int swiglu_rmsnorm_quant_fp8(const void *X, const void *gamma, float eps, void *Aq, float *sA,

@@ -13,7 +13,9 @@
 // A row whose mean square plus eps is zero normalises to zeros; s = 0 gives
 // all-zero codes.
 //
-// Two passes, because the scale depends on every element:
+// Two passes, because the scale depends on every element.  Rows of up to
+// 25600 elements go through the shared-memory kernels further down; these
+// loop kernels serve longer rows:
 //   1. amax pass: one warp per row reads the row once, accumulating the sum
 //      of squares and max|x * gamma|; the row's max|a| is that max times
 //      1/rms (a positive factor, so the maximum commutes with the rounding),
@@ -30,8 +32,10 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
+#include "launch.h"
 #include "swiglu.h"
 
 namespace swiglu {
@@ -83,6 +87,18 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 template <bool GAMMA>
 __device__ __forceinline__ void load_row_vec(const uint4 *x, const uint4 *g, int v, float f[8]) {
   unpack_bf16x8(__ldg(x + v), f);
+  if (GAMMA) {
+    float gf[8];
+    unpack_bf16x8(__ldg(g + v), gf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], gf[i]);
+  }
+}
+
+template <bool GAMMA>
+__device__ __forceinline__ void load_row_vec_smem(const uint4 *x, const uint4 *g, int v,
+                                                  float f[8]) {
+  unpack_bf16x8(x[v], f);
   if (GAMMA) {
     float gf[8];
     unpack_bf16x8(__ldg(g + v), gf);
@@ -191,17 +207,192 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint4 *__restrict
   }
 }
 
+// ---- the same two passes with rows staged in shared memory ---------------
+//
+// Each block takes 4 rows: one thread copies them into shared memory with
+// bulk copies (the copy engine moves the whole 4-row tile at once), then each
+// warp reads its row from shared memory, once for the sum of squares and once
+// more for the maximum (amax pass) or the codes (quantise pass).  With a few
+// tens of KB per block, every SM has many rows in flight, which is what a
+// read of a few tens of MB needs to run at HBM speed.  The sum of squares
+// runs in the same order as in the loop kernels above.
+//
+// Launch chain, each later kernel with programmatic dependent launch:
+//   zero kernel (normal launch: starts after all earlier work has completed)
+//   -> amax pass: copies its rows in at once (X and gamma were complete
+//      before the zero kernel started), waits for the zero kernel only
+//      before its atomic maximum on the scale;
+//   -> quantise pass: likewise copies and reduces its rows first and waits
+//      for the amax pass only before it reads the scale.
+
+constexpr int kSmemRows = 4;                 // rows per block, one per warp
+constexpr int kSmemThreads = kSmemRows * 32;
+constexpr int kSmemMaxBytes = 200 * 1024;    // dynamic shared memory budget per block
+constexpr uint32_t kWaitProducerLoad = 8;    // where a wait gave up (device error word)
+
+__global__ void zero_scale_kernel(float *s) {
+  *s = 0.0f;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Bulk-copy this block's rows into shared memory and wait for them (bounded).
+__device__ __forceinline__ bool stage_rows(const uint8_t *X, int64_t row0, int nrows, int K,
+                                           uint32_t buf, uint32_t bar, uint32_t *err,
+                                           uint64_t timeout_ns) {
+  if (threadIdx.x == 0) {
+    const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
+    ptx::mbar_arrive_expect_tx(bar, row_bytes * nrows);
+    for (int r = 0; r < nrows; ++r)
+      ptx::bulk_load(buf + r * row_bytes, X + (row0 + r) * row_bytes, row_bytes, bar);
+  }
+  const uint64_t t0 = ptx::globaltimer_ns();
+  bool ok = true;
+  while (!ptx::mbar_try_wait(bar, 0)) {
+    if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+      ok = false;
+      break;
+    }
+  }
+  if (!ok && threadIdx.x == 0 && atomicCAS(err, 0u, kErrTimeout) == 0u)
+    atomicExch(err + 1, kWaitProducerLoad);
+  return __syncthreads_and(ok) != 0;
+}
+
+template <bool NORM, bool GAMMA, bool QUANT>
+__global__ void __launch_bounds__(kSmemThreads) rows_smem_kernel(
+    const uint8_t *__restrict__ X, const uint4 *__restrict__ gamma, float eps, int64_t M, int K,
+    float *scale, uint2 *__restrict__ Q, uint32_t *err, uint64_t timeout_ns) {
+  extern __shared__ __align__(16) uint8_t rows_smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ float red[kSmemRows];
+  if (!QUANT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = K / 8;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kSmemRows;
+  const int nrows = static_cast<int>(M - row0 < kSmemRows ? M - row0 : kSmemRows);
+  const uint32_t b = ptx::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = stage_rows(X, row0, nrows, K, ptx::smem_u32(rows_smem), b, err, timeout_ns);
+  const bool live = ok && warp < nrows;
+  const uint4 *x = reinterpret_cast<const uint4 *>(rows_smem) + warp * nvec;
+  float inv = 1.0f;
+  if (live && NORM) {
+    float ss = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+      float xf[8];
+      unpack_bf16x8(x[v], xf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = __fmaf_rn(xf[j], xf[j], ss);
+    }
+    inv = inv_rms(warp_sum(ss), K, eps);
+  }
+  if (!QUANT) {
+    float rm = 0.0f;
+    if (live) {
+      for (int v = lane; v < nvec; v += 32) {
+        float f[8];
+        load_row_vec_smem<GAMMA>(x, gamma, v, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) rm = fmaxf(rm, fabsf(f[j]));
+      }
+      rm = warp_max(rm);
+      if (NORM) rm = __fmul_rn(rm, inv);
+    }
+    if (lane == 0) red[warp] = rm;
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the zero kernel has written the scale
+    if (threadIdx.x == 0) {
+      float m = red[0];
+#pragma unroll
+      for (int i = 1; i < kSmemRows; ++i) m = fmaxf(m, red[i]);
+      atomicMax(reinterpret_cast<unsigned int *>(scale), __float_as_uint(__fdiv_rn(m, kE4M3Max)));
+    }
+    return;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the amax pass has finished the scale
+  if (!live) return;
+  const float s = *reinterpret_cast<const volatile float *>(scale);
+  const float rcp = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
+  const float c = NORM ? __fmul_rn(inv, rcp) : rcp;
+  uint2 *q = Q + (row0 + warp) * nvec;
+  for (int v = lane; v < nvec; v += 32) {
+    if (c == 0.0f) {  // zero scale or zero row: all codes +0
+      q[v] = make_uint2(0u, 0u);
+      continue;
+    }
+    float f[8];
+    load_row_vec_smem<GAMMA>(x, gamma, v, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = NORM ? __fmul_rn(f[j], c) : __fdiv_rn(f[j], s);
+    uint2 o;
+    o.x = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+    o.y = cvt_e4m3x2(f[4], f[5]) | (cvt_e4m3x2(f[6], f[7]) << 16);
+    q[v] = o;
+  }
+}
+
+template <bool NORM, bool GAMMA>
+cudaError_t launch_rows_smem(const void *X, const uint4 *g, float eps, void *Q, float *s,
+                             int64_t M, int K, uint32_t *err, uint64_t timeout_ns,
+                             cudaStream_t st) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(rows_smem_kernel<NORM, GAMMA, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMaxBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(rows_smem_kernel<NORM, GAMMA, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMaxBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int64_t blocks = (M + kSmemRows - 1) / kSmemRows;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(kSmemRows) * K * 2;
+  zero_scale_kernel<<<1, 32, 0, st>>>(s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kSmemThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint8_t *x = static_cast<const uint8_t *>(X);
+  uint2 *q = static_cast<uint2 *>(Q);
+  e = cudaLaunchKernelEx(&cfg, rows_smem_kernel<NORM, GAMMA, false>, x, g, eps, M, K, s, q, err,
+                         timeout_ns);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, rows_smem_kernel<NORM, GAMMA, true>, x, g, eps, M, K, s, q, err,
+                            timeout_ns);
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 template <bool NORM, bool GAMMA>
 cudaError_t launch_producer(const void *X, const void *gamma, float eps, void *Q, float *s,
                             int64_t M, int K, cudaStream_t st) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(s, 0, sizeof(float), st);
+  uint32_t *err = nullptr;
+  int sms = 0;
+  uint64_t timeout_ns = 0;
+  if (device_info(&err, &sms, &timeout_ns) != SWIGLU_OK) return cudaErrorUnknown;
+  if (M > 0 && int64_t(kSmemRows) * K * 2 <= kSmemMaxBytes)
+    return launch_rows_smem<NORM, GAMMA>(X, static_cast<const uint4 *>(gamma), eps, Q, s, M, K,
+                                         err, timeout_ns, st);
+  cudaError_t e = cudaMemsetAsync(s, 0, sizeof(float), st);
   if (e != cudaSuccess || M == 0) return e;
+  // longer rows: the loop kernels
   // Up to 8 blocks of 8 warps per SM (64 warps, the SM's limit), one warp per
   // row, grid-stride beyond that.
   const int64_t want = (M + kWarps - 1) / kWarps;

@@ -410,6 +410,19 @@ VariantGeom variant_geom(int variant, bool interleaved) {
   }
 }
 
+// This device's error word, SM count and wait limit, for kernels launched
+// from other translation units (one-time per-device set-up on first use).
+int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns) {
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  *err = st->err;
+  *sm_count = st->sm_count;
+  *timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  return SWIGLU_OK;
+}
+
 }  // namespace swiglu
 
 extern "C" {
