@@ -80,6 +80,12 @@ def _load():
         lib.oracle_rmsnorm_bf16.restype = ctypes.c_int
         lib.oracle_quant_e4m3.argtypes = [p, i64, p, p]
         lib.oracle_quant_e4m3.restype = ctypes.c_int
+        lib.oracle_int4_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_int4_value.restype = d
+        lib.oracle_dequant_int4.argtypes = [p, p, i64, i64, i64, p]
+        lib.oracle_dequant_int4.restype = ctypes.c_int
+        lib.oracle_swiglu_w4.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
+        lib.oracle_swiglu_w4.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -298,3 +304,38 @@ def quant_e4m3(a):
 def rmsnorm_quant_e4m3(X, gamma=None, eps: float = 1e-6):
     """RMSNorm then per-tensor E4M3 quantisation: returns (scale, codes [M,K])."""
     return quant_e4m3(rmsnorm_bf16(X, gamma, eps))
+
+
+# ---- weight-only INT4 -----------------------------------------------------
+
+def int4_value(nibble: int) -> float:
+    """Signed 4-bit two's complement value of a nibble."""
+    return _load().oracle_int4_value(int(nibble))
+
+
+def dequant_int4(Wq, S, G: int) -> np.ndarray:
+    """W[k,n] = BF16(q[k,n] * S[k // G, n]) in double: Wq [K, N/2] bytes (column
+    n in the low nibble when even, high when odd), S [K/G, N] BF16 bits."""
+    Wq = _u8(Wq)
+    S = _u16(S)
+    K, half = Wq.shape
+    N = 2 * half
+    W = np.empty((K, N), dtype=np.float64)
+    rc = _load().oracle_dequant_int4(_ptr(Wq), _ptr(S), K, N, int(G), _ptr(W))
+    if rc != 0:
+        raise ValueError("oracle_dequant_int4: K must be a multiple of G")
+    return W
+
+
+def swiglu_w4(A, W1q, S1, W2q, S2, G: int, rows=None) -> np.ndarray:
+    """The definition with INT4 weights (dequantised as in dequant_int4)."""
+    A, W1q, W2q, S1, S2 = _u16(A), _u8(W1q), _u8(W2q), _u16(S1), _u16(S2)
+    M, K = A.shape
+    N = 2 * W1q.shape[1]
+    r, nr = _rows(rows, M)
+    Y = np.empty((nr, N), dtype=np.float64)
+    rc = _load().oracle_swiglu_w4(_ptr(A), _ptr(W1q), _ptr(S1), _ptr(W2q), _ptr(S2), M, N, K,
+                                  int(G), _ptr(r) if r is not None else None, nr, _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_w4 failed")
+    return Y

@@ -520,3 +520,53 @@ int oracle_quant_e4m3(const double *a, int64_t n, float *scale, uint8_t *q)
     }
     return 0;
 }
+
+/* ---- weight-only INT4 (SURVEY.md row "lower-precision weight variants") ----
+ *
+ * The page names INT4 as a precision that raises tensor-core density
+ * (section "Definizione del Problema") without defining a format.  Reading
+ * (the plainest common one): signed 4-bit weights q in [-8, 7], two's
+ * complement, packed two per byte along N (byte k*(N/2) + n/2 holds column n
+ * in its low nibble when n is even, in its high nibble when n is odd), one
+ * BF16 scale per column and per group of G consecutive K rows; the weight the
+ * product uses is the BF16 value of q * s (q * s is exact in binary32; it is
+ * rounded once to BF16, nearest even), the form in which BF16 tensor cores
+ * consume it.  Everything after that is the BF16 definition above.
+ */
+double oracle_int4_value(uint8_t nibble)
+{
+    int v = nibble & 0xF;
+    return (double)(v < 8 ? v : v - 16);
+}
+
+/* W[k,n] = BF16(q[k,n] * S[k/G, n]) for Wq [K, N/2] bytes and S [K/G, N] BF16. */
+int oracle_dequant_int4(const uint8_t *Wq, const uint16_t *S, int64_t K, int64_t N, int64_t G,
+                        double *W)
+{
+    if (K < 0 || N < 0 || N % 2 != 0 || G <= 0 || K % G != 0)
+        return -1;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            uint8_t byte = Wq[k * (N / 2) + n / 2];
+            uint8_t nib = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+            double p = oracle_int4_value(nib) * oracle_bf16_to_f64(S[(k / G) * N + n]);
+            W[k * N + n] = oracle_bf16_to_f64(oracle_f64_to_bf16(p));
+        }
+    return 0;
+}
+
+/* Y = SiLU(A W1) (.) (A W2) with W1, W2 given as INT4 + group scales. */
+int oracle_swiglu_w4(const uint16_t *A, const uint8_t *W1q, const uint16_t *S1,
+                     const uint8_t *W2q, const uint16_t *S2, int64_t M, int64_t N, int64_t K,
+                     int64_t G, const int64_t *rows, int64_t nrows, double *Y)
+{
+    double *w1 = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    double *w2 = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    int rc = -1;
+    if (w1 && w2 && oracle_dequant_int4(W1q, S1, K, N, G, w1) == 0 &&
+        oracle_dequant_int4(W2q, S2, K, N, G, w2) == 0)
+        rc = swiglu_rows_f64(A, 0, 1.0, w1, w2, M, N, K, rows, nrows, NULL, NULL, Y);
+    free(w1);
+    free(w2);
+    return rc;
+}

@@ -110,3 +110,24 @@ def make_producer_inputs(M: int, K: int, seed: int):
     gamma = (1.0 + 0.1 * torch.randn(K, generator=g)).to(torch.bfloat16)
     X = torch.randn(M, K, generator=g).to(torch.bfloat16).contiguous()
     return X, gamma
+
+
+def quantize_int4(W: torch.Tensor, G: int = 128):
+    """Per-column, per-group symmetric INT4 codes of a [K,N] FP32 weight:
+    scale s = max|w| over the group / 7 (rounded to BF16), q = round(w / s)
+    clamped to [-8, 7]; returns (packed [K, N/2] uint8 with column n in the low
+    nibble when even, scales [K/G, N] BF16)."""
+    K, N = W.shape
+    Wg = W.reshape(K // G, G, N)
+    s = (Wg.abs().amax(dim=1) / 7.0).clamp_min(2.0 ** -100).to(torch.bfloat16)
+    q = torch.round(Wg / s.float().unsqueeze(1)).clamp(-8, 7).to(torch.int32).reshape(K, N)
+    nib = (q & 0xF).to(torch.uint8)
+    packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).contiguous()
+    return packed, s.contiguous()
+
+
+def make_w4(M: int, N: int, K: int, seed: int, G: int = 128):
+    """A [M,K] BF16 and INT4 weights of the same draws as make_bf16:
+    returns (A, (W1q, S1), (W2q, S2))."""
+    A, W1, W2 = draw_fp32(M, N, K, seed)
+    return (A.to(torch.bfloat16).contiguous(), quantize_int4(W1, G), quantize_int4(W2, G))

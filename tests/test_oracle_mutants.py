@@ -235,3 +235,42 @@ def test_planted_producer_mistake_is_caught(tmp_path, name):
     except AssertionError:      # the mutant broke a call outright
         failures = ["call failed"]
     assert failures, f"pins did not catch mutant {name}"
+
+
+# Planted mistakes in the INT4 weight path, caught by the INT4 pins.
+INT4_MUTANTS = {
+    "nibble_order": ("uint8_t nib = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
+                     "uint8_t nib = (n & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    "no_sign_extension": ("return (double)(v < 8 ? v : v - 16);", "return (double)v;"),
+    "group_by_modulo": ("oracle_bf16_to_f64(S[(k / G) * N + n]);", "oracle_bf16_to_f64(S[(k % G) * N + n]);"),
+    "no_bf16_rounding": ("W[k * N + n] = oracle_bf16_to_f64(oracle_f64_to_bf16(p));", "W[k * N + n] = p;"),
+}
+
+
+def _build_int4(tmp_path, name, src_text):
+    lib = _build(tmp_path, name, src_text)
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.oracle_int4_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_int4_value.restype = ctypes.c_double
+    lib.oracle_dequant_int4.argtypes = [p, p, i64, i64, i64, p]
+    lib.oracle_swiglu_w4.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
+    return lib
+
+
+def test_unmodified_oracle_passes_int4_pins(tmp_path):
+    from test_oracle_int4_pins import int4_pin_failures
+    assert int4_pin_failures(_build_int4(tmp_path, "orig_int4", open(SRC).read())) == []
+
+
+@pytest.mark.parametrize("name", sorted(INT4_MUTANTS))
+def test_planted_int4_mistake_is_caught(tmp_path, name):
+    from test_oracle_int4_pins import int4_pin_failures
+    src = open(SRC).read()
+    old, new = INT4_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique in the oracle source"
+    lib = _build_int4(tmp_path, name, src.replace(old, new, 1))
+    try:
+        failures = int4_pin_failures(lib)
+    except AssertionError:
+        failures = ["call failed"]
+    assert failures, f"pins did not catch mutant {name}"
