@@ -48,12 +48,16 @@ WORKLOADS = {
     # the FP8 projection fed by its producer (RMSNorm of the hidden state X and
     # per-tensor E4M3 quantisation of A), timed together
     "qwen2.5-7b-fp8-rmsnorm": (3584, 18944, (512, 4096), 4),
+    # INT4 weights (group 128), BF16 A and Y
+    "qwen2.5-0.5b-w4": (896, 4864, (64, 128, 512, 2048), 1),
+    "qwen2.5-7b-w4": (3584, 18944, (128, 256, 1024), 2),
     # the SwiGLU MLP block: (H, F, Ms, seed)
     "qwen2.5-0.5b-mlp": (896, 4864, (128, 512, 2048, 8192), 1),
     "qwen2.5-7b-mlp": (3584, 18944, (256, 1024, 4096), 2),
 }
 DEFAULT_WORKLOAD = "qwen2.5-0.5b"
 RMS_EPS = 1e-6   # RMSNorm epsilon of the producer workload (Qwen-2.5's value)
+W4_GROUP = 128   # K rows per INT4 scale group
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CSRC = os.path.join(ROOT, "swiglu_gemm_transformer_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -211,10 +215,11 @@ class Workload:
         self.dev = dev
         self.producer = name.endswith("-fp8-rmsnorm")
         self.kind = ("fp8" if name.endswith("-fp8") or self.producer else
-                     "mlp" if name.endswith("-mlp") else "bf16")
+                     "mlp" if name.endswith("-mlp") else "w4" if name.endswith("-w4") else "bf16")
         self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
-        forms = ("mlp",) if self.kind == "mlp" else ("separate", "interleaved")
+        forms = (("mlp",) if self.kind == "mlp" else ("separate",) if self.kind == "w4"
+                 else ("separate", "interleaved"))
         self.host = {}
         for M in Ms:
             if self.producer:   # X and gamma in BF16; the FP8 weights of the same recipe
@@ -224,6 +229,9 @@ class Workload:
             elif self.fp8:
                 q, sc = si.make_e4m3(M, N, K, seed)
                 self.host[M] = (q[0], q[1].t().contiguous(), q[2].t().contiguous(), sc)
+            elif self.kind == "w4":
+                A, (W1q, S1), (W2q, S2) = si.make_w4(M, N, K, seed, W4_GROUP)
+                self.host[M] = (A, W1q, S1, W2q, S2)
             elif self.kind == "mlp":   # K = H (hidden), N = F (intermediate)
                 A, W1, W2 = si.make_bf16(M, N, K, seed)
                 self.host[M] = (A, W1, W2, si.make_bf16(1, K, N, seed + 100)[1])
@@ -255,6 +263,9 @@ class Workload:
         with the producer, A's codes are written once and read once more)."""
         if self.kind == "mlp":
             return 2 * (M * self.K + 3 * self.K * self.N + M * self.K)
+        if self.kind == "w4":   # A, two code matrices, two scale matrices, Y
+            return (2 * M * self.K + 2 * (self.K * self.N // 2)
+                    + 2 * (self.K // W4_GROUP) * self.N * 2 + 2 * M * self.N)
         b = self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
         if self.producer:
             b += self.producer_bytes(M)
@@ -273,6 +284,8 @@ class Workload:
         dev, sg = self.dev, self.sg
         h = self.host[M]
         out = torch.empty(self.out_shape(M), dtype=torch.bfloat16, device=dev)
+        if self.kind == "w4":
+            return tuple(t.to(dev) for t in h) + (out,)
         if self.kind == "mlp":
             ws = torch.empty(int(self.lib.swiglu_mlp_workspace_size(M, self.K, self.N)),
                              dtype=torch.uint8, device=dev)
@@ -302,6 +315,9 @@ class Workload:
         def check(name, rc):
             if rc:
                 raise sg.SwigluError(name, rc)
+        if self.kind == "w4":
+            return lambda: check("swiglu_fused_w4", lib.swiglu_fused_w4(
+                d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, W4_GROUP, self._stream()))
         if self.kind == "mlp":
             nbytes = bufs[5].numel()
             return lambda: check("swiglu_mlp", lib.swiglu_mlp(d[0], d[1], d[2], d[3], None, d[4],
@@ -350,6 +366,8 @@ class Workload:
     def api_call(self, form, M, v, bufs):
         """The same call through the public Python API; returns the output tensor."""
         sg = self.sg
+        if self.kind == "w4":
+            return sg.swiglu_fused_w4(*bufs[:5], bufs[5], group=W4_GROUP)
         if self.kind == "mlp":
             return sg.swiglu_mlp(bufs[0], bufs[1], bufs[2], bufs[3], None, bufs[4], workspace=bufs[5])
         if self.fp8:
@@ -380,6 +398,8 @@ class Workload:
             return "mlp"
         if self.producer:
             return "rmsnorm_quant+2sm_fp8"
+        if self.kind == "w4":
+            return "w4_sk2"
         return "2sm_fp8" if self.fp8 else self.sg.variant_name(v)
 
     def step(self):
@@ -562,6 +582,9 @@ def run_ours(args, ws, rank, local):
                          f"producer (RMSNorm of X, eps {RMS_EPS}, per-tensor E4M3 quantisation), "
                          f"separate and interleaved weights, seed {wl.seed}"
                          if wl.producer else
+                         f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)} with INT4 "
+                         f"weights (group {W4_GROUP}, BF16 scales), BF16 A and Y, seed {wl.seed}"
+                         if wl.kind == "w4" else
                          f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
                          f"separate and interleaved weights, seed {wl.seed}"),
             "calls_per_step": n_calls,
@@ -705,7 +728,7 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
     the same inputs, per call and as one step; fusion efficiency per call;
     optionally the same function under torch.compile."""
     import torch
-    if wl.fp8:
+    if wl.fp8 or wl.kind == "w4":
         return None
     factory = unfused_factory(wl)
     eager_us = measure_calls(wl, stream, args.call_launches, factory)
@@ -775,6 +798,11 @@ def oracle_sample(workload: str, target_s: float):
     mlp = workload.endswith("-mlp")
     fp8 = workload.endswith("-fp8")
     prod = workload.endswith("-fp8-rmsnorm")
+    w4 = workload.endswith("-w4")
+    if w4:
+        A4, (W1q, S1), (W2q, S2) = si.make_w4(max(Ms), N, K, seed, W4_GROUP)
+        a4 = si.bits_u16(A4)
+        w4args = (W1q.numpy(), si.bits_u16(S1), W2q.numpy(), si.bits_u16(S2), W4_GROUP)
     if prod:   # the producer's inputs per M, the FP8 weights of the same recipe
         (_, W1q, W2q), sc = si.make_e4m3(1, N, K, seed)
         w18, w28 = si.bits_u8(W1q), si.bits_u8(W2q)
@@ -787,7 +815,7 @@ def oracle_sample(workload: str, target_s: float):
         a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
         wf = oracle.pack_interleaved(w1, w2)
         w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
-    forms = ("mlp",) if mlp else ("separate", "interleaved")
+    forms = ("mlp",) if mlp else ("separate",) if w4 else ("separate", "interleaved")
     per_row = (6 if mlp else 4) * N * K
 
     def one(rows_per_call):
@@ -796,7 +824,9 @@ def oracle_sample(workload: str, target_s: float):
         for form in forms:
             for M in Ms:
                 rows = np.sort(rng.integers(0, M, size=rows_per_call))
-                if prod:   # RMSNorm and quantisation of all of A (the scale needs every row)
+                if w4:
+                    oracle.swiglu_w4(a4[:M], *w4args, rows=rows)
+                elif prod:   # RMSNorm and quantisation of all of A (the scale needs every row)
                     sA, aq = oracle.rmsnorm_quant_e4m3(xg[M][0], xg[M][1], RMS_EPS)
                     oracle.swiglu_e4m3(aq, w18, w28, sA, sc[1], sc[2], rows=rows)
                 elif mlp:

@@ -150,6 +150,30 @@ int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t
                                 int64_t K, void *stream);
 
 /*
+ * INT4 weights (weight-only quantisation; the page names INT4 in section
+ * "Definizione del Problema" as a precision that raises tensor-core density,
+ * without fixing a format).  Format: signed 4-bit two's complement codes,
+ * packed two per byte along N (byte k*(N/2) + n/2 holds column n in its low
+ * nibble when n is even, in its high nibble when n is odd); one BF16 scale per
+ * column and per group of `group` consecutive K rows.  The weight is
+ * BF16(q * s) (the product rounded once, to nearest even); the result is the
+ * BF16 definition with those weights:
+ *     Y = SiLU(A x W1) (.) (A x W2),  W[k,n] = BF16(q[k,n] * S[k/group, n])
+ *   A        : device, BF16 [M,K] row-major      (read)
+ *   W1q, W2q : device, uint8 [K, N/2] row-major  (read)
+ *   S1, S2   : device, BF16 [K/group, N]         (read)
+ *   Y        : device, BF16 [M,N] row-major      (written)
+ * group must be a multiple of 64 dividing K; N a multiple of 32; K a multiple
+ * of 8; pointers 16-byte aligned.  Runs the split-K cluster kernel
+ * (SWIGLU_VARIANT_1SM_N64_SK2's structure) whose epilogue warps decode each
+ * stage's codes to BF16 in shared memory before the MMA reads them: the
+ * weight stream is 4.1 bits per weight instead of 16.
+ */
+int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *W2q,
+                    const void *S2, void *Y, int64_t M, int64_t N, int64_t K, int64_t group,
+                    void *stream);
+
+/*
  * The producer of the FP8 form's A operand: RMSNorm of each row of X followed
  * by per-tensor E4M3 quantisation (FP8 quantisation is what the page's
  * section "Definizione del Problema" names as raising tensor-core density; the

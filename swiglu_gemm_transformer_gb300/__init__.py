@@ -40,6 +40,7 @@ EXPORTS = {
     "swiglu_pack_interleaved_fp8": ("ppp ll p", ctypes.c_int),
     "swiglu_rmsnorm_quant_fp8": ("pp f pp ll p", ctypes.c_int),
     "swiglu_quant_fp8": ("ppp ll p", ctypes.c_int),
+    "swiglu_fused_w4": ("ppppp p lll l p", ctypes.c_int),
     "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
     "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
     "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
@@ -298,6 +299,29 @@ def swiglu_quant_fp8(X, Xq=None, s=None, *, stream=None):
     rc = lib().swiglu_quant_fp8(X.data_ptr(), Xq.data_ptr(), _scale(s, "s"), M, K, _stream(stream))
     _check("swiglu_quant_fp8", rc)
     return Xq, s
+
+
+def swiglu_fused_w4(A, W1q, S1, W2q, S2, Y=None, *, group: int = 128, stream=None):
+    """Y = SiLU(A @ W1) * (A @ W2) with INT4 weights: W1q/W2q uint8 [K, N/2]
+    (two codes per byte along N), S1/S2 BF16 [K/group, N]."""
+    import torch
+    _need(A, "A", torch.bfloat16)
+    _need(W1q, "W1q", torch.uint8), _need(W2q, "W2q", torch.uint8)
+    _need(S1, "S1", torch.bfloat16), _need(S2, "S2", torch.bfloat16)
+    M, K = A.shape
+    N = 2 * W1q.shape[1]
+    if W1q.shape[0] != K or W2q.shape != W1q.shape or S1.shape != (K // group, N) or S2.shape != S1.shape:
+        raise ValueError("shape mismatch")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _need(Y, "Y", torch.bfloat16)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [M, N]")
+    rc = lib().swiglu_fused_w4(A.data_ptr(), W1q.data_ptr(), S1.data_ptr(), W2q.data_ptr(),
+                               S2.data_ptr(), Y.data_ptr(), M, N, K, int(group), _stream(stream))
+    _check("swiglu_fused_w4", rc)
+    return Y
 
 
 def _workspace(nbytes, device, workspace):

@@ -33,7 +33,7 @@ cudaError_t launch_sk(const LaunchArgs &la) {
   cfg.stream = la.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
+  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.s1, la.s2, la.p);
 }
 
 }  // namespace
@@ -41,5 +41,7 @@ cudaError_t launch_sk(const LaunchArgs &la) {
 cudaError_t launch_bf16_sk(bool interleaved, const LaunchArgs &la) {
   return interleaved ? launch_sk<SkCfg<true>>(la) : launch_sk<SkCfg<false>>(la);
 }
+
+cudaError_t launch_w4_sk(const LaunchArgs &la) { return launch_sk<SkCfg<false, true>>(la); }
 
 }  // namespace swiglu

@@ -13,6 +13,7 @@ namespace swiglu {
 
 struct LaunchArgs {
   CUtensorMap a, b0, b1, y;
+  CUtensorMap s1, s2;  // INT4 weights: the gate and up scale matrices
   KParams p;
   int grid;
   int device;
@@ -34,6 +35,7 @@ VariantGeom variant_geom(int variant, bool interleaved);
 cudaError_t launch_bf16_separate(int variant, const LaunchArgs &la);
 cudaError_t launch_bf16_interleaved(int variant, const LaunchArgs &la);
 cudaError_t launch_bf16_sk(bool interleaved, const LaunchArgs &la);
+cudaError_t launch_w4_sk(const LaunchArgs &la);
 int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns);
 cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf, int64_t n_elems,
                                         int sm_count, cudaStream_t s);

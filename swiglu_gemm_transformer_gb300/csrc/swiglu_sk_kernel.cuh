@@ -48,9 +48,14 @@ namespace swiglu {
 
 enum : uint32_t { WAIT_SK_RECV = 7 };
 
-template <bool INTERLEAVED_>
+// W4_: the weights arrive as INT4 codes (two per byte along N) with one BF16
+// scale per column and group of K rows; the epilogue warps, idle during the
+// K loop, decode each stage's codes into the BF16 operand layout the MMA
+// reads (see the W4 paragraph above the kernel).
+template <bool INTERLEAVED_, bool W4_ = false>
 struct SkCfg {
   static constexpr bool INTERLEAVED = INTERLEAVED_;
+  static constexpr bool W4 = W4_;
   static constexpr int BM = 128;                 // rows per tile (MMA M)
   static constexpr int BK = 64;                  // K per stage
   static constexpr int BN = 64;                  // output columns per tile
@@ -63,8 +68,15 @@ struct SkCfg {
   static constexpr int B_SBO = 8 * ROW_BYTES;
   static constexpr int B_KSTEP = 16 * ROW_BYTES;
   static constexpr int B_BYTES = NB_ATOMS * ATOM_BYTES;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
-  static constexpr int STAGES = 6;
+  // W4: per weight matrix a [64 K x 32 byte] box of codes and a [1 x 64] box
+  // of scales, behind the A tile and the decoded B tiles of the stage
+  static constexpr int RAW_W_BYTES = BK * (ATOM_COLS / 2);      // 2 KB
+  static constexpr int RAW_S_BYTES = ATOM_COLS * 2;             // 128 B
+  static constexpr int RAW_OFF = A_BYTES + B_BYTES;
+  static constexpr int RAW_BYTES = W4 ? 2 * (RAW_W_BYTES + RAW_S_BYTES) : 0;
+  static constexpr int TMA_BYTES = A_BYTES + (W4 ? RAW_BYTES : B_BYTES);  // bytes TMA lands per stage
+  static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + RAW_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGES = W4 ? 5 : 6;
   // Receive buffer: the peer's partial gate and up sums of the 32 output
   // columns this CTA keeps, for all 128 rows: value v (v < 32: gate of kept
   // output v; v >= 32: up of kept output v - 32) of row i at
@@ -74,7 +86,7 @@ struct SkCfg {
   static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
   static constexpr int RECV_BYTES = BM * 2 * KEEP * 4;  // 32 KB
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], acc_full, recv, drain
+  static constexpr int NUM_BARS = 3 * STAGES + 3;  // full[S], empty[S], decoded[S], acc_full, recv, drain
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
   static constexpr int EPI_WARPS = 8;            // 4 TMEM lane groups x 2 column halves
   static constexpr int PRODUCER_WARP = 8;
@@ -83,6 +95,7 @@ struct SkCfg {
   static constexpr int TMEM_COLS = 128;
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(!W4 || !INTERLEAVED, "INT4 weights: separate form only");
 };
 
 // This warp's 32 rows x 16 outputs starting at tile output `o0`: gate and up
@@ -120,12 +133,65 @@ __device__ __forceinline__ static void sk_load16(uint32_t tacc, bool have_acc, i
   }
 }
 
+// INT4 weights: decode one stage's codes and scales into the two BF16 weight
+// tiles the MMA reads, [64 K rows x 64 columns] each in the layout a TMA copy
+// with the 128-byte swizzle would leave (row k at 128 k bytes, its 16-byte
+// chunk j -- columns 8j .. 8j+7 -- at position j ^ (k % 8)).
+//
+// Weight = BF16(q * s), in packed BF16 pairs: flipping each code's sign bit
+// gives the offset-binary n = q + 8, and the BF16 pattern 0x4300 | n is the
+// number 128 + n exactly; subtracting 136 leaves q exactly; one BF16 multiply
+// by the scale pair then rounds q * s once, to nearest even.  Byte b of a
+// 4-byte group of codes holds columns 8j + 2b (low nibble) and 8j + 2b + 1
+// (high nibble), and the scales of those two columns are adjacent in memory,
+// so each 32-bit word of the scale vector is the pair a product needs.
+//
+// Thread `tid` of the 256 epilogue threads owns one column chunk j of one
+// weight matrix t and rows rr, rr + 16, rr + 32, rr + 48: it loads its eight
+// scales once per stage, and a warp's code loads and tile stores each cover
+// 512 contiguous bytes.
+template <class C>
+__device__ __forceinline__ static void w4_decode_stage(uint8_t *stage, int tid) {
+  static_assert(C::EPI_WARPS == 8 && C::BK == 64, "decode mapping: 256 threads, 64 rows");
+  const int t = tid >> 7;          // 0: gate weights, 1: up weights
+  const int j = tid & 7;           // columns 8j .. 8j + 7
+  const int rr = (tid >> 3) & 15;  // rows rr + 16 i
+  const uint8_t *raw_w = stage + C::RAW_OFF + t * C::RAW_W_BYTES;
+  const uint4 sv = *reinterpret_cast<const uint4 *>(stage + C::RAW_OFF + 2 * C::RAW_W_BYTES +
+                                                    t * C::RAW_S_BYTES + j * 16);
+  const __nv_bfloat162 sc[4] = {*reinterpret_cast<const __nv_bfloat162 *>(&sv.x),
+                                *reinterpret_cast<const __nv_bfloat162 *>(&sv.y),
+                                *reinterpret_cast<const __nv_bfloat162 *>(&sv.z),
+                                *reinterpret_cast<const __nv_bfloat162 *>(&sv.w)};
+  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
+  uint8_t *tile = stage + C::A_BYTES + t * C::ATOM_BYTES;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = rr + 16 * i;
+    const uint32_t codes = *reinterpret_cast<const uint32_t *>(raw_w + k * 32 + j * 4) ^ 0x88888888u;
+    uint32_t out[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t w = ((codes >> (8 * b)) & 0xFu) | (((codes >> (8 * b + 4)) & 0xFu) << 16) |
+                         0x43004300u;
+      const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&w), k136);
+      const __nv_bfloat162 v = __hmul2(q, sc[b]);
+      out[b] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+    *reinterpret_cast<uint4 *>(tile + k * 128 + ((j ^ (k & 7)) * 16)) =
+        make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     swiglu_bf16_sk_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB0,  // W1, or W_fused
                           const __grid_constant__ CUtensorMap tmB1,  // W2 (separate form only)
-                          const __grid_constant__ CUtensorMap tmY, const KParams p) {
+                          const __grid_constant__ CUtensorMap tmY,
+                          const __grid_constant__ CUtensorMap tmS1,  // INT4: gate scales
+                          const __grid_constant__ CUtensorMap tmS2,  // INT4: up scales
+                          const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -137,6 +203,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const uint32_t accf_bar = bars + 8u * (2 * C::STAGES);
   const uint32_t recv_bar = bars + 8u * (2 * C::STAGES + 1);
   const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 2);
+  auto dec_bar = [&](int s) { return bars + 8u * (2 * C::STAGES + 3 + s); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -165,13 +232,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::mbar_init(accf_bar, 1);
     ptx::mbar_init(recv_bar, 1);
     ptx::mbar_init(drain_bar, 1);
+    for (int s = 0; s < C::STAGES; ++s) ptx::mbar_init(dec_bar(s), C::EPI_WARPS);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     if (recv_bytes) ptx::mbar_arrive_expect_tx(recv_bar, recv_bytes);
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB0);
     if (!C::INTERLEAVED) ptx::prefetch_tmap(&tmB1);
-    ptx::prefetch_tmap(&tmY);
+    if (C::W4) {
+      ptx::prefetch_tmap(&tmS1);
+      ptx::prefetch_tmap(&tmS2);
+    }
   }
   if (warp == C::MMA_WARP) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
@@ -183,7 +254,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   ptx::grid_launch_dependents();
   auto load_w = [&](uint32_t sb, uint32_t fb, int kb) {
-    if (C::INTERLEAVED) {
+    if (C::W4) {  // codes and scales of both weight matrices, behind the BF16 tiles
+      const uint32_t r = sb - C::A_BYTES + C::RAW_OFF;
+      const int g = kb * C::BK / p.w4_group;
+      ptx::tma_load_2d(r, &tmB0, fb, nb * (C::BN / 2), kb * C::BK);
+      ptx::tma_load_2d(r + C::RAW_W_BYTES, &tmB1, fb, nb * (C::BN / 2), kb * C::BK);
+      ptx::tma_load_2d(r + 2 * C::RAW_W_BYTES, &tmS1, fb, nb * C::BN, g);
+      ptx::tma_load_2d(r + 2 * C::RAW_W_BYTES + C::RAW_S_BYTES, &tmS2, fb, nb * C::BN, g);
+    } else if (C::INTERLEAVED) {
       ptx::tma_load_2d(sb, &tmB0, fb, nb * C::MMA_N, kb * C::BK);
       ptx::tma_load_2d(sb + C::ATOM_BYTES, &tmB0, fb, nb * C::MMA_N + C::ATOM_COLS, kb * C::BK);
     } else {
@@ -198,7 +276,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     pre = static_cast<uint32_t>(kb1 - kb0 < C::STAGES ? kb1 - kb0 : C::STAGES);
     if (lane == 0)
       for (uint32_t s = 0; s < pre; ++s) {
-        ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+        ptx::mbar_arrive_expect_tx(full_bar(s), C::TMA_BYTES);
         load_w(base + s * C::STAGE_BYTES + C::A_BYTES, full_bar(s), kb0 + (int)s);
       }
     __syncwarp();
@@ -220,7 +298,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t sa = base + stage * C::STAGE_BYTES;
         const uint32_t sb = sa + C::A_BYTES;
         const uint32_t fb = full_bar(stage);
-        if (!early) ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        if (!early) ptx::mbar_arrive_expect_tx(fb, C::TMA_BYTES);
         ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
         if (!early) load_w(sb, fb, kb);
         ++issued;
@@ -243,7 +321,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
+        if (!wait_bar(C::W4 ? dec_bar(stage) : full_bar(stage), phase, p.timeout_ns, abort_flag,
+                      p.err, WAIT_MMA_FULL)) {
           ok = false;
           break;
         }
@@ -277,7 +356,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int q = warp & 3;
     const int h = warp >> 2;
     const int row = q * 32 + lane;  // tile row of this thread
-    bool ok = wait_bar(accf_bar, 0, p.timeout_ns, abort_flag, p.err, WAIT_EPI_ACC_FULL);
+    bool ok = true;
+    if (C::W4) {  // during the K loop: decode each stage's weights for the MMA
+      uint32_t stage = 0, phase = 0;
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
+        ok = wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        w4_decode_stage<C>(smem + stage * C::STAGE_BYTES, static_cast<int>(threadIdx.x));
+        ptx::fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(dec_bar(stage));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ok = ok && wait_bar(accf_bar, 0, p.timeout_ns, abort_flag, p.err, WAIT_EPI_ACC_FULL);
     ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);

@@ -44,6 +44,9 @@ struct KParams {
   int32_t k_splits, kb_per_split;
   // Y itself (the split-K small-M kernel stores its few rows directly).
   void *Y;
+  // INT4 weights: K rows per scale group (a multiple of 64).
+  int32_t w4_group;
+  int32_t pad2_;
 };
 
 // Bounded wait, slow path.  Returns false on timeout or when another role of
