@@ -86,6 +86,16 @@ def _load():
         lib.oracle_dequant_int4.restype = ctypes.c_int
         lib.oracle_swiglu_w4.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
         lib.oracle_swiglu_w4.restype = ctypes.c_int
+        lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_to_f64.restype = d
+        lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_to_f64.restype = d
+        lib.oracle_dequant_mxfp8.argtypes = [p, p, i64, i64, p]
+        lib.oracle_dequant_mxfp8.restype = ctypes.c_int
+        lib.oracle_dequant_nvfp4.argtypes = [p, p, d, i64, i64, p]
+        lib.oracle_dequant_nvfp4.restype = ctypes.c_int
+        lib.oracle_swiglu_mx.argtypes = [p, ctypes.c_int, p, p, d, p, p, d, i64, i64, i64, p, i64, p]
+        lib.oracle_swiglu_mx.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -338,4 +348,55 @@ def swiglu_w4(A, W1q, S1, W2q, S2, G: int, rows=None) -> np.ndarray:
                                   int(G), _ptr(r) if r is not None else None, nr, _ptr(Y))
     if rc != 0:
         raise ValueError("oracle_swiglu_w4 failed")
+    return Y
+
+
+# ---- weight-only MXFP8 and NVFP4 -------------------------------------------
+
+def e2m1_to_f64(code: int) -> float:
+    return _load().oracle_e2m1_to_f64(int(code))
+
+
+def e8m0_to_f64(e: int) -> float:
+    return _load().oracle_e8m0_to_f64(int(e))
+
+
+def dequant_mxfp8(C, S) -> np.ndarray:
+    """W[k,n] = BF16(E4M3(C[k,n]) * 2^(S[k//32, n] - 127)); C [K,N], S [K/32,N] bytes."""
+    C, S = _u8(C), _u8(S)
+    K, N = C.shape
+    W = np.empty((K, N), dtype=np.float64)
+    if _load().oracle_dequant_mxfp8(_ptr(C), _ptr(S), K, N, _ptr(W)) != 0:
+        raise ValueError("oracle_dequant_mxfp8: K must be a multiple of 32")
+    return W
+
+
+def dequant_nvfp4(C, S, global_scale: float) -> np.ndarray:
+    """W[k,n] = E2M1(c[k,n]) * E4M3(S[k//16, n]) * global; C [K, N/2] packed (even
+    column in the low nibble), S [K/16, N] E4M3 bytes."""
+    C, S = _u8(C), _u8(S)
+    K, half = C.shape
+    W = np.empty((K, 2 * half), dtype=np.float64)
+    if _load().oracle_dequant_nvfp4(_ptr(C), _ptr(S), float(global_scale), K, 2 * half, _ptr(W)) != 0:
+        raise ValueError("oracle_dequant_nvfp4: K must be a multiple of 16")
+    return W
+
+
+def swiglu_mx(A, fmt: str, w1, w2, rows=None) -> np.ndarray:
+    """The definition with block-scaled weights: fmt "mxfp8" with w = (C, S), or
+    "nvfp4" with w = (C, S, global)."""
+    A = _u16(A)
+    M, K = A.shape
+    f = 0 if fmt == "mxfp8" else 1
+    C1, S1 = _u8(w1[0]), _u8(w1[1])
+    C2, S2 = _u8(w2[0]), _u8(w2[1])
+    g1 = float(w1[2]) if f else 1.0
+    g2 = float(w2[2]) if f else 1.0
+    N = C1.shape[1] * (2 if f else 1)
+    r, nr = _rows(rows, M)
+    Y = np.empty((nr, N), dtype=np.float64)
+    rc = _load().oracle_swiglu_mx(_ptr(A), f, _ptr(C1), _ptr(S1), g1, _ptr(C2), _ptr(S2), g2,
+                                  M, N, K, _ptr(r) if r is not None else None, nr, _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_mx failed")
     return Y

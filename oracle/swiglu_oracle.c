@@ -570,3 +570,83 @@ int oracle_swiglu_w4(const uint16_t *A, const uint8_t *W1q, const uint16_t *S1,
     free(w2);
     return rc;
 }
+
+/* ---- weight-only MXFP8 and NVFP4 (the block-scaled formats the GEMM page
+ * names for Blackwell: "MXFP8" and "NVFP4" in its benchmark paragraph) ------
+ *
+ * Readings (the page names the formats only; these follow the published OCP
+ * Microscaling specification and NVIDIA's NVFP4 description):
+ *   MXFP8: E4M3 element codes (one byte each, row-major [K,N]); every block of
+ *     32 consecutive K rows of a column shares one E8M0 scale (byte e: the
+ *     value 2^(e - 127), e = 255 is NaN), scales [K/32, N].  Weight =
+ *     BF16(E4M3(c) * 2^(e-127)) (exact unless the value leaves BF16's normal
+ *     range).
+ *   NVFP4: E2M1 element codes (1 sign, 2 exponent bits with bias 1, 1
+ *     mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), packed two per
+ *     byte along N like the INT4 codes; every block of 16 consecutive K rows
+ *     of a column shares an E4M3 scale, scales [K/16, N]; one FP32 scale per
+ *     tensor on top.  Weight = E2M1(c) * E4M3(s) * global.
+ */
+double oracle_e2m1_to_f64(uint8_t code)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double v = mag[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+double oracle_e8m0_to_f64(uint8_t e)
+{
+    if (e == 255)
+        return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* W[k,n] = BF16(E4M3(C[k,n]) * E8M0(S[k/32, n])); C [K,N], S [K/32, N]. */
+int oracle_dequant_mxfp8(const uint8_t *C, const uint8_t *S, int64_t K, int64_t N, double *W)
+{
+    if (K < 0 || N < 0 || K % 32 != 0)
+        return -1;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            double v = oracle_e4m3_to_f64(C[k * N + n]) * oracle_e8m0_to_f64(S[(k / 32) * N + n]);
+            W[k * N + n] = oracle_bf16_to_f64(oracle_f64_to_bf16(v));
+        }
+    return 0;
+}
+
+/* W[k,n] = E2M1(c[k,n]) * E4M3(S[k/16, n]) * global; C [K, N/2] packed. */
+int oracle_dequant_nvfp4(const uint8_t *C, const uint8_t *S, double global, int64_t K, int64_t N,
+                         double *W)
+{
+    if (K < 0 || N < 0 || N % 2 != 0 || K % 16 != 0)
+        return -1;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            uint8_t byte = C[k * (N / 2) + n / 2];
+            uint8_t code = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+            W[k * N + n] = oracle_e2m1_to_f64(code) * oracle_e4m3_to_f64(S[(k / 16) * N + n]) * global;
+        }
+    return 0;
+}
+
+/* Y = SiLU(A W1) (.) (A W2) with MXFP8 (fmt 0) or NVFP4 (fmt 1) weights;
+ * g1, g2: the NVFP4 per-tensor scales (ignored for MXFP8). */
+int oracle_swiglu_mx(const uint16_t *A, int fmt, const uint8_t *C1, const uint8_t *S1, double g1,
+                     const uint8_t *C2, const uint8_t *S2, double g2, int64_t M, int64_t N,
+                     int64_t K, const int64_t *rows, int64_t nrows, double *Y)
+{
+    double *w1 = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    double *w2 = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    int rc = -1;
+    if (w1 && w2) {
+        int ok = fmt == 0 ? (oracle_dequant_mxfp8(C1, S1, K, N, w1) == 0 &&
+                             oracle_dequant_mxfp8(C2, S2, K, N, w2) == 0)
+                          : (oracle_dequant_nvfp4(C1, S1, g1, K, N, w1) == 0 &&
+                             oracle_dequant_nvfp4(C2, S2, g2, K, N, w2) == 0);
+        if (ok)
+            rc = swiglu_rows_f64(A, 0, 1.0, w1, w2, M, N, K, rows, nrows, NULL, NULL, Y);
+    }
+    free(w1);
+    free(w2);
+    return rc;
+}

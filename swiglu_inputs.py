@@ -131,3 +131,50 @@ def make_w4(M: int, N: int, K: int, seed: int, G: int = 128):
     returns (A, (W1q, S1), (W2q, S2))."""
     A, W1, W2 = draw_fp32(M, N, K, seed)
     return (A.to(torch.bfloat16).contiguous(), quantize_int4(W1, G), quantize_int4(W2, G))
+
+
+_E2M1_MAG = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def quantize_mxfp8(W: torch.Tensor):
+    """MXFP8 codes of a [K,N] FP32 weight: per block of 32 K rows of a column
+    the E8M0 exponent e = 127 + ceil(log2(max|w| / 448)) (the smallest power of
+    two that brings the block within E4M3's range), codes = E4M3(w / 2^(e-127))
+    (torch's RNE cast).  Returns (codes [K,N] uint8, scales [K/32,N] uint8)."""
+    K, N = W.shape
+    Wb = W.reshape(K // 32, 32, N)
+    amax = Wb.abs().amax(dim=1).clamp_min(2.0 ** -120)
+    e = (127 + torch.ceil(torch.log2(amax / 448.0))).clamp(0, 254)
+    scale = torch.pow(2.0, e - 127)
+    q = (Wb / scale.unsqueeze(1)).clamp(-448, 448).to(torch.float8_e4m3fn)
+    return q.reshape(K, N).view(torch.uint8).contiguous(), e.to(torch.uint8).contiguous()
+
+
+def quantize_nvfp4(W: torch.Tensor):
+    """NVFP4 codes of a [K,N] FP32 weight: a per-tensor FP32 scale
+    g = max|w| / (6 * 448); per block of 16 K rows of a column the E4M3 scale
+    s = E4M3(max|w| / 6 / g); codes = the E2M1 value nearest |w| / (s g) (ties
+    to the smaller magnitude), with the sign bit, packed two per byte along N.
+    Returns (packed [K, N/2] uint8, scales [K/16, N] uint8, g)."""
+    K, N = W.shape
+    g = float(W.abs().max()) / (6.0 * 448.0)
+    g = g if g > 0 else 1.0
+    Wb = W.reshape(K // 16, 16, N)
+    amax = Wb.abs().amax(dim=1)
+    s8 = (amax / 6.0 / g).clamp(max=448.0).to(torch.float8_e4m3fn)
+    s = s8.float().clamp_min(2.0 ** -9)
+    x = (Wb / (s.unsqueeze(1) * g)).abs()
+    mags = torch.tensor(_E2M1_MAG)
+    code = (x.unsqueeze(-1) - mags).abs().argmin(dim=-1).to(torch.uint8)
+    code = code | ((Wb < 0).to(torch.uint8) << 3)
+    code = code.reshape(K, N)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).contiguous()
+    return packed, s8.view(torch.uint8).contiguous(), g
+
+
+def make_mx(M: int, N: int, K: int, seed: int, fmt: str):
+    """A [M,K] BF16 and the weights of the BF16 recipe's draws in MXFP8
+    (fmt "mxfp8": (codes, scales)) or NVFP4 ("nvfp4": (codes, scales, g))."""
+    A, W1, W2 = draw_fp32(M, N, K, seed)
+    q = quantize_mxfp8 if fmt == "mxfp8" else quantize_nvfp4
+    return A.to(torch.bfloat16).contiguous(), q(W1), q(W2)

@@ -274,3 +274,47 @@ def test_planted_int4_mistake_is_caught(tmp_path, name):
     except AssertionError:
         failures = ["call failed"]
     assert failures, f"pins did not catch mutant {name}"
+
+
+# Planted mistakes in the MXFP8 / NVFP4 weight paths, caught by the MX pins.
+MX_MUTANTS = {
+    "e8m0_bias": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),
+    "mxfp8_block_16": ("* oracle_e8m0_to_f64(S[(k / 32) * N + n]);", "* oracle_e8m0_to_f64(S[(k / 16) * N + n]);"),
+    "e2m1_table": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 4.0, 3.0, 6.0}"),
+    "nvfp4_nibble_order": ("uint8_t code = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
+                           "uint8_t code = (n & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    "nvfp4_drops_global": ("* oracle_e4m3_to_f64(S[(k / 16) * N + n]) * global;", "* oracle_e4m3_to_f64(S[(k / 16) * N + n]);"),
+    "nvfp4_block_32": ("* oracle_e4m3_to_f64(S[(k / 16) * N + n]) * global;", "* oracle_e4m3_to_f64(S[(k / 32) * N + n]) * global;"),
+}
+
+
+def _build_mx(tmp_path, name, src_text):
+    lib = _build(tmp_path, name, src_text)
+    p, i64, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+    lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1_to_f64.restype = d
+    lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0_to_f64.restype = d
+    lib.oracle_dequant_mxfp8.argtypes = [p, p, i64, i64, p]
+    lib.oracle_dequant_nvfp4.argtypes = [p, p, d, i64, i64, p]
+    lib.oracle_swiglu_mx.argtypes = [p, ctypes.c_int, p, p, d, p, p, d, i64, i64, i64, p, i64, p]
+    return lib
+
+
+def test_unmodified_oracle_passes_mx_pins(tmp_path):
+    from test_oracle_mx_pins import mx_pin_failures
+    assert mx_pin_failures(_build_mx(tmp_path, "orig_mx", open(SRC).read())) == []
+
+
+@pytest.mark.parametrize("name", sorted(MX_MUTANTS))
+def test_planted_mx_mistake_is_caught(tmp_path, name):
+    from test_oracle_mx_pins import mx_pin_failures
+    src = open(SRC).read()
+    old, new = MX_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique in the oracle source"
+    lib = _build_mx(tmp_path, name, src.replace(old, new, 1))
+    try:
+        failures = mx_pin_failures(lib)
+    except AssertionError:
+        failures = ["call failed"]
+    assert failures, f"pins did not catch mutant {name}"
