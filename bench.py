@@ -51,6 +51,11 @@ WORKLOADS = {
     # INT4 weights (group 128), BF16 A and Y
     "qwen2.5-0.5b-w4": (896, 4864, (64, 128, 512, 2048), 1),
     "qwen2.5-7b-w4": (3584, 18944, (128, 256, 1024), 2),
+    # MXFP8 / NVFP4 weights (decoded to BF16 in the kernel), BF16 A and Y
+    "qwen2.5-0.5b-mxfp8": (896, 4864, (64, 128, 512), 1),
+    "qwen2.5-7b-mxfp8": (3584, 18944, (128, 256), 2),
+    "qwen2.5-0.5b-nvfp4": (896, 4864, (64, 128, 512), 1),
+    "qwen2.5-7b-nvfp4": (3584, 18944, (128, 256), 2),
     # the SwiGLU MLP block: (H, F, Ms, seed)
     "qwen2.5-0.5b-mlp": (896, 4864, (128, 512, 2048, 8192), 1),
     "qwen2.5-7b-mlp": (3584, 18944, (256, 1024, 4096), 2),
@@ -215,10 +220,12 @@ class Workload:
         self.dev = dev
         self.producer = name.endswith("-fp8-rmsnorm")
         self.kind = ("fp8" if name.endswith("-fp8") or self.producer else
-                     "mlp" if name.endswith("-mlp") else "w4" if name.endswith("-w4") else "bf16")
+                     "mlp" if name.endswith("-mlp") else "w4" if name.endswith("-w4") else
+                     "mx" if name.endswith(("-mxfp8", "-nvfp4")) else "bf16")
+        self.mxfmt = name.rsplit("-", 1)[1] if self.kind == "mx" else None
         self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
-        forms = (("mlp",) if self.kind == "mlp" else ("separate",) if self.kind == "w4"
+        forms = (("mlp",) if self.kind == "mlp" else ("separate",) if self.kind in ("w4", "mx")
                  else ("separate", "interleaved"))
         self.host = {}
         for M in Ms:
@@ -232,6 +239,13 @@ class Workload:
             elif self.kind == "w4":
                 A, (W1q, S1), (W2q, S2) = si.make_w4(M, N, K, seed, W4_GROUP)
                 self.host[M] = (A, W1q, S1, W2q, S2)
+            elif self.kind == "mx":
+                A, w1, w2 = si.make_mx(M, N, K, seed, self.mxfmt)
+                if self.mxfmt == "mxfp8":
+                    self.host[M] = (A, w1[0], w1[1], w2[0], w2[1])
+                else:
+                    f32 = lambda v: torch.tensor([v], dtype=torch.float32)
+                    self.host[M] = (A, w1[0], w1[1], f32(w1[2]), w2[0], w2[1], f32(w2[2]))
             elif self.kind == "mlp":   # K = H (hidden), N = F (intermediate)
                 A, W1, W2 = si.make_bf16(M, N, K, seed)
                 self.host[M] = (A, W1, W2, si.make_bf16(1, K, N, seed + 100)[1])
@@ -266,6 +280,12 @@ class Workload:
         if self.kind == "w4":   # A, two code matrices, two scale matrices, Y
             return (2 * M * self.K + 2 * (self.K * self.N // 2)
                     + 2 * (self.K // W4_GROUP) * self.N * 2 + 2 * M * self.N)
+        if self.kind == "mx":
+            if self.mxfmt == "mxfp8":   # one byte per code, one per 32 codes of a column
+                w = 2 * (self.K * self.N + (self.K // 32) * self.N)
+            else:                       # half a byte per code, one per 16, two tensor scales
+                w = 2 * (self.K * self.N // 2 + (self.K // 16) * self.N) + 8
+            return 2 * M * self.K + w + 2 * M * self.N
         b = self.eb * (M * self.K + 2 * self.K * self.N) + M * self.N * 2
         if self.producer:
             b += self.producer_bytes(M)
@@ -284,7 +304,7 @@ class Workload:
         dev, sg = self.dev, self.sg
         h = self.host[M]
         out = torch.empty(self.out_shape(M), dtype=torch.bfloat16, device=dev)
-        if self.kind == "w4":
+        if self.kind in ("w4", "mx"):
             return tuple(t.to(dev) for t in h) + (out,)
         if self.kind == "mlp":
             ws = torch.empty(int(self.lib.swiglu_mlp_workspace_size(M, self.K, self.N)),
@@ -318,6 +338,12 @@ class Workload:
         if self.kind == "w4":
             return lambda: check("swiglu_fused_w4", lib.swiglu_fused_w4(
                 d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, W4_GROUP, self._stream()))
+        if self.kind == "mx" and self.mxfmt == "mxfp8":
+            return lambda: check("swiglu_fused_mxfp8", lib.swiglu_fused_mxfp8(
+                d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, self._stream()))
+        if self.kind == "mx":
+            return lambda: check("swiglu_fused_nvfp4", lib.swiglu_fused_nvfp4(
+                d[0], d[1], d[2], d[3], d[4], d[5], d[6], d[7], M, N, K, self._stream()))
         if self.kind == "mlp":
             nbytes = bufs[5].numel()
             return lambda: check("swiglu_mlp", lib.swiglu_mlp(d[0], d[1], d[2], d[3], None, d[4],
@@ -368,6 +394,10 @@ class Workload:
         sg = self.sg
         if self.kind == "w4":
             return sg.swiglu_fused_w4(*bufs[:5], bufs[5], group=W4_GROUP)
+        if self.kind == "mx" and self.mxfmt == "mxfp8":
+            return sg.swiglu_fused_mxfp8(*bufs[:5], bufs[5])
+        if self.kind == "mx":
+            return sg.swiglu_fused_nvfp4(*bufs[:7], bufs[7])
         if self.kind == "mlp":
             return sg.swiglu_mlp(bufs[0], bufs[1], bufs[2], bufs[3], None, bufs[4], workspace=bufs[5])
         if self.fp8:
@@ -400,6 +430,8 @@ class Workload:
             return "rmsnorm_quant+2sm_fp8"
         if self.kind == "w4":
             return "w4_sk2"
+        if self.kind == "mx":
+            return f"{self.mxfmt}_sk2"
         return "2sm_fp8" if self.fp8 else self.sg.variant_name(v)
 
     def step(self):
@@ -585,6 +617,9 @@ def run_ours(args, ws, rank, local):
                          f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)} with INT4 "
                          f"weights (group {W4_GROUP}, BF16 scales), BF16 A and Y, seed {wl.seed}"
                          if wl.kind == "w4" else
+                         f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)} with "
+                         f"{wl.mxfmt.upper()} weights, BF16 A and Y, seed {wl.seed}"
+                         if wl.kind == "mx" else
                          f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
                          f"separate and interleaved weights, seed {wl.seed}"),
             "calls_per_step": n_calls,
@@ -728,7 +763,7 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
     the same inputs, per call and as one step; fusion efficiency per call;
     optionally the same function under torch.compile."""
     import torch
-    if wl.fp8 or wl.kind == "w4":
+    if wl.fp8 or wl.kind in ("w4", "mx"):
         return None
     factory = unfused_factory(wl)
     eager_us = measure_calls(wl, stream, args.call_launches, factory)
@@ -799,6 +834,12 @@ def oracle_sample(workload: str, target_s: float):
     fp8 = workload.endswith("-fp8")
     prod = workload.endswith("-fp8-rmsnorm")
     w4 = workload.endswith("-w4")
+    mxf = workload.rsplit("-", 1)[1] if workload.endswith(("-mxfp8", "-nvfp4")) else None
+    if mxf:
+        Amx, m1, m2 = si.make_mx(max(Ms), N, K, seed, mxf)
+        amx = si.bits_u16(Amx)
+        cv = lambda w: tuple(x.numpy() if hasattr(x, "numpy") else x for x in w)
+        mxargs = (mxf, cv(m1), cv(m2))
     if w4:
         A4, (W1q, S1), (W2q, S2) = si.make_w4(max(Ms), N, K, seed, W4_GROUP)
         a4 = si.bits_u16(A4)
@@ -815,7 +856,7 @@ def oracle_sample(workload: str, target_s: float):
         a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
         wf = oracle.pack_interleaved(w1, w2)
         w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
-    forms = ("mlp",) if mlp else ("separate",) if w4 else ("separate", "interleaved")
+    forms = ("mlp",) if mlp else ("separate",) if (w4 or mxf) else ("separate", "interleaved")
     per_row = (6 if mlp else 4) * N * K
 
     def one(rows_per_call):
@@ -824,7 +865,9 @@ def oracle_sample(workload: str, target_s: float):
         for form in forms:
             for M in Ms:
                 rows = np.sort(rng.integers(0, M, size=rows_per_call))
-                if w4:
+                if mxf:
+                    oracle.swiglu_mx(amx[:M], *mxargs, rows=rows)
+                elif w4:
                     oracle.swiglu_w4(a4[:M], *w4args, rows=rows)
                 elif prod:   # RMSNorm and quantisation of all of A (the scale needs every row)
                     sA, aq = oracle.rmsnorm_quant_e4m3(xg[M][0], xg[M][1], RMS_EPS)

@@ -174,6 +174,29 @@ int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *
                     void *stream);
 
 /*
+ * MXFP8 and NVFP4 weights (weight-only; the formats the GEMM page names for
+ * Blackwell, read per the OCP Microscaling specification and NVIDIA's NVFP4):
+ *   MXFP8: C1, C2: E4M3 codes, uint8 [K,N] row-major; S1, S2: E8M0 scales,
+ *          uint8 [K/32, N] (value 2^(e-127)), one per column and 32 K rows.
+ *          W = BF16(E4M3(c) * 2^(e-127)).
+ *   NVFP4: C1, C2: E2M1 codes, uint8 [K, N/2] (two per byte along N, column n
+ *          in the low nibble when even); S1, S2: E4M3 scales, uint8 [K/16, N],
+ *          one per column and 16 K rows; g1, g2: device pointers to one FP32
+ *          scale per tensor.  W = E2M1(c) * E4M3(s) * g.
+ * Y = SiLU(A x W1) (.) (A x W2) with BF16 A [M,K] and Y [M,N].  The codes are
+ * decoded to BF16 in shared memory inside the split-K cluster kernel (E4M3 *
+ * 2^k and E2M1 * E4M3 are exact in BF16) and multiplied on BF16 tensor cores;
+ * the NVFP4 tensor scales multiply the gate and up sums before the
+ * activation.  K a multiple of 64, N of 32; pointers 16-byte aligned (g1, g2:
+ * 4-byte).
+ */
+int swiglu_fused_mxfp8(const void *A, const void *C1, const void *S1, const void *C2,
+                       const void *S2, void *Y, int64_t M, int64_t N, int64_t K, void *stream);
+int swiglu_fused_nvfp4(const void *A, const void *C1, const void *S1, const float *g1,
+                       const void *C2, const void *S2, const float *g2, void *Y, int64_t M,
+                       int64_t N, int64_t K, void *stream);
+
+/*
  * The producer of the FP8 form's A operand: RMSNorm of each row of X followed
  * by per-tensor E4M3 quantisation (FP8 quantisation is what the page's
  * section "Definizione del Problema" names as raising tensor-core density; the

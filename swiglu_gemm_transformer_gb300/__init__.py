@@ -41,6 +41,8 @@ EXPORTS = {
     "swiglu_rmsnorm_quant_fp8": ("pp f pp ll p", ctypes.c_int),
     "swiglu_quant_fp8": ("ppp ll p", ctypes.c_int),
     "swiglu_fused_w4": ("ppppp p lll l p", ctypes.c_int),
+    "swiglu_fused_mxfp8": ("ppppp p lll p", ctypes.c_int),
+    "swiglu_fused_nvfp4": ("pppppppp lll p", ctypes.c_int),
     "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
     "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
     "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
@@ -321,6 +323,55 @@ def swiglu_fused_w4(A, W1q, S1, W2q, S2, Y=None, *, group: int = 128, stream=Non
     rc = lib().swiglu_fused_w4(A.data_ptr(), W1q.data_ptr(), S1.data_ptr(), W2q.data_ptr(),
                                S2.data_ptr(), Y.data_ptr(), M, N, K, int(group), _stream(stream))
     _check("swiglu_fused_w4", rc)
+    return Y
+
+
+def _out(A, N, Y):
+    import torch
+    M = A.shape[0]
+    if Y is None:
+        return torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(Y, "Y", torch.bfloat16)
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [M, N]")
+    return Y
+
+
+def swiglu_fused_mxfp8(A, C1, S1, C2, S2, Y=None, *, stream=None):
+    """Y = SiLU(A @ W1) * (A @ W2), W = E4M3(C) * 2^(S - 127) per 32 K rows:
+    C1/C2 uint8 [K,N], S1/S2 uint8 [K/32,N]."""
+    import torch
+    _need(A, "A", torch.bfloat16)
+    for t, n in ((C1, "C1"), (C2, "C2"), (S1, "S1"), (S2, "S2")):
+        _need(t, n, torch.uint8)
+    M, K = A.shape
+    N = C1.shape[1]
+    if C1.shape != (K, N) or C2.shape != C1.shape or S1.shape != (K // 32, N) or S2.shape != S1.shape:
+        raise ValueError("shape mismatch")
+    Y = _out(A, N, Y)
+    rc = lib().swiglu_fused_mxfp8(A.data_ptr(), C1.data_ptr(), S1.data_ptr(), C2.data_ptr(),
+                                  S2.data_ptr(), Y.data_ptr(), M, N, K, _stream(stream))
+    _check("swiglu_fused_mxfp8", rc)
+    return Y
+
+
+def swiglu_fused_nvfp4(A, C1, S1, g1, C2, S2, g2, Y=None, *, stream=None):
+    """Y = SiLU(A @ W1) * (A @ W2), W = E2M1(C) * E4M3(S) * g per 16 K rows:
+    C1/C2 uint8 [K,N/2] (two codes per byte), S1/S2 uint8 [K/16,N] E4M3,
+    g1/g2 one-element float32 CUDA tensors."""
+    import torch
+    _need(A, "A", torch.bfloat16)
+    for t, n in ((C1, "C1"), (C2, "C2"), (S1, "S1"), (S2, "S2")):
+        _need(t, n, torch.uint8)
+    M, K = A.shape
+    N = 2 * C1.shape[1]
+    if C1.shape[0] != K or C2.shape != C1.shape or S1.shape != (K // 16, N) or S2.shape != S1.shape:
+        raise ValueError("shape mismatch")
+    Y = _out(A, N, Y)
+    rc = lib().swiglu_fused_nvfp4(A.data_ptr(), C1.data_ptr(), S1.data_ptr(), _scale(g1, "g1"),
+                                  C2.data_ptr(), S2.data_ptr(), _scale(g2, "g2"), Y.data_ptr(),
+                                  M, N, K, _stream(stream))
+    _check("swiglu_fused_nvfp4", rc)
     return Y
 
 

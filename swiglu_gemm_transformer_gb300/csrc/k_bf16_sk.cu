@@ -42,6 +42,9 @@ cudaError_t launch_bf16_sk(bool interleaved, const LaunchArgs &la) {
   return interleaved ? launch_sk<SkCfg<true>>(la) : launch_sk<SkCfg<false>>(la);
 }
 
-cudaError_t launch_w4_sk(const LaunchArgs &la) { return launch_sk<SkCfg<false, true>>(la); }
+cudaError_t launch_w4_sk(const LaunchArgs &la) { return launch_sk<SkCfg<false, WF_INT4>>(la); }
+cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la) {
+  return nvfp4 ? launch_sk<SkCfg<false, WF_NVFP4>>(la) : launch_sk<SkCfg<false, WF_MXFP8>>(la);
+}
 
 }  // namespace swiglu

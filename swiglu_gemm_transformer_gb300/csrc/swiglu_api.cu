@@ -268,6 +268,76 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   return launch_w4_sk(la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
+// MXFP8 (nvfp4 = false) or NVFP4 (true) weights: the split-K cluster kernel
+// with the matching decode stage.  g1, g2: NVFP4 per-tensor scales.
+int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const float *g1,
+           const void *C2, const void *S2, const float *g2, void *Y, int64_t M, int64_t N,
+           int64_t K, void *stream) {
+  if (M < 0 || N < 0 || K < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SWIGLU_OK;
+  if (!Y) return SWIGLU_ERR_INVALID_ARG;
+  if (K % 64 != 0) return SWIGLU_ERR_UNSUPPORTED;
+  if (N % 32 != 0) return SWIGLU_ERR_MISALIGNED;
+  if (K > 0 && (!A || !C1 || !C2 || !S1 || !S2 || (nvfp4 && (!g1 || !g2))))
+    return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (K > 0 && (!aligned16(A) || !aligned16(C1) || !aligned16(C2) ||
+                                  !aligned16(S1) || !aligned16(S2))))
+    return SWIGLU_ERR_MISALIGNED;
+  if (nvfp4 && K > 0 &&
+      ((reinterpret_cast<uintptr_t>(g1) & 3u) || (reinterpret_cast<uintptr_t>(g2) & 3u)))
+    return SWIGLU_ERR_MISALIGNED;
+  const int64_t code_pitch = nvfp4 ? N / 2 : N;
+  const int64_t blk = nvfp4 ? 16 : 32;
+  const uint64_t y_bytes = uint64_t(M) * N * 2, a_bytes = uint64_t(M) * K * 2;
+  const uint64_t c_bytes = uint64_t(K) * code_pitch, s_bytes = uint64_t(K / blk) * N;
+  if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, C1, c_bytes) ||
+      overlaps(Y, y_bytes, C2, c_bytes) || overlaps(Y, y_bytes, S1, s_bytes) ||
+      overlaps(Y, y_bytes, S2, s_bytes))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cudaMemsetAsync(Y, 0, y_bytes, s) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof la);
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
+  const uint32_t cbox = nvfp4 ? 32 : 64, srows = nvfp4 ? 4 : 2;
+  rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, C1, code_pitch, K, code_pitch, cbox, 64, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, C2, code_pitch, K, code_pitch, cbox, 64, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, U8, S1, N, K / blk, N, 64, srows, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, U8, S2, N, K / blk, N, 64, srows, NOSW);
+  if (rc == SWIGLU_OK)
+    rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc != SWIGLU_OK) return rc;
+  KParams &p = la.p;
+  p.M = int32_t(M);
+  p.N = int32_t(N);
+  p.K = int32_t(K);
+  p.num_m_blk = int32_t(cdiv(M, 128));
+  p.num_n_blk = int32_t(cdiv(N, 64));
+  p.num_k_blk = int32_t(cdiv(K, 64));
+  p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.err = st->err;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blk;
+  p.w_early = g_weights_read_only.load(std::memory_order_relaxed);
+  p.Y = Y;
+  p.sW1 = g1;
+  p.sW2 = g2;
+  if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
+  la.device = dev;
+  la.stream = s;
+  return launch_mx_sk(nvfp4, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
 // FP8 E4M3 path: CTA-pair kernel, K-major weights, per-tensor scales.
 int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, const float *sW1,
             const float *sW2, void *Y, int64_t M, int64_t N, int64_t K, bool interleaved,
@@ -544,6 +614,17 @@ int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *
                     const void *S2, void *Y, int64_t M, int64_t N, int64_t K, int64_t group,
                     void *stream) {
   return run_w4(A, W1q, S1, W2q, S2, Y, M, N, K, group, stream);
+}
+
+int swiglu_fused_mxfp8(const void *A, const void *C1, const void *S1, const void *C2,
+                       const void *S2, void *Y, int64_t M, int64_t N, int64_t K, void *stream) {
+  return run_mx(false, A, C1, S1, nullptr, C2, S2, nullptr, Y, M, N, K, stream);
+}
+
+int swiglu_fused_nvfp4(const void *A, const void *C1, const void *S1, const float *g1,
+                       const void *C2, const void *S2, const float *g2, void *Y, int64_t M,
+                       int64_t N, int64_t K, void *stream) {
+  return run_mx(true, A, C1, S1, g1, C2, S2, g2, Y, M, N, K, stream);
 }
 
 int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t, int64_t N,

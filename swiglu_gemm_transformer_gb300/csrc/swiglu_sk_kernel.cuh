@@ -39,6 +39,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "sm103_ptx.cuh"
@@ -48,14 +49,23 @@ namespace swiglu {
 
 enum : uint32_t { WAIT_SK_RECV = 7 };
 
-// W4_: the weights arrive as INT4 codes (two per byte along N) with one BF16
-// scale per column and group of K rows; the epilogue warps, idle during the
-// K loop, decode each stage's codes into the BF16 operand layout the MMA
-// reads (see the W4 paragraph above the kernel).
-template <bool INTERLEAVED_, bool W4_ = false>
+// Weight formats of the split-K kernel.  Besides BF16, the weights may arrive
+// as low-precision codes with block scales; the epilogue warps, idle during
+// the K loop, decode each stage into the BF16 operand layout the MMA reads
+// (see the decode functions above the kernel):
+//   WF_INT4  : signed 4-bit codes (two per byte along N), BF16 scale per
+//              column and group of K rows;
+//   WF_MXFP8 : E4M3 codes, E8M0 scale per column and 32 K rows;
+//   WF_NVFP4 : E2M1 codes (two per byte along N), E4M3 scale per column and
+//              16 K rows, and one FP32 scale per tensor (applied to the
+//              gate and up sums before the activation).
+enum : int { WF_BF16 = 0, WF_INT4 = 1, WF_MXFP8 = 2, WF_NVFP4 = 3 };
+
+template <bool INTERLEAVED_, int WF_ = WF_BF16>
 struct SkCfg {
   static constexpr bool INTERLEAVED = INTERLEAVED_;
-  static constexpr bool W4 = W4_;
+  static constexpr int WF = WF_;
+  static constexpr bool DECODE = WF != WF_BF16;
   static constexpr int BM = 128;                 // rows per tile (MMA M)
   static constexpr int BK = 64;                  // K per stage
   static constexpr int BN = 64;                  // output columns per tile
@@ -68,15 +78,19 @@ struct SkCfg {
   static constexpr int B_SBO = 8 * ROW_BYTES;
   static constexpr int B_KSTEP = 16 * ROW_BYTES;
   static constexpr int B_BYTES = NB_ATOMS * ATOM_BYTES;
-  // W4: per weight matrix a [64 K x 32 byte] box of codes and a [1 x 64] box
-  // of scales, behind the A tile and the decoded B tiles of the stage
-  static constexpr int RAW_W_BYTES = BK * (ATOM_COLS / 2);      // 2 KB
-  static constexpr int RAW_S_BYTES = ATOM_COLS * 2;             // 128 B
+  // Decoded formats: per weight matrix a [64 K rows x 64 columns] box of codes
+  // and a [SCALE_ROWS x 64] box of scales, behind the A tile and the decoded
+  // B tiles of the stage.
+  static constexpr int CODE_ROW_BYTES = WF == WF_MXFP8 ? 64 : 32;  // bytes per K row of the box
+  static constexpr int SCALE_ROWS = WF == WF_INT4 ? 1 : WF == WF_MXFP8 ? 2 : 4;  // per 64 K rows
+  static constexpr int SCALE_ELEM = WF == WF_INT4 ? 2 : 1;        // bytes per scale
+  static constexpr int RAW_W_BYTES = BK * CODE_ROW_BYTES;
+  static constexpr int RAW_S_BYTES = SCALE_ROWS * ATOM_COLS * SCALE_ELEM;
   static constexpr int RAW_OFF = A_BYTES + B_BYTES;
-  static constexpr int RAW_BYTES = W4 ? 2 * (RAW_W_BYTES + RAW_S_BYTES) : 0;
-  static constexpr int TMA_BYTES = A_BYTES + (W4 ? RAW_BYTES : B_BYTES);  // bytes TMA lands per stage
+  static constexpr int RAW_BYTES = DECODE ? 2 * (RAW_W_BYTES + RAW_S_BYTES) : 0;
+  static constexpr int TMA_BYTES = A_BYTES + (DECODE ? RAW_BYTES : B_BYTES);  // bytes TMA lands per stage
   static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + RAW_BYTES + 1023) / 1024 * 1024;
-  static constexpr int STAGES = W4 ? 5 : 6;
+  static constexpr int STAGES = !DECODE ? 6 : WF == WF_MXFP8 ? 4 : 5;
   // Receive buffer: the peer's partial gate and up sums of the 32 output
   // columns this CTA keeps, for all 128 rows: value v (v < 32: gate of kept
   // output v; v >= 32: up of kept output v - 32) of row i at
@@ -95,7 +109,7 @@ struct SkCfg {
   static constexpr int TMEM_COLS = 128;
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(!W4 || !INTERLEAVED, "INT4 weights: separate form only");
+  static_assert(!DECODE || !INTERLEAVED, "decoded weight formats: separate form only");
 };
 
 // This warp's 32 rows x 16 outputs starting at tile output `o0`: gate and up
@@ -183,6 +197,86 @@ __device__ __forceinline__ static void w4_decode_stage(uint8_t *stage, int tid) 
   }
 }
 
+// Two E4M3 codes (low byte, high byte of `two`) to two floats, exactly.
+__device__ __forceinline__ static float2 e4m3x2_to_float2(uint32_t two) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(two));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+}
+
+// E2M1 code (1 sign, 2 exponent bits with bias 1, 1 mantissa bit) to float,
+// exactly: 2^(e-1) (1 + m/2) for e > 0, m/2 for e = 0.
+__device__ __forceinline__ static float e2m1_to_float(uint32_t code) {
+  const uint32_t e = (code >> 1) & 3u, m = code & 1u;
+  const uint32_t mag = e ? (((126u + e) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
+  return __uint_as_float(mag | ((code & 8u) << 28));
+}
+
+// MXFP8: weight = BF16(E4M3(c) * 2^(e-127)); the product is exact in FP32
+// (E8M0 e = 0 is 2^-127, a binary32 subnormal) and rounded once.  Same
+// thread mapping as the INT4 decode; codes are one byte per column.
+template <class C>
+__device__ __forceinline__ static void mx8_decode_stage(uint8_t *stage, int tid) {
+  const int t = tid >> 7, j = tid & 7, rr = (tid >> 3) & 15;
+  const uint8_t *raw_w = stage + C::RAW_OFF + t * C::RAW_W_BYTES;
+  const uint8_t *raw_s = stage + C::RAW_OFF + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES;
+  uint8_t *tile = stage + C::A_BYTES + t * C::ATOM_BYTES;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = rr + 16 * i;
+    const uint2 codes = *reinterpret_cast<const uint2 *>(raw_w + k * 64 + j * 8);
+    const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + (k >> 5) * 64 + j * 8);
+    uint32_t out[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t cw = b < 2 ? codes.x : codes.y, sw = b < 2 ? sc.x : sc.y;
+      const int sh = 16 * (b & 1);
+      const float2 f = e4m3x2_to_float2((cw >> sh) & 0xFFFFu);
+      const uint32_t e0 = (sw >> sh) & 0xFFu, e1 = (sw >> (sh + 8)) & 0xFFu;
+      const float p0 = __uint_as_float(e0 ? e0 << 23 : 0x00400000u);
+      const float p1 = __uint_as_float(e1 ? e1 << 23 : 0x00400000u);
+      out[b] = pack_bf16x2(__fmul_rn(f.x, p0), __fmul_rn(f.y, p1));
+    }
+    *reinterpret_cast<uint4 *>(tile + k * 128 + ((j ^ (k & 7)) * 16)) =
+        make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// NVFP4: BF16(E2M1(c) * E4M3(s)), exact (at most 6 significant bits); the
+// per-tensor FP32 scale multiplies the gate and up sums in the epilogue.
+template <class C>
+__device__ __forceinline__ static void nv4_decode_stage(uint8_t *stage, int tid) {
+  const int t = tid >> 7, j = tid & 7, rr = (tid >> 3) & 15;
+  const uint8_t *raw_w = stage + C::RAW_OFF + t * C::RAW_W_BYTES;
+  const uint8_t *raw_s = stage + C::RAW_OFF + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES;
+  uint8_t *tile = stage + C::A_BYTES + t * C::ATOM_BYTES;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = rr + 16 * i;
+    const uint32_t codes = *reinterpret_cast<const uint32_t *>(raw_w + k * 32 + j * 4);
+    const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + (k >> 4) * 64 + j * 8);
+    uint32_t out[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 s2 = e4m3x2_to_float2(((b < 2 ? sc.x : sc.y) >> (16 * (b & 1))) & 0xFFFFu);
+      const float v0 = e2m1_to_float((codes >> (8 * b)) & 0xFu);
+      const float v1 = e2m1_to_float((codes >> (8 * b + 4)) & 0xFu);
+      out[b] = pack_bf16x2(__fmul_rn(v0, s2.x), __fmul_rn(v1, s2.y));
+    }
+    *reinterpret_cast<uint4 *>(tile + k * 128 + ((j ^ (k & 7)) * 16)) =
+        make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+template <class C>
+__device__ __forceinline__ static void decode_stage(uint8_t *stage, int tid) {
+  if (C::WF == WF_INT4) w4_decode_stage<C>(stage, tid);
+  if (C::WF == WF_MXFP8) mx8_decode_stage<C>(stage, tid);
+  if (C::WF == WF_NVFP4) nv4_decode_stage<C>(stage, tid);
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     swiglu_bf16_sk_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -239,7 +333,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB0);
     if (!C::INTERLEAVED) ptx::prefetch_tmap(&tmB1);
-    if (C::W4) {
+    if (C::DECODE) {
       ptx::prefetch_tmap(&tmS1);
       ptx::prefetch_tmap(&tmS2);
     }
@@ -254,11 +348,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   ptx::grid_launch_dependents();
   auto load_w = [&](uint32_t sb, uint32_t fb, int kb) {
-    if (C::W4) {  // codes and scales of both weight matrices, behind the BF16 tiles
+    if (C::DECODE) {  // codes and scales of both weight matrices, behind the BF16 tiles
       const uint32_t r = sb - C::A_BYTES + C::RAW_OFF;
-      const int g = kb * C::BK / p.w4_group;
-      ptx::tma_load_2d(r, &tmB0, fb, nb * (C::BN / 2), kb * C::BK);
-      ptx::tma_load_2d(r + C::RAW_W_BYTES, &tmB1, fb, nb * (C::BN / 2), kb * C::BK);
+      const int g = C::WF == WF_INT4 ? kb * C::BK / p.w4_group : kb * C::SCALE_ROWS;
+      ptx::tma_load_2d(r, &tmB0, fb, nb * C::CODE_ROW_BYTES, kb * C::BK);
+      ptx::tma_load_2d(r + C::RAW_W_BYTES, &tmB1, fb, nb * C::CODE_ROW_BYTES, kb * C::BK);
       ptx::tma_load_2d(r + 2 * C::RAW_W_BYTES, &tmS1, fb, nb * C::BN, g);
       ptx::tma_load_2d(r + 2 * C::RAW_W_BYTES + C::RAW_S_BYTES, &tmS2, fb, nb * C::BN, g);
     } else if (C::INTERLEAVED) {
@@ -321,7 +415,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_bar(C::W4 ? dec_bar(stage) : full_bar(stage), phase, p.timeout_ns, abort_flag,
+        if (!wait_bar(C::DECODE ? dec_bar(stage) : full_bar(stage), phase, p.timeout_ns, abort_flag,
                       p.err, WAIT_MMA_FULL)) {
           ok = false;
           break;
@@ -357,13 +451,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int h = warp >> 2;
     const int row = q * 32 + lane;  // tile row of this thread
     bool ok = true;
-    if (C::W4) {  // during the K loop: decode each stage's weights for the MMA
+    if (C::DECODE) {  // during the K loop: decode each stage's weights for the MMA
       uint32_t stage = 0, phase = 0;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         ok = wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        w4_decode_stage<C>(smem + stage * C::STAGE_BYTES, static_cast<int>(threadIdx.x));
+        decode_stage<C>(smem + stage * C::STAGE_BYTES, static_cast<int>(threadIdx.x));
         ptx::fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(dec_bar(stage));
@@ -424,6 +518,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const float4 pu = recv[(8 + 4 * h + k) * C::BM + row];
           g[4 * k] += pg.x; g[4 * k + 1] += pg.y; g[4 * k + 2] += pg.z; g[4 * k + 3] += pg.w;
           u[4 * k] += pu.x; u[4 * k + 1] += pu.y; u[4 * k + 2] += pu.z; u[4 * k + 3] += pu.w;
+        }
+        if (C::WF == WF_NVFP4) {  // the per-tensor scales of the gate and up weights
+          const float gs = *p.sW1, us = *p.sW2;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            g[i] *= gs;
+            u[i] *= us;
+          }
         }
         uint32_t packed[8];
 #pragma unroll

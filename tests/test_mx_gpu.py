@@ -1,0 +1,77 @@
+"""GPU parity of the MXFP8 and NVFP4 weight paths against the oracle.
+
+The kernel decodes the codes to BF16 exactly (E4M3 * 2^k and E2M1 * E4M3 are
+representable in BF16 for these inputs) and applies the NVFP4 tensor scale to
+the FP32 sums, so the acceptance rule is the BF16 one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def sg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import swiglu_gemm_transformer_gb300 as m
+    m.lib()
+    return m
+
+
+def _run(sg, fmt, M, N, K, seed, rows=None):
+    A, w1, w2 = si.make_mx(M, N, K, seed, fmt)
+    Ad = A.to(DEV)
+    if fmt == "mxfp8":
+        Y = sg.swiglu_fused_mxfp8(Ad, w1[0].to(DEV), w1[1].to(DEV), w2[0].to(DEV), w2[1].to(DEV))
+        o1, o2 = (w1[0].numpy(), w1[1].numpy()), (w2[0].numpy(), w2[1].numpy())
+    else:
+        g1 = torch.tensor([w1[2]], dtype=torch.float32, device=DEV)
+        g2 = torch.tensor([w2[2]], dtype=torch.float32, device=DEV)
+        Y = sg.swiglu_fused_nvfp4(Ad, w1[0].to(DEV), w1[1].to(DEV), g1, w2[0].to(DEV), w2[1].to(DEV), g2)
+        # the kernel reads the scales as binary32; the oracle takes the same values
+        o1 = (w1[0].numpy(), w1[1].numpy(), float(np.float32(w1[2])))
+        o2 = (w2[0].numpy(), w2[1].numpy(), float(np.float32(w2[2])))
+    rc, detail = sg.swiglu_device_status()
+    assert rc == sg.OK, (sg.status_string(rc), detail)
+    ref = oracle.swiglu_mx(si.bits_u16(A), fmt, o1, o2, rows=rows)
+    got = Y.double().cpu().numpy()
+    if rows is not None:
+        got = got[rows]
+    oracle.assert_parity(got, ref, f"{fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("shape", [(1, 64, 64), (7, 96, 128), (63, 288, 384), (128, 4864, 896),
+                                   (200, 160, 512), (65, 4864, 896)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_mx_shapes(sg, fmt, shape):
+    M, N, K = shape
+    _run(sg, fmt, M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_mx_7b_shape_sampled(sg, fmt):
+    M, N, K = 256, 18944, 3584
+    _run(sg, fmt, M, N, K, seed=2, rows=si.sample_rows(M, 128, 32, seed=2))
+
+
+def test_mx_argument_errors(sg):
+    lib = sg.lib()
+    A = torch.zeros(4, 128, dtype=torch.bfloat16, device=DEV)
+    C = torch.zeros(128, 64, dtype=torch.uint8, device=DEV)
+    S = torch.zeros(8, 64, dtype=torch.uint8, device=DEV)
+    g = torch.ones(1, device=DEV)
+    Y = torch.empty(4, 64, dtype=torch.bfloat16, device=DEV)
+    pm = [A.data_ptr(), C.data_ptr(), S.data_ptr(), C.data_ptr(), S.data_ptr(), Y.data_ptr()]
+    assert lib.swiglu_fused_mxfp8(*pm, 4, 64, 96, None) == sg.ERR_UNSUPPORTED      # K not a multiple of 64
+    assert lib.swiglu_fused_mxfp8(*pm, 4, 48, 128, None) == sg.ERR_MISALIGNED      # N not a multiple of 32
+    pn = [A.data_ptr(), C.data_ptr(), S.data_ptr(), None, C.data_ptr(), S.data_ptr(), g.data_ptr(), Y.data_ptr()]
+    assert lib.swiglu_fused_nvfp4(*pn, 4, 64, 128, None) == sg.ERR_INVALID_ARG     # missing tensor scale
+    torch.cuda.synchronize()
