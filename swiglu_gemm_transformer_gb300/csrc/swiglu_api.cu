@@ -124,8 +124,10 @@ int choose_variant(int64_t M, int64_t N, int64_t K, bool /*interleaved*/, int sm
   // streams per K step (32 KB instead of 48 KB).
   if (M > 128) return SWIGLU_VARIANT_2SM_N128;
   // Small M (one 128-row block): narrow the tiles until they occupy every SM
-  // (the page's Kernel-2 argument: more thread blocks for small batches).
-  if (cdiv(N, 128) >= sm_count) return SWIGLU_VARIANT_1SM_N128;
+  // (the page's Kernel-2 argument: more thread blocks for small batches); a
+  // 128-column tile per SM is worth a few idle SMs (7B, M = 128: 148 tiles,
+  // 43.6 us against 46.4 us for 296 tiles of 64 columns).
+  if (10 * cdiv(N, 128) >= 9 * sm_count) return SWIGLU_VARIANT_1SM_N128;
   if (cdiv(N, 64) >= sm_count) return SWIGLU_VARIANT_1SM_N64;
   return SWIGLU_VARIANT_1SM_N32;
 }
@@ -239,11 +241,15 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
+  // Few output columns: 64-column tiles split along K over CTA pairs; many:
+  // 128-column tiles, one CTA each (A read once for twice the weights).
+  const bool wide = 2 * cdiv(N, 64) > st->sm_count;
+  const uint32_t cols = wide ? 128 : 64;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1q, N / 2, K, N / 2, 32, 64, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2q, N / 2, K, N / 2, 32, 64, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, BF16, S1, N, K / G, N * 2, 64, 1, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, BF16, S2, N, K / G, N * 2, 64, 1, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1q, N / 2, K, N / 2, cols / 2, 64, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2q, N / 2, K, N / 2, cols / 2, 64, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, BF16, S1, N, K / G, N * 2, cols, 1, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, BF16, S2, N, K / G, N * 2, cols, 1, NOSW);
   if (rc == SWIGLU_OK)
     rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc != SWIGLU_OK) return rc;
@@ -252,20 +258,21 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   p.N = int32_t(N);
   p.K = int32_t(K);
   p.num_m_blk = int32_t(cdiv(M, 128));
-  p.num_n_blk = int32_t(cdiv(N, 64));
+  p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
   p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blk;
-  p.w_early = g_weights_read_only.load(std::memory_order_relaxed);
+  p.w_early = wide ? 0 : g_weights_read_only.load(std::memory_order_relaxed);
   p.Y = Y;
   p.w4_group = int32_t(G);
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
   la.stream = s;
-  return launch_w4_sk(la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  const cudaError_t e = wide ? launch_dq_kernel(1, la) : launch_w4_sk(la);
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
 // MXFP8 (nvfp4 = false) or NVFP4 (true) weights: the split-K cluster kernel
@@ -307,12 +314,14 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
-  const uint32_t cbox = nvfp4 ? 32 : 64, srows = nvfp4 ? 4 : 2;
+  const bool wide = 2 * cdiv(N, 64) > st->sm_count;  // as for INT4
+  const uint32_t cols = wide ? 128 : 64;
+  const uint32_t cbox = nvfp4 ? cols / 2 : cols, srows = nvfp4 ? 4 : 2;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, C1, code_pitch, K, code_pitch, cbox, 64, NOSW);
   if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, C2, code_pitch, K, code_pitch, cbox, 64, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, U8, S1, N, K / blk, N, 64, srows, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, U8, S2, N, K / blk, N, 64, srows, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, U8, S1, N, K / blk, N, cols, srows, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, U8, S2, N, K / blk, N, cols, srows, NOSW);
   if (rc == SWIGLU_OK)
     rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc != SWIGLU_OK) return rc;
@@ -321,21 +330,22 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   p.N = int32_t(N);
   p.K = int32_t(K);
   p.num_m_blk = int32_t(cdiv(M, 128));
-  p.num_n_blk = int32_t(cdiv(N, 64));
+  p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
   p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blk;
-  p.w_early = g_weights_read_only.load(std::memory_order_relaxed);
+  p.w_early = wide ? 0 : g_weights_read_only.load(std::memory_order_relaxed);
   p.Y = Y;
   p.sW1 = g1;
   p.sW2 = g2;
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
   la.stream = s;
-  return launch_mx_sk(nvfp4, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  const cudaError_t e = wide ? launch_dq_kernel(nvfp4 ? 3 : 2, la) : launch_mx_sk(nvfp4, la);
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
 // FP8 E4M3 path: CTA-pair kernel, K-major weights, per-tensor scales.

@@ -44,6 +44,7 @@
 
 #include "sm103_ptx.cuh"
 #include "tc_common.cuh"
+#include "weight_decode.cuh"
 
 namespace swiglu {
 
@@ -59,8 +60,6 @@ enum : uint32_t { WAIT_SK_RECV = 7 };
 //   WF_NVFP4 : E2M1 codes (two per byte along N), E4M3 scale per column and
 //              16 K rows, and one FP32 scale per tensor (applied to the
 //              gate and up sums before the activation).
-enum : int { WF_BF16 = 0, WF_INT4 = 1, WF_MXFP8 = 2, WF_NVFP4 = 3 };
-
 template <bool INTERLEAVED_, int WF_ = WF_BF16>
 struct SkCfg {
   static constexpr bool INTERLEAVED = INTERLEAVED_;
@@ -81,9 +80,9 @@ struct SkCfg {
   // Decoded formats: per weight matrix a [64 K rows x 64 columns] box of codes
   // and a [SCALE_ROWS x 64] box of scales, behind the A tile and the decoded
   // B tiles of the stage.
-  static constexpr int CODE_ROW_BYTES = WF == WF_MXFP8 ? 64 : 32;  // bytes per K row of the box
-  static constexpr int SCALE_ROWS = WF == WF_INT4 ? 1 : WF == WF_MXFP8 ? 2 : 4;  // per 64 K rows
-  static constexpr int SCALE_ELEM = WF == WF_INT4 ? 2 : 1;        // bytes per scale
+  static constexpr int CODE_ROW_BYTES = ATOM_COLS * WFormat<WF>::CODE_BITS / 8;  // per K row
+  static constexpr int SCALE_ROWS = WFormat<WF>::SCALE_ROWS;     // per 64 K rows
+  static constexpr int SCALE_ELEM = WFormat<WF>::SCALE_BYTES;    // bytes per scale
   static constexpr int RAW_W_BYTES = BK * CODE_ROW_BYTES;
   static constexpr int RAW_S_BYTES = SCALE_ROWS * ATOM_COLS * SCALE_ELEM;
   static constexpr int RAW_OFF = A_BYTES + B_BYTES;
@@ -110,6 +109,7 @@ struct SkCfg {
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!DECODE || !INTERLEAVED, "decoded weight formats: separate form only");
+  static_assert(!DECODE || EPI_WARPS == 8, "the decode stage uses the 256 epilogue threads");
 };
 
 // This warp's 32 rows x 16 outputs starting at tile output `o0`: gate and up
@@ -147,134 +147,16 @@ __device__ __forceinline__ static void sk_load16(uint32_t tacc, bool have_acc, i
   }
 }
 
-// INT4 weights: decode one stage's codes and scales into the two BF16 weight
-// tiles the MMA reads, [64 K rows x 64 columns] each in the layout a TMA copy
-// with the 128-byte swizzle would leave (row k at 128 k bytes, its 16-byte
-// chunk j -- columns 8j .. 8j+7 -- at position j ^ (k % 8)).
-//
-// Weight = BF16(q * s), in packed BF16 pairs: flipping each code's sign bit
-// gives the offset-binary n = q + 8, and the BF16 pattern 0x4300 | n is the
-// number 128 + n exactly; subtracting 136 leaves q exactly; one BF16 multiply
-// by the scale pair then rounds q * s once, to nearest even.  Byte b of a
-// 4-byte group of codes holds columns 8j + 2b (low nibble) and 8j + 2b + 1
-// (high nibble), and the scales of those two columns are adjacent in memory,
-// so each 32-bit word of the scale vector is the pair a product needs.
-//
-// Thread `tid` of the 256 epilogue threads owns one column chunk j of one
-// weight matrix t and rows rr, rr + 16, rr + 32, rr + 48: it loads its eight
-// scales once per stage, and a warp's code loads and tile stores each cover
-// 512 contiguous bytes.
-template <class C>
-__device__ __forceinline__ static void w4_decode_stage(uint8_t *stage, int tid) {
-  static_assert(C::EPI_WARPS == 8 && C::BK == 64, "decode mapping: 256 threads, 64 rows");
-  const int t = tid >> 7;          // 0: gate weights, 1: up weights
-  const int j = tid & 7;           // columns 8j .. 8j + 7
-  const int rr = (tid >> 3) & 15;  // rows rr + 16 i
-  const uint8_t *raw_w = stage + C::RAW_OFF + t * C::RAW_W_BYTES;
-  const uint4 sv = *reinterpret_cast<const uint4 *>(stage + C::RAW_OFF + 2 * C::RAW_W_BYTES +
-                                                    t * C::RAW_S_BYTES + j * 16);
-  const __nv_bfloat162 sc[4] = {*reinterpret_cast<const __nv_bfloat162 *>(&sv.x),
-                                *reinterpret_cast<const __nv_bfloat162 *>(&sv.y),
-                                *reinterpret_cast<const __nv_bfloat162 *>(&sv.z),
-                                *reinterpret_cast<const __nv_bfloat162 *>(&sv.w)};
-  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
-  uint8_t *tile = stage + C::A_BYTES + t * C::ATOM_BYTES;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = rr + 16 * i;
-    const uint32_t codes = *reinterpret_cast<const uint32_t *>(raw_w + k * 32 + j * 4) ^ 0x88888888u;
-    uint32_t out[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t w = ((codes >> (8 * b)) & 0xFu) | (((codes >> (8 * b + 4)) & 0xFu) << 16) |
-                         0x43004300u;
-      const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&w), k136);
-      const __nv_bfloat162 v = __hmul2(q, sc[b]);
-      out[b] = *reinterpret_cast<const uint32_t *>(&v);
-    }
-    *reinterpret_cast<uint4 *>(tile + k * 128 + ((j ^ (k & 7)) * 16)) =
-        make_uint4(out[0], out[1], out[2], out[3]);
-  }
-}
-
-// Two E4M3 codes (low byte, high byte of `two`) to two floats, exactly.
-__device__ __forceinline__ static float2 e4m3x2_to_float2(uint32_t two) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(h2)
-      : "r"(two));
-  return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-}
-
-// E2M1 code (1 sign, 2 exponent bits with bias 1, 1 mantissa bit) to float,
-// exactly: 2^(e-1) (1 + m/2) for e > 0, m/2 for e = 0.
-__device__ __forceinline__ static float e2m1_to_float(uint32_t code) {
-  const uint32_t e = (code >> 1) & 3u, m = code & 1u;
-  const uint32_t mag = e ? (((126u + e) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
-  return __uint_as_float(mag | ((code & 8u) << 28));
-}
-
-// MXFP8: weight = BF16(E4M3(c) * 2^(e-127)); the product is exact in FP32
-// (E8M0 e = 0 is 2^-127, a binary32 subnormal) and rounded once.  Same
-// thread mapping as the INT4 decode; codes are one byte per column.
-template <class C>
-__device__ __forceinline__ static void mx8_decode_stage(uint8_t *stage, int tid) {
-  const int t = tid >> 7, j = tid & 7, rr = (tid >> 3) & 15;
-  const uint8_t *raw_w = stage + C::RAW_OFF + t * C::RAW_W_BYTES;
-  const uint8_t *raw_s = stage + C::RAW_OFF + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES;
-  uint8_t *tile = stage + C::A_BYTES + t * C::ATOM_BYTES;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = rr + 16 * i;
-    const uint2 codes = *reinterpret_cast<const uint2 *>(raw_w + k * 64 + j * 8);
-    const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + (k >> 5) * 64 + j * 8);
-    uint32_t out[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t cw = b < 2 ? codes.x : codes.y, sw = b < 2 ? sc.x : sc.y;
-      const int sh = 16 * (b & 1);
-      const float2 f = e4m3x2_to_float2((cw >> sh) & 0xFFFFu);
-      const uint32_t e0 = (sw >> sh) & 0xFFu, e1 = (sw >> (sh + 8)) & 0xFFu;
-      const float p0 = __uint_as_float(e0 ? e0 << 23 : 0x00400000u);
-      const float p1 = __uint_as_float(e1 ? e1 << 23 : 0x00400000u);
-      out[b] = pack_bf16x2(__fmul_rn(f.x, p0), __fmul_rn(f.y, p1));
-    }
-    *reinterpret_cast<uint4 *>(tile + k * 128 + ((j ^ (k & 7)) * 16)) =
-        make_uint4(out[0], out[1], out[2], out[3]);
-  }
-}
-
-// NVFP4: BF16(E2M1(c) * E4M3(s)), exact (at most 6 significant bits); the
-// per-tensor FP32 scale multiplies the gate and up sums in the epilogue.
-template <class C>
-__device__ __forceinline__ static void nv4_decode_stage(uint8_t *stage, int tid) {
-  const int t = tid >> 7, j = tid & 7, rr = (tid >> 3) & 15;
-  const uint8_t *raw_w = stage + C::RAW_OFF + t * C::RAW_W_BYTES;
-  const uint8_t *raw_s = stage + C::RAW_OFF + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES;
-  uint8_t *tile = stage + C::A_BYTES + t * C::ATOM_BYTES;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = rr + 16 * i;
-    const uint32_t codes = *reinterpret_cast<const uint32_t *>(raw_w + k * 32 + j * 4);
-    const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + (k >> 4) * 64 + j * 8);
-    uint32_t out[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float2 s2 = e4m3x2_to_float2(((b < 2 ? sc.x : sc.y) >> (16 * (b & 1))) & 0xFFFFu);
-      const float v0 = e2m1_to_float((codes >> (8 * b)) & 0xFu);
-      const float v1 = e2m1_to_float((codes >> (8 * b + 4)) & 0xFu);
-      out[b] = pack_bf16x2(__fmul_rn(v0, s2.x), __fmul_rn(v1, s2.y));
-    }
-    *reinterpret_cast<uint4 *>(tile + k * 128 + ((j ^ (k & 7)) * 16)) =
-        make_uint4(out[0], out[1], out[2], out[3]);
-  }
-}
-
+// Decode one stage's codes of both weight matrices (gate, then up) into the
+// two BF16 atoms the MMA reads; threads 0-127 take the gate matrix, 128-255
+// the up matrix.
 template <class C>
 __device__ __forceinline__ static void decode_stage(uint8_t *stage, int tid) {
-  if (C::WF == WF_INT4) w4_decode_stage<C>(stage, tid);
-  if (C::WF == WF_MXFP8) mx8_decode_stage<C>(stage, tid);
-  if (C::WF == WF_NVFP4) nv4_decode_stage<C>(stage, tid);
+  const int t = tid >> 7;
+  decode_weights<C::WF, 64, 128, C::ATOM_BYTES>(
+      stage + C::RAW_OFF + t * C::RAW_W_BYTES,
+      stage + C::RAW_OFF + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES,
+      stage + C::A_BYTES + t * C::ATOM_BYTES, tid & 127);
 }
 
 template <class C>

@@ -53,8 +53,8 @@ def test_host_side_variant_choice(lib):
     assert lib.swiglu_select_variant(128, 4864, 896, 1) == sg.VARIANT_1SM_N64_SK2
     # M = 256: 2 x 76 one-CTA tiles of 64 columns are one wave
     assert lib.swiglu_select_variant(256, 4864, 896, 0) == sg.VARIANT_1SM_N64
-    # 7B shape, M = 128: 296 column blocks of 64 already fill the GPU
-    assert lib.swiglu_select_variant(128, 18944, 3584, 0) == sg.VARIANT_1SM_N64
+    # 7B shape, M = 128: 148 column blocks of 128 nearly fill 152 SMs
+    assert lib.swiglu_select_variant(128, 18944, 3584, 0) == sg.VARIANT_1SM_N128
     assert lib.swiglu_select_variant(8192, 4864, 896, 0) == sg.VARIANT_2SM_N128
 
 

@@ -49,7 +49,9 @@ def _run(sg, fmt, M, N, K, seed, rows=None):
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("shape", [(1, 64, 64), (7, 96, 128), (63, 288, 384), (128, 4864, 896),
-                                   (200, 160, 512), (65, 4864, 896)],
+                                   (200, 160, 512), (65, 4864, 896),
+                                   # wide weight matrices: the 128-column one-CTA kernel
+                                   (37, 9760, 256), (130, 9856, 192)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_mx_shapes(sg, fmt, shape):
     M, N, K = shape

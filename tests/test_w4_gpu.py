@@ -41,7 +41,10 @@ def _run(sg, M, N, K, G, seed, rows=None):
 
 @pytest.mark.parametrize("shape", [(1, 64, 128, 128), (7, 96, 256, 64), (63, 288, 384, 128),
                                    (128, 4864, 896, 128), (200, 160, 512, 128), (384, 320, 640, 64),
-                                   (65, 4864, 896, 128)],
+                                   (65, 4864, 896, 128),
+                                   # wide weight matrices: the 128-column one-CTA kernel, with
+                                   # a ragged last tile (9760 = 76 x 128 + 32) and ragged M
+                                   (37, 9760, 256, 128), (130, 9856, 192, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_w4_shapes(sg, shape):
     M, N, K, G = shape
