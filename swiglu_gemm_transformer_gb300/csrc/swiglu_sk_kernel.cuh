@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t packed[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          packed[i] = pack_bf16x2(silu_mul_1sfu(g[2 * i], u[2 * i]),
-                                  silu_mul_1sfu(g[2 * i + 1], u[2 * i + 1]));
+          packed[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]),
+                                  silu_mul(g[2 * i + 1], u[2 * i + 1]));
         // 32 bytes of this row of Y; N is a multiple of 8, so each 16-byte
         // half is wholly inside or wholly outside the matrix
         const int yrow = mb * C::BM + row;

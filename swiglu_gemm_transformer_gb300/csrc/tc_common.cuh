@@ -101,20 +101,15 @@ __device__ __forceinline__ static void tile_coords(int t, const KParams &p, int 
   nb = r / rows;
 }
 
-// SiLU(g) * u = g * u / (1 + e^-g), FP32.
+// SiLU(g) * u = g * u / (1 + e^-g), FP32, with one special-function-unit
+// operation per element (the unit's throughput is what bounds an epilogue
+// that is not hidden behind MMAs): e^-g = 2^(-g log2 e) by ex2.approx, then
+// the reciprocal of d = 1 + e^-g (d >= 1, capped at 1e30 so that it stays
+// finite) on the FMA pipe: the classic bit-level first guess (subtracting the
+// float's bits from a constant, which roughly negates the exponent; relative
+// error below 6 %) refined by three Newton-Raphson steps r <- r (2 - d r),
+// each of which squares the relative error (< 1e-7 after three).
 __device__ __forceinline__ static float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
-// The same with one special-function-unit operation instead of two, for
-// epilogues that are not hidden behind MMAs (few rows): e^-g = 2^(-g log2 e)
-// by ex2.approx, then the reciprocal of d = 1 + e^-g (d >= 1, capped at 1e30
-// so that it stays finite) on the FMA pipe: the classic bit-level first guess
-// (subtracting the float's bits from a constant, which roughly negates the
-// exponent; relative error below 6 %) refined by three Newton-Raphson steps
-// r <- r (2 - d r), each of which squares the relative error (< 1e-7 after
-// three).
-__device__ __forceinline__ static float silu_mul_1sfu(float g, float u) {
   float e;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
   const float d = 1.0f + fminf(e, 1e30f);
