@@ -11,14 +11,16 @@
 // the point: every CTA reads its 128 rows of A once for 128 output columns
 // (256 gate and up columns), so A's bytes per weight byte are half those of a
 // 64-column tile -- with 4-bit weights A is otherwise the larger stream.
-//   * warp 8 (one thread) streams each K step's A box and the two matrices'
-//     code and scale boxes into a STAGES-deep ring (TMA);
-//   * warps 0-7 decode each stage's codes into one of three BF16 operand
-//     buffers ([64 K x 256] in the 128-byte-swizzled layout), then release the
-//     stage's codes (the stage is free once the MMA has also read its A);
+//   * warp 8 (one thread) streams each K step's A box into a short ring and
+//     warp 10 (one thread) the two matrices' code and scale boxes into a deep
+//     one (TMA): the weight stream is small per step, so many steps of it are
+//     in flight;
+//   * warps 0-7 decode each step's codes into one of two BF16 operand
+//     buffers ([64 K x 256] in the 128-byte-swizzled layout) and release the
+//     codes slot;
 //   * warp 9 (one thread) issues tcgen05.mma M=128 x N=256 x K=16, gate and
 //     up columns side by side in TMEM (columns [0,128) gate, [128,256) up),
-//     and frees the decoded buffer and the A stage through tcgen05.commit;
+//     and frees the decoded buffer and the A slot through tcgen05.commit;
 //   * after the last K step warps 0-7 run the usual epilogue (TMEM loads,
 //     SiLU(g) * u in FP32, BF16, TMA stores through staging buffers that
 //     reuse the decoded buffers), applying NVFP4's per-tensor scales.
@@ -47,23 +49,29 @@ struct DqCfg {
   static constexpr int CODE_ROW_BYTES = BN * WFormat<WF>::CODE_BITS / 8;
   static constexpr int RAW_W_BYTES = BK * CODE_ROW_BYTES;
   static constexpr int RAW_S_BYTES = WFormat<WF>::SCALE_ROWS * BN * WFormat<WF>::SCALE_BYTES;
-  static constexpr int TMA_BYTES = A_BYTES + 2 * (RAW_W_BYTES + RAW_S_BYTES);
-  static constexpr int STAGE_BYTES = (TMA_BYTES + 1023) / 1024 * 1024;
-  // Three decoded buffers let the decoders run a stage ahead of the MMA, so
-  // the barrier round trips between them overlap work instead of adding to it.
-  static constexpr int DEC_BUFS = 3;
-  static constexpr int STAGES = WF == WF_MXFP8 ? 3 : 4;
-  static constexpr int DEC_OFF = STAGES * STAGE_BYTES;
+  static constexpr int RAW_BYTES = 2 * (RAW_W_BYTES + RAW_S_BYTES);  // codes + scales of one K step
+  // Two rings: A (from L2, short latency) and the codes (from DRAM, small):
+  // the codes ring is as deep as about 104 KB allows, so many K steps of the
+  // weight stream are in flight while A and the decode keep pace.
+  static constexpr int A_STAGES = 3;
+  static constexpr int C_STAGES_RAW = (104 * 1024) / RAW_BYTES;
+  static constexpr int C_STAGES = C_STAGES_RAW > 16 ? 16 : C_STAGES_RAW;
+  static constexpr int DEC_BUFS = 2;
+  static constexpr int C_OFF = A_STAGES * A_BYTES;
+  static constexpr int DEC_OFF = (C_OFF + C_STAGES * RAW_BYTES + 1023) / 1024 * 1024;
   static constexpr int BAR_OFF = DEC_OFF + DEC_BUFS * DEC_BYTES;
-  // full[S], empty[S], dfull[D], dempty[D], acc_full, drain, spare
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * DEC_BUFS + 3;
+  // a_full[A], a_empty[A], c_full[C], c_empty[C], dfull[D], dempty[D], acc_full, drain, spare
+  static constexpr int NUM_BARS = 2 * A_STAGES + 2 * C_STAGES + 2 * DEC_BUFS + 3;
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
-  static constexpr int EPI_WARPS = 8, PRODUCER_WARP = 8, MMA_WARP = 9, THREADS = 320;
+  static constexpr int EPI_WARPS = 8, PRODUCER_WARP = 8, MMA_WARP = 9, CODES_WARP = 10;
+  static constexpr int THREADS = 32 * 11;
   static constexpr int TMEM_COLS = 256;
   static constexpr int B_SBO = 8 * 128, B_KSTEP = 16 * 128;
   static constexpr int STG_BYTES = 32 * 64;  // a warp's 32 x 32 BF16 staging block
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(RAW_BYTES % 128 == 0, "codes stages stay 128-byte aligned");
+  static_assert(C_STAGES >= 4, "codes ring depth");
   static_assert(EPI_WARPS * 2 * STG_BYTES <= DEC_BUFS * DEC_BYTES, "staging reuses the decoded buffers");
   static_assert(WF != WF_BF16, "a decoded weight format");
 };
@@ -83,11 +91,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t *smem = smem_raw + (base - raw);
 
   const uint32_t bars = base + C::BAR_OFF;
-  auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto empty_bar = [&](int s) { return bars + 8u * (C::STAGES + s); };
-  auto dfull_bar = [&](int d) { return bars + 8u * (2 * C::STAGES + d); };
-  auto dempty_bar = [&](int d) { return bars + 8u * (2 * C::STAGES + C::DEC_BUFS + d); };
-  const uint32_t accf_bar = bars + 8u * (2 * C::STAGES + 2 * C::DEC_BUFS);
+  auto a_full = [&](int s) { return bars + 8u * s; };
+  auto a_empty = [&](int s) { return bars + 8u * (C::A_STAGES + s); };
+  auto c_full = [&](int s) { return bars + 8u * (2 * C::A_STAGES + s); };
+  auto c_empty = [&](int s) { return bars + 8u * (2 * C::A_STAGES + C::C_STAGES + s); };
+  auto dfull_bar = [&](int d) { return bars + 8u * (2 * C::A_STAGES + 2 * C::C_STAGES + d); };
+  auto dempty_bar = [&](int d) {
+    return bars + 8u * (2 * C::A_STAGES + 2 * C::C_STAGES + C::DEC_BUFS + d);
+  };
+  const uint32_t accf_bar = bars + 8u * (2 * C::A_STAGES + 2 * C::C_STAGES + 2 * C::DEC_BUFS);
   const uint32_t drain_bar = accf_bar + 8u;
   const uint32_t spare_bar = accf_bar + 16u;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
@@ -105,9 +117,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto kstep = [&](int i) { return i + k_rot < nk ? i + k_rot : i + k_rot - nk; };
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1 + C::EPI_WARPS);  // the MMA's A and the decoders' codes
+    for (int s = 0; s < C::A_STAGES; ++s) {
+      ptx::mbar_init(a_full(s), 1);
+      ptx::mbar_init(a_empty(s), 1);            // the MMA's commit
+    }
+    for (int s = 0; s < C::C_STAGES; ++s) {
+      ptx::mbar_init(c_full(s), 1);
+      ptx::mbar_init(c_empty(s), C::EPI_WARPS);  // every decoding warp
     }
     for (int d = 0; d < C::DEC_BUFS; ++d) {
       ptx::mbar_init(dfull_bar(d), C::EPI_WARPS);
@@ -136,56 +152,64 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
 
+  // One ring's producer: waits for a free slot, then `load(slot, barrier, k)`.
+  auto produce = [&](int stages, auto full, auto empty, uint32_t bytes, auto load) {
+    uint32_t slot = 0, phase = 0, issued = 0;
+    bool ok = true;
+    for (int i = 0; i < nk; ++i) {
+      if (!wait_bar(empty(slot), phase ^ 1u, p.timeout_ns, abort_flag, p.err, WAIT_PRODUCER_EMPTY)) {
+        ok = false;
+        break;
+      }
+      ptx::mbar_arrive_expect_tx(full(slot), bytes);
+      load(static_cast<int>(slot), full(slot), kstep(i));
+      ++issued;
+      if (++slot == static_cast<uint32_t>(stages)) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {  // let the copies in flight land before shared memory is released
+      const uint32_t n = issued < (uint32_t)stages ? issued : (uint32_t)stages;
+      for (uint32_t i = issued - n; i < issued; ++i)
+        wait_quiet(full(i % stages), (i / stages) & 1u, p.timeout_ns);
+    }
+  };
+
   if (warp == C::PRODUCER_WARP) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, issued = 0;
-      bool ok = true;
-      for (int i = 0; i < nk; ++i) {
-        const int kb = kstep(i);
-        if (!wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
-                      WAIT_PRODUCER_EMPTY)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sa = base + stage * C::STAGE_BYTES;
-        const uint32_t r = sa + C::A_BYTES;
-        const uint32_t fb = full_bar(stage);
+    // ------------------------------------------------------------ A producer
+    if (lane == 0)
+      produce(C::A_STAGES, a_full, a_empty, C::A_BYTES, [&](int s, uint32_t fb, int kb) {
+        ptx::tma_load_2d(base + s * C::A_BYTES, &tmA, fb, kb * C::BK, mb * C::BM);
+      });
+    __syncwarp();
+  } else if (warp == C::CODES_WARP) {
+    // ------------------------------------------------------------ codes producer
+    if (lane == 0)
+      produce(C::C_STAGES, c_full, c_empty, C::RAW_BYTES, [&](int s, uint32_t fb, int kb) {
+        const uint32_t r = base + C::C_OFF + s * C::RAW_BYTES;
         const int g = C::WF == WF_INT4 ? kb * C::BK / p.w4_group : kb * WFormat<C::WF>::SCALE_ROWS;
-        ptx::mbar_arrive_expect_tx(fb, C::TMA_BYTES);
-        ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
         ptx::tma_load_2d(r, &tmC1, fb, nb * C::CODE_ROW_BYTES, kb * C::BK);
         ptx::tma_load_2d(r + C::RAW_W_BYTES, &tmC2, fb, nb * C::CODE_ROW_BYTES, kb * C::BK);
         ptx::tma_load_2d(r + 2 * C::RAW_W_BYTES, &tmS1, fb, nb * C::BN, g);
         ptx::tma_load_2d(r + 2 * C::RAW_W_BYTES + C::RAW_S_BYTES, &tmS2, fb, nb * C::BN, g);
-        ++issued;
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) {
-        const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
-        for (uint32_t i = issued - n; i < issued; ++i)
-          wait_quiet(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
-      }
-    }
+      });
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
+      uint32_t a = 0, aphase = 0;
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb) {  // kb: position in the (rotated) K loop
         const int d = kb % C::DEC_BUFS;
         const uint32_t dphase = static_cast<uint32_t>(kb / C::DEC_BUFS) & 1u;
-        if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL) ||
+        if (!wait_bar(a_full(a), aphase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL) ||
             !wait_bar(dfull_bar(d), dphase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t sa = base + stage * C::STAGE_BYTES;
+        const uint32_t sa = base + a * C::A_BYTES;
         const uint32_t sb = base + C::DEC_OFF + d * C::DEC_BYTES;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
@@ -194,11 +218,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               ptx::smem_desc(sb + kk * C::B_KSTEP, C::ATOM_BYTES, C::B_SBO, ptx::SW_128B);
           ptx::mma_f16(tmem_base, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
         }
-        ptx::mma_commit(empty_bar(stage));  // this stage's A has been read
+        ptx::mma_commit(a_empty(a));        // this A stage has been read
         ptx::mma_commit(dempty_bar(d));     // and the decoded buffer
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
+        if (++a == static_cast<uint32_t>(C::A_STAGES)) {
+          a = 0;
+          aphase ^= 1u;
         }
       }
       if (ok) ptx::mma_commit(accf_bar);
@@ -209,15 +233,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   } else {
     // ------------------------------------------------------------ decode, then epilogue (warps 0-7)
     bool ok = true;
-    uint32_t stage = 0, phase = 0;
+    uint32_t c = 0, cphase = 0;
     for (int kb = 0; kb < nk && ok; ++kb) {
       const int d = kb % C::DEC_BUFS;
       const uint32_t dphase = static_cast<uint32_t>(kb / C::DEC_BUFS) & 1u;
-      ok = wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL) &&
+      ok = wait_bar(c_full(c), cphase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL) &&
            wait_bar(dempty_bar(d), dphase ^ 1u, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      uint8_t *st = smem + stage * C::STAGE_BYTES + C::A_BYTES;
+      const uint8_t *st = smem + C::C_OFF + c * C::RAW_BYTES;
       const int t = static_cast<int>(threadIdx.x) >> 7;  // 0: gate, 1: up
       decode_weights<C::WF, C::BN, 128, C::ATOM_BYTES>(
           st + t * C::RAW_W_BYTES, st + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES,
@@ -226,11 +250,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(dfull_bar(d));
-        ptx::mbar_arrive(empty_bar(stage));  // this stage's codes have been read
+        ptx::mbar_arrive(c_empty(c));  // this stage's codes have been read
       }
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1u;
+      if (++c == static_cast<uint32_t>(C::C_STAGES)) {
+        c = 0;
+        cphase ^= 1u;
       }
     }
     ok = ok && wait_bar(accf_bar, 0, p.timeout_ns, abort_flag, p.err, WAIT_EPI_ACC_FULL);
