@@ -66,6 +66,9 @@ struct DqCfg {
   static constexpr int EPI_WARPS = 8, PRODUCER_WARP = 8, MMA_WARP = 9, CODES_WARP = 10;
   static constexpr int THREADS = 32 * 11;
   static constexpr int TMEM_COLS = 256;
+  // INT4 codes decode as column pairs (c, c + 4): fewer integer operations;
+  // the accumulator columns then carry that order, undone by the epilogue
+  static constexpr bool PAIRED = WF == WF_INT4;
   static constexpr int B_SBO = 8 * 128, B_KSTEP = 16 * 128;
   static constexpr int STG_BYTES = 32 * 64;  // a warp's 32 x 32 BF16 staging block
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok) break;
       const uint8_t *st = smem + C::C_OFF + c * C::RAW_BYTES;
       const int t = static_cast<int>(threadIdx.x) >> 7;  // 0: gate, 1: up
-      decode_weights<C::WF, C::BN, 128, C::ATOM_BYTES>(
+      decode_weights<C::WF, C::BN, 128, C::ATOM_BYTES, C::PAIRED>(
           st + t * C::RAW_W_BYTES, st + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES,
           smem + C::DEC_OFF + d * C::DEC_BYTES + t * 2 * C::ATOM_BYTES, threadIdx.x & 127);
       ptx::fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t it = 0;
       const float gs = C::WF == WF_NVFP4 ? *p.sW1 : 1.0f;
       const float us = C::WF == WF_NVFP4 ? *p.sW2 : 1.0f;
-      epilogue_tile<false, C::BN, C::WF == WF_NVFP4>(tacc, mb * C::BM + q * 32, nb * C::BN, 2 * h,
+      epilogue_tile<false, C::BN, C::WF == WF_NVFP4, C::PAIRED>(tacc, mb * C::BM + q * 32, nb * C::BN, 2 * h,
                                                      2 * h + 2, &tmY, p.M, p.N, smem, base,
                                                      stg_base, it, lane, spare_bar, gs, us);
       if (lane == 0) ptx::bulk_wait_read<0>();

@@ -65,6 +65,9 @@ struct SkCfg {
   static constexpr bool INTERLEAVED = INTERLEAVED_;
   static constexpr int WF = WF_;
   static constexpr bool DECODE = WF != WF_BF16;
+  // INT4 codes decode as column pairs (c, c + 4); within every 8 accumulator
+  // columns the outputs then lie in the order 0 4 1 5 2 6 3 7
+  static constexpr bool PAIRED = WF == WF_INT4 && !INTERLEAVED_;
   static constexpr int BM = 128;                 // rows per tile (MMA M)
   static constexpr int BK = 64;                  // K per stage
   static constexpr int BN = 64;                  // output columns per tile
@@ -153,7 +156,7 @@ __device__ __forceinline__ static void sk_load16(uint32_t tacc, bool have_acc, i
 template <class C>
 __device__ __forceinline__ static void decode_stage(uint8_t *stage, int tid) {
   const int t = tid >> 7;
-  decode_weights<C::WF, 64, 128, C::ATOM_BYTES>(
+  decode_weights<C::WF, 64, 128, C::ATOM_BYTES, C::PAIRED>(
       stage + C::RAW_OFF + t * C::RAW_W_BYTES,
       stage + C::RAW_OFF + 2 * C::RAW_W_BYTES + t * C::RAW_S_BYTES,
       stage + C::A_BYTES + t * C::ATOM_BYTES, tid & 127);
@@ -409,11 +412,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             u[i] *= us;
           }
         }
+        // register holding output column o of these 16
+        auto at = [](int o) { return C::PAIRED ? (o & ~7) | ((o & 7) < 4 ? 2 * (o & 7) : 2 * (o & 7) - 7) : o; };
         uint32_t packed[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          packed[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]),
-                                  silu_mul(g[2 * i + 1], u[2 * i + 1]));
+          packed[i] = pack_bf16x2(silu_mul(g[at(2 * i)], u[at(2 * i)]),
+                                  silu_mul(g[at(2 * i + 1)], u[at(2 * i + 1)]));
         // 32 bytes of this row of Y; N is a multiple of 8, so each 16-byte
         // half is wholly inside or wholly outside the matrix
         const int yrow = mb * C::BM + row;

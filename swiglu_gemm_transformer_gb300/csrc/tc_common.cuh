@@ -136,7 +136,11 @@ __device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
 //   release   : cluster address of the barrier to arrive on once the warp has
 //               read the whole accumulator (frees the TMEM buffer for the MMA).
 //   gs, us    : scales applied to the gate and up accumulators (SCALED only).
-template <bool INTERLEAVED, int BN, bool SCALED = false>
+//   PAIRED    : separate form only; within every 8 accumulator columns the
+//               output columns lie in the order 0 4 1 5 2 6 3 7 (the order
+//               the paired 4-bit weight decode writes), undone here by the
+//               choice of registers.
+template <bool INTERLEAVED, int BN, bool SCALED = false, bool PAIRED = false>
 __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, int col0,
                                                      int c_begin, int c_end,
                                                      const CUtensorMap *tmY, int M, int N,
@@ -193,11 +197,13 @@ __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, in
                         silu_mul(__uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
       }
     } else {
+      // register holding output column o of the chunk
+      auto at = [](int o) { return PAIRED ? (o & ~7) | ((o & 7) < 4 ? 2 * (o & 7) : 2 * (o & 7) - 7) : o; };
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        packed[i] =
-            pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                        silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+        packed[i] = pack_bf16x2(
+            silu_mul(__uint_as_float(g[at(2 * i)]), __uint_as_float(u[at(2 * i)])),
+            silu_mul(__uint_as_float(g[at(2 * i + 1)]), __uint_as_float(u[at(2 * i + 1)])));
     }
     const int ccol = col0 + c * 32;
     const uint32_t stg = stg_base + (it & 1u) * 2048u;

@@ -18,6 +18,11 @@
 //              E2M1 * E4M3, exact in BF16 (the per-tensor FP32 scale is applied
 //              to the accumulated sums by the kernel).
 //
+// PAIRED (INT4 only): the eight columns of a chunk are written in the order
+// 0 4 1 5 2 6 3 7, so that each BF16 pair (c, c + 4) comes out of one shift
+// and one logic operation on the code word; the MMA's output columns then
+// carry the same order, which the epilogue undoes.
+//
 // Thread `tid` of NTHREADS owns one 8-column chunk j of every row it visits
 // (rows rr, rr + R, rr + 2R, ... with R = NTHREADS / (COLS / 8)): it loads its
 // chunk's scales once per 64-row stage (once per scale row for MXFP8/NVFP4),
@@ -63,18 +68,57 @@ __device__ __forceinline__ static uint32_t bf16x2_bits(float lo, float hi) {
 
 // raw_w: the [64 x COLS] codes (COLS * CODE_BITS / 8 bytes per row);
 // raw_s: the stage's scale rows (COLS scales each); tile: the first atom.
-template <int WF, int COLS, int NTHREADS, int ATOM_BYTES>
+// All of a thread's code words (and scales) are loaded before any is decoded,
+// so the shared-memory loads overlap and the decode chains of different rows
+// are independent.
+template <int WF, int COLS, int NTHREADS, int ATOM_BYTES, bool PAIRED = false>
 __device__ __forceinline__ static void decode_weights(const uint8_t *raw_w, const uint8_t *raw_s,
                                                       uint8_t *tile, int tid) {
   constexpr int CHUNKS = COLS / 8;            // 8-column chunks per row
   constexpr int R = NTHREADS / CHUNKS;        // rows per pass
+  constexpr int ROWS = 64 / R;                // rows per thread
   constexpr int ROW_BYTES = COLS * WFormat<WF>::CODE_BITS / 8;
+  constexpr int SR = WFormat<WF>::SCALE_ROWS;  // scale rows per 64 rows
   static_assert(NTHREADS % CHUNKS == 0 && 64 % R == 0, "thread mapping");
+  static_assert(R <= 64 / SR, "a pass stays within one scale row");
   const int j = tid % CHUNKS;
   const int rr = tid / CHUNKS;
   uint8_t *atom = tile + (j / 8) * ATOM_BYTES;
   const int c = j % 8;
-  if (WF == WF_INT4) {
+  // row rr + i R lies in scale row i R SR / 64 (rr < R <= 64 / SR)
+  auto store = [&](int i, uint32_t o0, uint32_t o1, uint32_t o2, uint32_t o3) {
+    const int k = rr + i * R;
+    *reinterpret_cast<uint4 *>(atom + k * 128 + ((c ^ (k & 7)) * 16)) = make_uint4(o0, o1, o2, o3);
+  };
+  if (WF == WF_INT4 && PAIRED) {
+    // nibble c of a code word is column c; (word >> 4b) & 0x000F000F holds
+    // columns b and b + 4 in the two halves.  With the sign bits flipped
+    // (n = q + 8) and 0x4300 or-ed in, each half is the BF16 value 128 + n;
+    // minus 136 is q; one BF16 multiply by the scale pair rounds q * s once.
+    const uint4 sv = *reinterpret_cast<const uint4 *>(raw_s + j * 16);
+    uint32_t sp[4];  // scale pairs (b, b + 4)
+    sp[0] = __byte_perm(sv.x, sv.z, 0x5410);
+    sp[1] = __byte_perm(sv.x, sv.z, 0x7632);
+    sp[2] = __byte_perm(sv.y, sv.w, 0x5410);
+    sp[3] = __byte_perm(sv.y, sv.w, 0x7632);
+    const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
+    uint32_t cw[ROWS];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i)
+      cw[i] = *reinterpret_cast<const uint32_t *>(raw_w + (rr + i * R) * ROW_BYTES + j * 4);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      uint32_t out[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t w = ((cw[i] >> (4 * b)) & 0x000F000Fu) ^ 0x43084308u;
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&w), k136);
+        const __nv_bfloat162 v = __hmul2(q, *reinterpret_cast<const __nv_bfloat162 *>(&sp[b]));
+        out[b] = *reinterpret_cast<const uint32_t *>(&v);
+      }
+      store(i, out[0], out[1], out[2], out[3]);
+    }
+  } else if (WF == WF_INT4) {
     // flipping each code's sign bit gives n = q + 8; the BF16 pattern
     // 0x4300 | n is exactly 128 + n; minus 136 is q; one BF16 multiply by the
     // adjacent scale pair rounds q * s once
@@ -84,57 +128,73 @@ __device__ __forceinline__ static void decode_weights(const uint8_t *raw_w, cons
                                   *reinterpret_cast<const __nv_bfloat162 *>(&sv.z),
                                   *reinterpret_cast<const __nv_bfloat162 *>(&sv.w)};
     const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
+    uint32_t cw[ROWS];
 #pragma unroll
-    for (int k = rr; k < 64; k += R) {
-      const uint32_t codes =
-          *reinterpret_cast<const uint32_t *>(raw_w + k * ROW_BYTES + j * 4) ^ 0x88888888u;
+    for (int i = 0; i < ROWS; ++i)
+      cw[i] = *reinterpret_cast<const uint32_t *>(raw_w + (rr + i * R) * ROW_BYTES + j * 4);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const uint32_t lo = (cw[i] ^ 0x88888888u) & 0x0F0F0F0Fu;         // even columns
+      const uint32_t hi = ((cw[i] ^ 0x88888888u) >> 4) & 0x0F0F0F0Fu;  // odd columns
       uint32_t out[4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint32_t w = ((codes >> (8 * b)) & 0xFu) | (((codes >> (8 * b + 4)) & 0xFu) << 16) |
-                           0x43004300u;
+        // byte b of lo to bits 0-7, byte b of hi to bits 16-23
+        const uint32_t w = (__byte_perm(lo, hi, b | ((4 + b) << 8)) & 0x00FF00FFu) | 0x43004300u;
         const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&w), k136);
         const __nv_bfloat162 v = __hmul2(q, sc[b]);
         out[b] = *reinterpret_cast<const uint32_t *>(&v);
       }
-      *reinterpret_cast<uint4 *>(atom + k * 128 + ((c ^ (k & 7)) * 16)) =
-          make_uint4(out[0], out[1], out[2], out[3]);
+      store(i, out[0], out[1], out[2], out[3]);
     }
   } else if (WF == WF_MXFP8) {
+    // 2^(e-127) from the exponent bits; e = 0 is 2^-127, a binary32 subnormal
+    float p[SR][8];
 #pragma unroll
-    for (int k = rr; k < 64; k += R) {
-      const uint2 codes = *reinterpret_cast<const uint2 *>(raw_w + k * ROW_BYTES + j * 8);
-      const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + (k >> 5) * COLS + j * 8);
+    for (int s = 0; s < SR; ++s) {
+      const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + s * COLS + j * 8);
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const uint32_t e = ((b < 4 ? sc.x : sc.y) >> (8 * (b & 3))) & 0xFFu;
+        p[s][b] = __uint_as_float(e ? e << 23 : 0x00400000u);
+      }
+    }
+    uint2 cw[ROWS];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i)
+      cw[i] = *reinterpret_cast<const uint2 *>(raw_w + (rr + i * R) * ROW_BYTES + j * 8);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int s = i * R * SR / 64;
       uint32_t out[4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint32_t cw = b < 2 ? codes.x : codes.y, sw = b < 2 ? sc.x : sc.y;
-        const int sh = 16 * (b & 1);
-        const float2 f = e4m3x2_to_float2((cw >> sh) & 0xFFFFu);
-        const uint32_t e0 = (sw >> sh) & 0xFFu, e1 = (sw >> (sh + 8)) & 0xFFu;
-        // 2^(e-127) from its exponent bits; e = 0 is 2^-127, a binary32 subnormal
-        const float p0 = __uint_as_float(e0 ? e0 << 23 : 0x00400000u);
-        const float p1 = __uint_as_float(e1 ? e1 << 23 : 0x00400000u);
-        out[b] = bf16x2_bits(__fmul_rn(f.x, p0), __fmul_rn(f.y, p1));
+        const float2 f = e4m3x2_to_float2(((b < 2 ? cw[i].x : cw[i].y) >> (16 * (b & 1))) & 0xFFFFu);
+        out[b] = bf16x2_bits(__fmul_rn(f.x, p[s][2 * b]), __fmul_rn(f.y, p[s][2 * b + 1]));
       }
-      *reinterpret_cast<uint4 *>(atom + k * 128 + ((c ^ (k & 7)) * 16)) =
-          make_uint4(out[0], out[1], out[2], out[3]);
+      store(i, out[0], out[1], out[2], out[3]);
     }
   } else if (WF == WF_NVFP4) {
+    uint2 sv[SR];
 #pragma unroll
-    for (int k = rr; k < 64; k += R) {
-      const uint32_t codes = *reinterpret_cast<const uint32_t *>(raw_w + k * ROW_BYTES + j * 4);
-      const uint2 sc = *reinterpret_cast<const uint2 *>(raw_s + (k >> 4) * COLS + j * 8);
+    for (int s = 0; s < SR; ++s)
+      sv[s] = *reinterpret_cast<const uint2 *>(raw_s + s * COLS + j * 8);
+    uint32_t cw[ROWS];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i)
+      cw[i] = *reinterpret_cast<const uint32_t *>(raw_w + (rr + i * R) * ROW_BYTES + j * 4);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int s = i * R * SR / 64;
       uint32_t out[4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const float2 s2 = e4m3x2_to_float2(((b < 2 ? sc.x : sc.y) >> (16 * (b & 1))) & 0xFFFFu);
-        const float v0 = e2m1_to_float((codes >> (8 * b)) & 0xFu);
-        const float v1 = e2m1_to_float((codes >> (8 * b + 4)) & 0xFu);
+        const float2 s2 = e4m3x2_to_float2(((b < 2 ? sv[s].x : sv[s].y) >> (16 * (b & 1))) & 0xFFFFu);
+        const float v0 = e2m1_to_float((cw[i] >> (8 * b)) & 0xFu);
+        const float v1 = e2m1_to_float((cw[i] >> (8 * b + 4)) & 0xFu);
         out[b] = bf16x2_bits(__fmul_rn(v0, s2.x), __fmul_rn(v1, s2.y));
       }
-      *reinterpret_cast<uint4 *>(atom + k * 128 + ((c ^ (k & 7)) * 16)) =
-          make_uint4(out[0], out[1], out[2], out[3]);
+      store(i, out[0], out[1], out[2], out[3]);
     }
   }
 }
