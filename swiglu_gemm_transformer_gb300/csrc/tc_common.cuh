@@ -101,23 +101,14 @@ __device__ __forceinline__ static void tile_coords(int t, const KParams &p, int 
   nb = r / rows;
 }
 
-// SiLU(g) * u = g * u / (1 + e^-g), FP32, with one special-function-unit
-// operation per element (the unit's throughput is what bounds an epilogue
-// that is not hidden behind MMAs): e^-g = 2^(-g log2 e) by ex2.approx, then
-// the reciprocal of d = 1 + e^-g (d >= 1, capped at 1e30 so that it stays
-// finite) on the FMA pipe: the classic bit-level first guess (subtracting the
-// float's bits from a constant, which roughly negates the exponent; relative
-// error below 6 %) refined by three Newton-Raphson steps r <- r (2 - d r),
-// each of which squares the relative error (< 1e-7 after three).
+// SiLU(g) * u = g * u / (1 + e^-g), FP32: two special-function-unit
+// operations (ex2 and the approximate reciprocal inside the fast divide).  A
+// variant with one SFU operation and a Newton-Raphson reciprocal on the FMA
+// pipe measured 6 % slower on the large-M pair kernel (its extra FMA work
+// competes with the epilogue's other arithmetic under the power cap) and no
+// faster on the split-K kernel, so this form is used everywhere.
 __device__ __forceinline__ static float silu_mul(float g, float u) {
-  float e;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
-  const float d = 1.0f + fminf(e, 1e30f);
-  float r = __uint_as_float(0x7EF311C3u - __float_as_uint(d));
-  r = r * fmaf(-d, r, 2.0f);
-  r = r * fmaf(-d, r, 2.0f);
-  r = r * fmaf(-d, r, 2.0f);
-  return g * r * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 __device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
