@@ -66,9 +66,10 @@ struct DqCfg {
   static constexpr int EPI_WARPS = 8, PRODUCER_WARP = 8, MMA_WARP = 9, CODES_WARP = 10;
   static constexpr int THREADS = 32 * 11;
   static constexpr int TMEM_COLS = 256;
-  // INT4 codes decode as column pairs (c, c + 4): fewer integer operations;
-  // the accumulator columns then carry that order, undone by the epilogue
-  static constexpr bool PAIRED = WF == WF_INT4;
+  // 4-bit codes (INT4, NVFP4) decode as column pairs (c, c + 4): fewer
+  // operations; the accumulator columns then carry that order, undone by the
+  // epilogue
+  static constexpr bool PAIRED = WF == WF_INT4 || WF == WF_NVFP4;
   static constexpr int B_SBO = 8 * 128, B_KSTEP = 16 * 128;
   static constexpr int STG_BYTES = 32 * 64;  // a warp's 32 x 32 BF16 staging block
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);

@@ -65,9 +65,9 @@ struct SkCfg {
   static constexpr bool INTERLEAVED = INTERLEAVED_;
   static constexpr int WF = WF_;
   static constexpr bool DECODE = WF != WF_BF16;
-  // INT4 codes decode as column pairs (c, c + 4); within every 8 accumulator
-  // columns the outputs then lie in the order 0 4 1 5 2 6 3 7
-  static constexpr bool PAIRED = WF == WF_INT4 && !INTERLEAVED_;
+  // 4-bit codes (INT4, NVFP4) decode as column pairs (c, c + 4); within every
+  // 8 accumulator columns the outputs then lie in the order 0 4 1 5 2 6 3 7
+  static constexpr bool PAIRED = (WF == WF_INT4 || WF == WF_NVFP4) && !INTERLEAVED_;
   static constexpr int BM = 128;                 // rows per tile (MMA M)
   static constexpr int BK = 64;                  // K per stage
   static constexpr int BN = 64;                  // output columns per tile

@@ -18,10 +18,10 @@
 //              E2M1 * E4M3, exact in BF16 (the per-tensor FP32 scale is applied
 //              to the accumulated sums by the kernel).
 //
-// PAIRED (INT4 only): the eight columns of a chunk are written in the order
-// 0 4 1 5 2 6 3 7, so that each BF16 pair (c, c + 4) comes out of one shift
-// and one logic operation on the code word; the MMA's output columns then
-// carry the same order, which the epilogue undoes.
+// PAIRED (4-bit codes: INT4, NVFP4): the eight columns of a chunk are written
+// in the order 0 4 1 5 2 6 3 7, so that each BF16 pair (c, c + 4) comes out of
+// shifts and logic operations on the whole code word; the MMA's output columns
+// then carry the same order, which the epilogue undoes.
 //
 // Thread `tid` of NTHREADS owns one 8-column chunk j of every row it visits
 // (rows rr, rr + R, rr + 2R, ... with R = NTHREADS / (COLS / 8)): it loads its
@@ -115,6 +115,47 @@ __device__ __forceinline__ static void decode_weights(const uint8_t *raw_w, cons
         const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&w), k136);
         const __nv_bfloat162 v = __hmul2(q, *reinterpret_cast<const __nv_bfloat162 *>(&sp[b]));
         out[b] = *reinterpret_cast<const uint32_t *>(&v);
+      }
+      store(i, out[0], out[1], out[2], out[3]);
+    }
+  } else if (WF == WF_NVFP4 && PAIRED) {
+    // An E2M1 code s e1 e0 m with its three magnitude bits placed at BF16 bits
+    // 8..6 (the exponent field's two low bits and the mantissa's top bit) and
+    // its sign at bit 15 is the BF16 number E2M1 * 2^-126 (e = 0, m = 1 is the
+    // subnormal 2^-127); a multiply by 2^126 and one by the E4M3 scale are
+    // both exact (at most 2 + 4 significant bits, far inside BF16's range).
+    // Columns b and b + 4 of a code word sit 16 bits apart, so one pair of
+    // shifts and two logic operations build both halves.
+    uint32_t sp[SR][4];  // scale pairs (b, b + 4) per scale row, BF16
+#pragma unroll
+    for (int s = 0; s < SR; ++s) {
+      const uint2 sv = *reinterpret_cast<const uint2 *>(raw_s + s * COLS + j * 8);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 f = e4m3x2_to_float2(__byte_perm(sv.x, sv.y, b | ((4 + b) << 4)) & 0xFFFFu);
+        sp[s][b] = bf16x2_bits(f.x, f.y);
+      }
+    }
+    const uint32_t k126 = 0x7E807E80u;  // 2^126 in both halves
+    uint32_t cw[ROWS];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i)
+      cw[i] = *reinterpret_cast<const uint32_t *>(raw_w + (rr + i * R) * ROW_BYTES + j * 4);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int s = i * R * SR / 64;
+      const uint32_t x = cw[i];
+      uint32_t out[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        // magnitude bits of nibbles b, b + 4 to bits 8..6 and 24..22; sign bits to 15 and 31
+        const uint32_t mag = (b == 0 ? x << 6 : b == 1 ? x << 2 : b == 2 ? x >> 2 : x >> 6) & 0x01C001C0u;
+        const uint32_t sgn = (b == 0 ? x << 12 : b == 1 ? x << 8 : b == 2 ? x << 4 : x) & 0x80008000u;
+        const uint32_t y = mag | sgn;
+        const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&y),
+                                         *reinterpret_cast<const __nv_bfloat162 *>(&k126));
+        const __nv_bfloat162 w = __hmul2(v, *reinterpret_cast<const __nv_bfloat162 *>(&sp[s][b]));
+        out[b] = *reinterpret_cast<const uint32_t *>(&w);
       }
       store(i, out[0], out[1], out[2], out[3]);
     }
