@@ -34,7 +34,15 @@ cudaError_t launch_dq(const LaunchArgs &la) {
 
 }  // namespace
 
-cudaError_t launch_dq_kernel(int wf, const LaunchArgs &la) {
+cudaError_t launch_dq_kernel(int wf, int m_blocks, const LaunchArgs &la) {
+  if (m_blocks == 2) {
+    switch (wf) {
+      case WF_INT4: return launch_dq<DqCfg<WF_INT4, 2>>(la);
+      case WF_MXFP8: return launch_dq<DqCfg<WF_MXFP8, 2>>(la);
+      case WF_NVFP4: return launch_dq<DqCfg<WF_NVFP4, 2>>(la);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (wf) {
     case WF_INT4: return launch_dq<DqCfg<WF_INT4>>(la);
     case WF_MXFP8: return launch_dq<DqCfg<WF_MXFP8>>(la);

@@ -37,8 +37,9 @@ cudaError_t launch_bf16_interleaved(int variant, const LaunchArgs &la);
 cudaError_t launch_bf16_sk(bool interleaved, const LaunchArgs &la);
 cudaError_t launch_w4_sk(const LaunchArgs &la);
 cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la);
-// wf: 1 INT4, 2 MXFP8, 3 NVFP4 (weight_decode.cuh)
-cudaError_t launch_dq_kernel(int wf, const LaunchArgs &la);
+// wf: 1 INT4, 2 MXFP8, 3 NVFP4 (weight_decode.cuh); m_blocks: 128-row blocks
+// per CTA (1, or 2 with la.p.num_m_blk counting 256-row blocks)
+cudaError_t launch_dq_kernel(int wf, int m_blocks, const LaunchArgs &la);
 int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns);
 cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf, int64_t n_elems,
                                         int sm_count, cudaStream_t s);

@@ -257,7 +257,10 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   p.M = int32_t(M);
   p.N = int32_t(N);
   p.K = int32_t(K);
-  p.num_m_blk = int32_t(cdiv(M, 128));
+  // wide kernel with M > 128: each CTA takes two 128-row blocks of A, so one
+  // decode of a weight step serves 256 rows
+  const int m_blocks = wide && M > 128 ? 2 : 1;
+  p.num_m_blk = int32_t(cdiv(M, 128 * m_blocks));
   p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
   p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
@@ -271,7 +274,7 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
   la.stream = s;
-  const cudaError_t e = wide ? launch_dq_kernel(1, la) : launch_w4_sk(la);
+  const cudaError_t e = wide ? launch_dq_kernel(1, m_blocks, la) : launch_w4_sk(la);
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
@@ -329,7 +332,10 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   p.M = int32_t(M);
   p.N = int32_t(N);
   p.K = int32_t(K);
-  p.num_m_blk = int32_t(cdiv(M, 128));
+  // wide kernel with M > 128: each CTA takes two 128-row blocks of A, so one
+  // decode of a weight step serves 256 rows
+  const int m_blocks = wide && M > 128 ? 2 : 1;
+  p.num_m_blk = int32_t(cdiv(M, 128 * m_blocks));
   p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
   p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
@@ -344,7 +350,7 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
   la.stream = s;
-  const cudaError_t e = wide ? launch_dq_kernel(nvfp4 ? 3 : 2, la) : launch_mx_sk(nvfp4, la);
+  const cudaError_t e = wide ? launch_dq_kernel(nvfp4 ? 3 : 2, m_blocks, la) : launch_mx_sk(nvfp4, la);
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 

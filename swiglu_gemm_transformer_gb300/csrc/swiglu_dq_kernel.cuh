@@ -7,7 +7,8 @@
 // form (section "Metodologia", item 1), with W1, W2 given as codes and block
 // scales (weight_decode.cuh).
 //
-// One CTA computes one 128 x 128 output tile over all of K.  Wide tiles are
+// One CTA computes one 128 x 128 output tile over all of K (or, for M > 128,
+// two 128-row blocks of the same columns: 256 x 128).  Wide tiles are
 // the point: every CTA reads its 128 rows of A once for 128 output columns
 // (256 gate and up columns), so A's bytes per weight byte are half those of a
 // 64-column tile -- with 4-bit weights A is otherwise the larger stream.
@@ -37,24 +38,31 @@
 
 namespace swiglu {
 
-template <int WF_>
+// MB_: 128-row blocks of A per CTA (1 or 2).  With two, one decode of each
+// weight step feeds the MMAs of both blocks (two accumulators, all 512 TMEM
+// columns): the decode, the weight stream and the per-step protocol are shared
+// by 256 rows.
+template <int WF_, int MB_ = 1>
 struct DqCfg {
   static constexpr int WF = WF_;
+  static constexpr int MB = MB_;
   static constexpr int BM = 128, BK = 64, BN = 128;
   static constexpr int MMA_N = 2 * BN;               // gate + up
   static constexpr int ATOM_COLS = 64;
   static constexpr int ATOM_BYTES = BK * ATOM_COLS * 2;  // 8 KB
-  static constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+  static constexpr int A_BOX_BYTES = BM * BK * 2;      // one block's A box, 16 KB
+  static constexpr int A_BYTES = MB * A_BOX_BYTES;       // one A stage
   static constexpr int DEC_BYTES = 4 * ATOM_BYTES;     // one decoded buffer: W1 then W2, 32 KB
   static constexpr int CODE_ROW_BYTES = BN * WFormat<WF>::CODE_BITS / 8;
   static constexpr int RAW_W_BYTES = BK * CODE_ROW_BYTES;
   static constexpr int RAW_S_BYTES = WFormat<WF>::SCALE_ROWS * BN * WFormat<WF>::SCALE_BYTES;
   static constexpr int RAW_BYTES = 2 * (RAW_W_BYTES + RAW_S_BYTES);  // codes + scales of one K step
   // Two rings: A (from L2, short latency) and the codes (from DRAM, small):
-  // the codes ring is as deep as about 104 KB allows, so many K steps of the
-  // weight stream are in flight while A and the decode keep pace.
+  // the codes ring is as deep as the rest of shared memory allows (about
+  // 104 KB, 56 KB with two A blocks), so many K steps of the weight stream
+  // are in flight while A and the decode keep pace.
   static constexpr int A_STAGES = 3;
-  static constexpr int C_STAGES_RAW = (104 * 1024) / RAW_BYTES;
+  static constexpr int C_STAGES_RAW = ((MB == 1 ? 104 : 56) * 1024) / RAW_BYTES;
   static constexpr int C_STAGES = C_STAGES_RAW > 16 ? 16 : C_STAGES_RAW;
   static constexpr int DEC_BUFS = 2;
   static constexpr int C_OFF = A_STAGES * A_BYTES;
@@ -65,7 +73,7 @@ struct DqCfg {
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
   static constexpr int EPI_WARPS = 8, PRODUCER_WARP = 8, MMA_WARP = 9, CODES_WARP = 10;
   static constexpr int THREADS = 32 * 11;
-  static constexpr int TMEM_COLS = 256;
+  static constexpr int TMEM_COLS = 256 * MB;
   // 4-bit codes (INT4, NVFP4) decode as column pairs (c, c + 4): fewer
   // operations; the accumulator columns then carry that order, undone by the
   // epilogue
@@ -75,7 +83,8 @@ struct DqCfg {
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, MMA_N, false, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(RAW_BYTES % 128 == 0, "codes stages stay 128-byte aligned");
-  static_assert(C_STAGES >= 4, "codes ring depth");
+  static_assert(C_STAGES >= (MB == 1 ? 4 : 3), "codes ring depth");
+  static_assert(MB == 1 || MB == 2, "one or two 128-row blocks");
   static_assert(EPI_WARPS * 2 * STG_BYTES <= DEC_BUFS * DEC_BYTES, "staging reuses the decoded buffers");
   static_assert(WF != WF_BF16, "a decoded weight format");
 };
@@ -184,7 +193,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ------------------------------------------------------------ A producer
     if (lane == 0)
       produce(C::A_STAGES, a_full, a_empty, C::A_BYTES, [&](int s, uint32_t fb, int kb) {
-        ptx::tma_load_2d(base + s * C::A_BYTES, &tmA, fb, kb * C::BK, mb * C::BM);
+#pragma unroll
+        for (int i = 0; i < C::MB; ++i)
+          ptx::tma_load_2d(base + s * C::A_BYTES + i * C::A_BOX_BYTES, &tmA, fb, kb * C::BK,
+                           (mb * C::MB + i) * C::BM);
       });
     __syncwarp();
   } else if (warp == C::CODES_WARP) {
@@ -217,10 +229,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t sb = base + C::DEC_OFF + d * C::DEC_BYTES;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
-          const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
           const uint64_t bdesc =
               ptx::smem_desc(sb + kk * C::B_KSTEP, C::ATOM_BYTES, C::B_SBO, ptx::SW_128B);
-          ptx::mma_f16(tmem_base, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+          for (int i = 0; i < C::MB; ++i) {  // block i accumulates in columns [256 i, 256 i + 256)
+            const uint64_t adesc =
+                ptx::smem_desc(sa + i * C::A_BOX_BYTES + kk * 32, 16, 1024, ptx::SW_128B);
+            ptx::mma_f16(tmem_base + i * C::MMA_N, adesc, bdesc, C::IDESC,
+                         (kb | kk) != 0 ? 1u : 0u);
+          }
         }
         ptx::mma_commit(a_empty(a));        // this A stage has been read
         ptx::mma_commit(dempty_bar(d));     // and the decoded buffer
@@ -272,9 +289,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t it = 0;
       const float gs = C::WF == WF_NVFP4 ? *p.sW1 : 1.0f;
       const float us = C::WF == WF_NVFP4 ? *p.sW2 : 1.0f;
-      epilogue_tile<false, C::BN, C::WF == WF_NVFP4, C::PAIRED>(tacc, mb * C::BM + q * 32, nb * C::BN, 2 * h,
-                                                     2 * h + 2, &tmY, p.M, p.N, smem, base,
-                                                     stg_base, it, lane, spare_bar, gs, us);
+#pragma unroll 1
+      for (int i = 0; i < C::MB; ++i) {
+        const int row_blk = (mb * C::MB + i) * C::BM;
+        if (row_blk >= p.M) break;  // a second block wholly below the matrix
+        epilogue_tile<false, C::BN, C::WF == WF_NVFP4, C::PAIRED>(
+            tacc + i * C::MMA_N, row_blk + q * 32, nb * C::BN, 2 * h, 2 * h + 2, &tmY, p.M, p.N,
+            smem, base, stg_base, it, lane, spare_bar, gs, us);
+      }
       if (lane == 0) ptx::bulk_wait_read<0>();
       __syncwarp();
     }

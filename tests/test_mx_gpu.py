@@ -51,7 +51,10 @@ def _run(sg, fmt, M, N, K, seed, rows=None):
 @pytest.mark.parametrize("shape", [(1, 64, 64), (7, 96, 128), (63, 288, 384), (128, 4864, 896),
                                    (200, 160, 512), (65, 4864, 896),
                                    # wide weight matrices: the 128-column one-CTA kernel
-                                   (37, 9760, 256), (130, 9856, 192)],
+                                   (37, 9760, 256), (130, 9856, 192),
+                                   # two 128-row blocks per CTA, the last CTA's second
+                                   # block wholly below the matrix
+                                   (300, 9760, 256)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_mx_shapes(sg, fmt, shape):
     M, N, K = shape

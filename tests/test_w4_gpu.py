@@ -44,7 +44,10 @@ def _run(sg, M, N, K, G, seed, rows=None):
                                    (65, 4864, 896, 128),
                                    # wide weight matrices: the 128-column one-CTA kernel, with
                                    # a ragged last tile (9760 = 76 x 128 + 32) and ragged M
-                                   (37, 9760, 256, 128), (130, 9856, 192, 64)],
+                                   (37, 9760, 256, 128), (130, 9856, 192, 64),
+                                   # two 128-row blocks per CTA, the last CTA's second
+                                   # block wholly below the matrix
+                                   (300, 9760, 256, 128)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_w4_shapes(sg, shape):
     M, N, K, G = shape
