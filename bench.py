@@ -423,15 +423,21 @@ class Workload:
             return 1
         return 2 + (1 if self.lib.swiglu_linear_workspace_size(M, self.K, self.N) > 0 else 0)
 
-    def variant_label(self, v):
+    def variant_label(self, v, M):
         if self.kind == "mlp":
             return "mlp"
         if self.producer:
             return "rmsnorm_quant+2sm_fp8"
-        if self.kind == "w4":
-            return "w4_sk2"
-        if self.kind == "mx":
-            return f"{self.mxfmt}_sk2"
+        if self.kind in ("w4", "mx"):
+            # the library's choice for weight formats: split-K over CTA pairs for
+            # few rows and columns, else the wide kernel (two row blocks if M > 128)
+            import torch
+            sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+            fmt = "w4" if self.kind == "w4" else self.mxfmt
+            if M <= 128 and 2 * -(-self.N // 64) <= sms:
+                return f"{fmt}_sk2"
+            mb2 = M > 128 and 10 * -(-M // 256) * -(-self.N // 128) >= 9 * sms
+            return f"{fmt}_wide" + ("_mb2" if mb2 else "")
         return "2sm_fp8" if self.fp8 else self.sg.variant_name(v)
 
     def step(self):
@@ -565,7 +571,7 @@ def run_ours(args, ws, rank, local):
         r = roofline_entry(flops, abytes, us, peak_tf, peaks["hbm_gbs"])
         bound, achieved_tf, achieved_gbs = r["bound"], r["tflops"], r["gbs"]
         kernels.append({
-            "form": form, "M": M, "variant": "2sm_fp8" if wl.producer else wl.variant_label(v),
+            "form": form, "M": M, "variant": "2sm_fp8" if wl.producer else wl.variant_label(v, M),
             "us": round(us, 3),
             "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
             "frac_of_roofline": round(r["frac_of_roofline"], 4),

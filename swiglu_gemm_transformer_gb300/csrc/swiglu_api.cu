@@ -241,9 +241,10 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
-  // Few output columns: 64-column tiles split along K over CTA pairs; many:
-  // 128-column tiles, one CTA each (A read once for twice the weights).
-  const bool wide = 2 * cdiv(N, 64) > st->sm_count;
+  // Few rows and few output columns: 64-column tiles split along K over CTA
+  // pairs; otherwise 128-column tiles, one CTA each over all of K (A read once
+  // for twice the weights), with two 128-row blocks per CTA when M > 128.
+  const bool wide = M > 128 || 2 * cdiv(N, 64) > st->sm_count;
   const uint32_t cols = wide ? 128 : 64;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1q, N / 2, K, N / 2, cols / 2, 64, NOSW);
@@ -258,8 +259,10 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   p.N = int32_t(N);
   p.K = int32_t(K);
   // wide kernel with M > 128: each CTA takes two 128-row blocks of A, so one
-  // decode of a weight step serves 256 rows
-  const int m_blocks = wide && M > 128 ? 2 : 1;
+  // decode of a weight step serves 256 rows -- when those CTAs still fill
+  // about one wave; otherwise one block each, for parallelism
+  const int m_blocks =
+      wide && M > 128 && 10 * cdiv(M, 256) * cdiv(N, cols) >= 9 * int64_t(st->sm_count) ? 2 : 1;
   p.num_m_blk = int32_t(cdiv(M, 128 * m_blocks));
   p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
@@ -317,7 +320,7 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
-  const bool wide = 2 * cdiv(N, 64) > st->sm_count;  // as for INT4
+  const bool wide = M > 128 || 2 * cdiv(N, 64) > st->sm_count;  // as for INT4
   const uint32_t cols = wide ? 128 : 64;
   const uint32_t cbox = nvfp4 ? cols / 2 : cols, srows = nvfp4 ? 4 : 2;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -333,8 +336,10 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   p.N = int32_t(N);
   p.K = int32_t(K);
   // wide kernel with M > 128: each CTA takes two 128-row blocks of A, so one
-  // decode of a weight step serves 256 rows
-  const int m_blocks = wide && M > 128 ? 2 : 1;
+  // decode of a weight step serves 256 rows -- when those CTAs still fill
+  // about one wave; otherwise one block each, for parallelism
+  const int m_blocks =
+      wide && M > 128 && 10 * cdiv(M, 256) * cdiv(N, cols) >= 9 * int64_t(st->sm_count) ? 2 : 1;
   p.num_m_blk = int32_t(cdiv(M, 128 * m_blocks));
   p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
