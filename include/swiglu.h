@@ -164,10 +164,12 @@ int swiglu_pack_interleaved_fp8(const void *W1t, const void *W2t, void *Wfused_t
  *   S1, S2   : device, BF16 [K/group, N]         (read)
  *   Y        : device, BF16 [M,N] row-major      (written)
  * group must be a multiple of 64 dividing K; N a multiple of 32; K a multiple
- * of 8; pointers 16-byte aligned.  Runs the split-K cluster kernel
- * (SWIGLU_VARIANT_1SM_N64_SK2's structure) whose epilogue warps decode each
- * stage's codes to BF16 in shared memory before the MMA reads them: the
- * weight stream is 4.1 bits per weight instead of 16.
+ * of 8; pointers 16-byte aligned.  For M <= 128 with few columns it runs the
+ * split-K cluster kernel (SWIGLU_VARIANT_1SM_N64_SK2's structure), otherwise
+ * a one-CTA-per-128-column kernel over all of K (one or two 128-row blocks per
+ * CTA); in both, warps decode each step's codes to BF16 in shared memory
+ * before the MMA reads them: the weight stream is 4.1 bits per weight instead
+ * of 16.
  */
 int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *W2q,
                     const void *S2, void *Y, int64_t M, int64_t N, int64_t K, int64_t group,
@@ -184,8 +186,9 @@ int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *
  *          one per column and 16 K rows; g1, g2: device pointers to one FP32
  *          scale per tensor.  W = E2M1(c) * E4M3(s) * g.
  * Y = SiLU(A x W1) (.) (A x W2) with BF16 A [M,K] and Y [M,N].  The codes are
- * decoded to BF16 in shared memory inside the split-K cluster kernel (E4M3 *
- * 2^k and E2M1 * E4M3 are exact in BF16) and multiplied on BF16 tensor cores;
+ * decoded to BF16 in shared memory inside the same kernels as the INT4 form
+ * (E4M3 * 2^k and E2M1 * E4M3 are exact in BF16) and multiplied on BF16 tensor
+ * cores;
  * the NVFP4 tensor scales multiply the gate and up sums before the
  * activation.  K a multiple of 64, N of 32; pointers 16-byte aligned (g1, g2:
  * 4-byte).
