@@ -428,16 +428,9 @@ class Workload:
             return "mlp"
         if self.producer:
             return "rmsnorm_quant+2sm_fp8"
-        if self.kind in ("w4", "mx"):
-            # the library's choice for weight formats: split-K over CTA pairs for
-            # few rows and columns, else the wide kernel (two row blocks if M > 128)
-            import torch
-            sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+        if self.kind in ("w4", "mx"):   # the library's choice of kernel
             fmt = "w4" if self.kind == "w4" else self.mxfmt
-            if M <= 128 and 2 * -(-self.N // 64) <= sms:
-                return f"{fmt}_sk2"
-            mb2 = M > 128 and 10 * -(-M // 256) * -(-self.N // 128) >= 9 * sms
-            return f"{fmt}_wide" + ("_mb2" if mb2 else "")
+            return f"{fmt}_{self.sg.WEIGHT_KERNELS[self.sg.swiglu_select_weight_kernel(M, self.N)]}"
         return "2sm_fp8" if self.fp8 else self.sg.variant_name(v)
 
     def step(self):

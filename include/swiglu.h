@@ -311,6 +311,14 @@ int swiglu_fused_interleaved_ex(const void *A, const void *Wfused, void *Y,
  * (interleaved = 0 or 1) on the current device.  Host-only. */
 int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved);
 
+/* The kernel the weight-format entry points (swiglu_fused_w4, _mxfp8, _nvfp4)
+ * run for M rows and N output columns on the current device: 0 = the split-K
+ * cluster kernel (M <= 128 and 2 * ceil(N/64) <= #SMs), 1 = the wide kernel
+ * with one 128-row block per CTA, 2 = the wide kernel with two (M > 128 and
+ * ceil(M/256) * ceil(N/128) >= 0.9 * #SMs).  -1 for negative sizes.
+ * Host-only (GB300's 152 SMs when no device is visible). */
+int swiglu_select_weight_kernel(int64_t M, int64_t N);
+
 /* Short name of a variant ("1sm_n128", ...); "?" for an unknown value. */
 const char *swiglu_variant_name(int32_t variant);
 

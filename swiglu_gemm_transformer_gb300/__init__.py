@@ -50,6 +50,7 @@ EXPORTS = {
     "swiglu_mlp_noalloc_scratch_bytes": ("", ctypes.c_uint64),
     "swiglu_mlp_noalloc": ("ppppp p lll p", ctypes.c_int),
     "swiglu_select_variant": ("lll i", ctypes.c_int),
+    "swiglu_select_weight_kernel": ("ll", ctypes.c_int),
     "swiglu_variant_name": ("i", ctypes.c_char_p),
     "swiglu_status_string": ("i", ctypes.c_char_p),
     "swiglu_device_status": ("p P", ctypes.c_int),
@@ -460,6 +461,15 @@ def swiglu_mlp_noalloc(A, W1, W2, W3, R, Z, *, stream=None):
 
 def swiglu_select_variant(M: int, N: int, K: int, interleaved: bool = False) -> int:
     return lib().swiglu_select_variant(M, N, K, 1 if interleaved else 0)
+
+
+WEIGHT_KERNELS = ("sk2", "wide", "wide_mb2")
+
+
+def swiglu_select_weight_kernel(M: int, N: int) -> int:
+    """0 split-K cluster kernel, 1 wide kernel, 2 wide kernel with two row
+    blocks per CTA: the kernel the INT4/MXFP8/NVFP4 entry points run."""
+    return lib().swiglu_select_weight_kernel(M, N)
 
 
 def swiglu_device_status(stream=None):

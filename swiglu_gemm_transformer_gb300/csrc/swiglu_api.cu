@@ -110,6 +110,18 @@ int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Kernel for the weight formats (INT4, MXFP8, NVFP4): 0 = the split-K
+// cluster kernel (64-column tiles; few rows and few columns, so that its
+// tiles fill the GPU), 1 = the wide kernel with one 128-row block per CTA,
+// 2 = the wide kernel with two (M > 128 and that grid still fills about one
+// wave: one decode of each weight step then serves 256 rows).
+int weight_kernel(int64_t M, int64_t N, int sm_count) {
+  if (M <= 128 && 2 * cdiv(N, 64) <= sm_count) return 0;
+  if (M > 128 && 10 * cdiv(M, 256) * cdiv(N, 128) >= 9 * int64_t(sm_count)) return 2;
+  return 1;
+}
+
+
 int choose_variant(int64_t M, int64_t N, int64_t K, bool /*interleaved*/, int sm_count) {
   // One 128-row block whose 128x64 tiles, split over two CTAs along K, fill
   // the GPU in one wave: the split-K cluster kernel keeps all of a CTA's
@@ -243,8 +255,9 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
   // Few rows and few output columns: 64-column tiles split along K over CTA
   // pairs; otherwise 128-column tiles, one CTA each over all of K (A read once
-  // for twice the weights), with two 128-row blocks per CTA when M > 128.
-  const bool wide = M > 128 || 2 * cdiv(N, 64) > st->sm_count;
+  // for twice the weights), with one or two 128-row blocks per CTA.
+  const int kern = weight_kernel(M, N, st->sm_count);
+  const bool wide = kern != 0;
   const uint32_t cols = wide ? 128 : 64;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1q, N / 2, K, N / 2, cols / 2, 64, NOSW);
@@ -258,11 +271,7 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   p.M = int32_t(M);
   p.N = int32_t(N);
   p.K = int32_t(K);
-  // wide kernel with M > 128: each CTA takes two 128-row blocks of A, so one
-  // decode of a weight step serves 256 rows -- when those CTAs still fill
-  // about one wave; otherwise one block each, for parallelism
-  const int m_blocks =
-      wide && M > 128 && 10 * cdiv(M, 256) * cdiv(N, cols) >= 9 * int64_t(st->sm_count) ? 2 : 1;
+  const int m_blocks = kern == 2 ? 2 : 1;
   p.num_m_blk = int32_t(cdiv(M, 128 * m_blocks));
   p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
@@ -320,7 +329,8 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
-  const bool wide = M > 128 || 2 * cdiv(N, 64) > st->sm_count;  // as for INT4
+  const int kern = weight_kernel(M, N, st->sm_count);  // as for INT4
+  const bool wide = kern != 0;
   const uint32_t cols = wide ? 128 : 64;
   const uint32_t cbox = nvfp4 ? cols / 2 : cols, srows = nvfp4 ? 4 : 2;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -335,11 +345,7 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   p.M = int32_t(M);
   p.N = int32_t(N);
   p.K = int32_t(K);
-  // wide kernel with M > 128: each CTA takes two 128-row blocks of A, so one
-  // decode of a weight step serves 256 rows -- when those CTAs still fill
-  // about one wave; otherwise one block each, for parallelism
-  const int m_blocks =
-      wide && M > 128 && 10 * cdiv(M, 256) * cdiv(N, cols) >= 9 * int64_t(st->sm_count) ? 2 : 1;
+  const int m_blocks = kern == 2 ? 2 : 1;
   p.num_m_blk = int32_t(cdiv(M, 128 * m_blocks));
   p.num_n_blk = int32_t(cdiv(N, cols));
   p.num_k_blk = int32_t(cdiv(K, 64));
@@ -713,6 +719,11 @@ int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved) 
     sms = 152;  // GB300's SM count, for host-only planning without a device
   }
   return choose_variant(M, N, K, interleaved != 0, sms);
+}
+
+int swiglu_select_weight_kernel(int64_t M, int64_t N) {
+  if (M < 0 || N < 0) return -1;
+  return weight_kernel(M, N, device_sm_count());
 }
 
 const char *swiglu_variant_name(int32_t variant) {

@@ -58,6 +58,23 @@ def test_host_side_variant_choice(lib):
     assert lib.swiglu_select_variant(8192, 4864, 896, 0) == sg.VARIANT_2SM_N128
 
 
+def test_host_side_weight_kernel_choice(lib):
+    # no GPU here: planning assumes GB300's 152 SMs
+    # 0.5B, M <= 128: 76 column blocks of 64, split along K over CTA pairs
+    assert lib.swiglu_select_weight_kernel(64, 4864) == 0
+    assert lib.swiglu_select_weight_kernel(128, 4864) == 0
+    # 7B, M = 128: too many 64-column tiles for one wave -> the wide kernel
+    assert lib.swiglu_select_weight_kernel(128, 18944) == 1
+    # M > 128: two row blocks per CTA when that grid still fills a wave
+    assert lib.swiglu_select_weight_kernel(256, 18944) == 2   # 1 x 148 CTAs
+    assert lib.swiglu_select_weight_kernel(2048, 4864) == 2   # 8 x 38 CTAs
+    # ... else one (0.5B M = 512: 2 x 38 two-block CTAs would idle half the GPU)
+    assert lib.swiglu_select_weight_kernel(512, 4864) == 1
+    assert lib.swiglu_select_weight_kernel(129, 64) == 1
+    assert lib.swiglu_select_weight_kernel(-1, 64) == -1
+    assert sg.WEIGHT_KERNELS[lib.swiglu_select_weight_kernel(256, 18944)] == "wide_mb2"
+
+
 # Fake, never-dereferenced device addresses: validation is pure host arithmetic.
 A_, W1_, W2_, Y_ = 0x10000000, 0x20000000, 0x30000000, 0x40000000
 
