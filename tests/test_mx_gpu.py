@@ -62,8 +62,9 @@ def test_mx_shapes(sg, fmt, shape):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
-def test_mx_7b_shape_sampled(sg, fmt):
-    M, N, K = 256, 18944, 3584
+@pytest.mark.parametrize("M", [128, 256])  # the wide kernel with one and with two row blocks
+def test_mx_7b_shape_sampled(sg, fmt, M):
+    N, K = 18944, 3584
     _run(sg, fmt, M, N, K, seed=2, rows=si.sample_rows(M, 128, 32, seed=2))
 
 

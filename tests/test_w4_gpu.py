@@ -54,8 +54,9 @@ def test_w4_shapes(sg, shape):
     _run(sg, M, N, K, G, seed=M + N + K)
 
 
-def test_w4_7b_shape_sampled(sg):
-    M, N, K = 256, 18944, 3584
+@pytest.mark.parametrize("M", [128, 256])  # the wide kernel with one and with two row blocks
+def test_w4_7b_shape_sampled(sg, M):
+    N, K = 18944, 3584
     _run(sg, M, N, K, 128, seed=2, rows=si.sample_rows(M, 128, 32, seed=2))
 
 
