@@ -15,11 +15,15 @@ cudaError_t launch_linear(int lin_n, const LaunchArgs &la) {
 
 // Z = BF16(sum_s ws[s] + R): four columns per thread (N is a multiple of 8),
 // one pass over the FP32 partial sums; memory-bound, grid-stride, with the
-// slices' loads unrolled so they are in flight together.
+// slices' loads unrolled so they are in flight together.  Launched as a
+// programmatic dependent of the linear kernel: its blocks are resident while
+// that kernel ends and read the partial sums only after it has completed.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ ws,
                                                             int splits, int64_t slice_vec4,
                                                             const uint2 *__restrict__ R,
                                                             uint2 *__restrict__ Z, int64_t n_vec4) {
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_vec4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -58,10 +62,19 @@ cudaError_t launch_splitk_reduce(const float *ws, int splits, const void *R, voi
   if (n_vec4 == 0) return cudaSuccess;
   const int threads = 256;
   const int grid = (int)std::min<int64_t>((n_vec4 + threads - 1) / threads, (int64_t)sm_count * 8);
-  splitk_reduce_kernel<<<grid, threads, 0, s>>>(reinterpret_cast<const float4 *>(ws), splits,
-                                                 M * N / 4, static_cast<const uint2 *>(R),
-                                                 static_cast<uint2 *>(Z), n_vec4);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, reinterpret_cast<const float4 *>(ws),
+                            splits, M * N / 4, static_cast<const uint2 *>(R),
+                            static_cast<uint2 *>(Z), n_vec4);
 }
 
 }  // namespace swiglu
