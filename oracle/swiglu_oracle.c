@@ -521,7 +521,7 @@ int oracle_quant_e4m3(const double *a, int64_t n, float *scale, uint8_t *q)
     return 0;
 }
 
-/* ---- weight-only INT4 (SURVEY.md row "lower-precision weight variants") ----
+/* ---- weight-only INT4 (a lower-precision weight variant) ----
  *
  * The page names INT4 as a precision that raises tensor-core density
  * (section "Definizione del Problema") without defining a format.  Reading
