@@ -818,92 +818,141 @@ def run_compile_context(args, wl, stream, fused_us):
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_sample(workload: str, target_s: float):
-    """Time the CPU oracle on a bounded sample of the workload: for every call
-    of the step, the same number of seeded rows.  Returns (TFLOP/s, threads,
-    description, seconds)."""
-    import numpy as np
-    import oracle
-    import swiglu_inputs as si
-    K, N, Ms, seed = WORKLOADS[workload]
-    oracle.build()
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    rng = np.random.default_rng(seed)
-    mlp = workload.endswith("-mlp")
-    fp8 = workload.endswith("-fp8")
-    prod = workload.endswith("-fp8-rmsnorm")
-    w4 = workload.endswith("-w4")
-    mxf = workload.rsplit("-", 1)[1] if workload.endswith(("-mxfp8", "-nvfp4")) else None
-    if mxf:
-        Amx, m1, m2 = si.make_mx(max(Ms), N, K, seed, mxf)
-        amx = si.bits_u16(Amx)
-        cv = lambda w: tuple(x.numpy() if hasattr(x, "numpy") else x for x in w)
-        mxargs = (mxf, cv(m1), cv(m2))
-    if w4:
-        A4, (W1q, S1), (W2q, S2) = si.make_w4(max(Ms), N, K, seed, W4_GROUP)
-        a4 = si.bits_u16(A4)
-        w4args = (W1q.numpy(), si.bits_u16(S1), W2q.numpy(), si.bits_u16(S2), W4_GROUP)
-    if prod:   # the producer's inputs per M, the FP8 weights of the same recipe
-        (_, W1q, W2q), sc = si.make_e4m3(1, N, K, seed)
-        w18, w28 = si.bits_u8(W1q), si.bits_u8(W2q)
-        xg = {M: tuple(si.bits_u16(t) for t in si.make_producer_inputs(M, K, seed)) for M in Ms}
-    elif fp8:
-        (Aq, W1q, W2q), sc = si.make_e4m3(max(Ms), N, K, seed)
-        a8, w18, w28 = si.bits_u8(Aq), si.bits_u8(W1q), si.bits_u8(W2q)
-    else:
-        A, W1, W2 = si.make_bf16(max(Ms), N, K, seed)
-        a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
-        wf = oracle.pack_interleaved(w1, w2)
-        w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
-    forms = ("mlp",) if mlp else ("separate",) if (w4 or mxf) else ("separate", "interleaved")
-    per_row = (6 if mlp else 4) * N * K
+class OracleSampler:
+    """The CPU oracle on bounded samples of a workload: for every call of the
+    step, the same number of seeded rows.  Inputs are made and the oracle's
+    rate calibrated once; each sample() then times one row sample."""
 
-    def one(rows_per_call):
+    def __init__(self, workload: str):
+        import numpy as np
+        import oracle
+        import swiglu_inputs as si
+        self.workload = workload
+        K, N, Ms, seed = WORKLOADS[workload]
+        self.K, self.N, self.Ms = K, N, Ms
+        oracle.build()
+        self.threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+        self.rng = np.random.default_rng(seed)
+        mlp = workload.endswith("-mlp")
+        fp8 = workload.endswith("-fp8")
+        prod = workload.endswith("-fp8-rmsnorm")
+        w4 = workload.endswith("-w4")
+        mxf = workload.rsplit("-", 1)[1] if workload.endswith(("-mxfp8", "-nvfp4")) else None
+        if mxf:
+            Amx, m1, m2 = si.make_mx(max(Ms), N, K, seed, mxf)
+            amx = si.bits_u16(Amx)
+            cv = lambda w: tuple(x.numpy() if hasattr(x, "numpy") else x for x in w)
+            mxargs = (mxf, cv(m1), cv(m2))
+        if w4:
+            A4, (W1q, S1), (W2q, S2) = si.make_w4(max(Ms), N, K, seed, W4_GROUP)
+            a4 = si.bits_u16(A4)
+            w4args = (W1q.numpy(), si.bits_u16(S1), W2q.numpy(), si.bits_u16(S2), W4_GROUP)
+        if prod:   # the producer's inputs per M, the FP8 weights of the same recipe
+            (_, W1q, W2q), sc = si.make_e4m3(1, N, K, seed)
+            w18, w28 = si.bits_u8(W1q), si.bits_u8(W2q)
+            xg = {M: tuple(si.bits_u16(t) for t in si.make_producer_inputs(M, K, seed)) for M in Ms}
+        elif fp8:
+            (Aq, W1q, W2q), sc = si.make_e4m3(max(Ms), N, K, seed)
+            a8, w18, w28 = si.bits_u8(Aq), si.bits_u8(W1q), si.bits_u8(W2q)
+        else:
+            A, W1, W2 = si.make_bf16(max(Ms), N, K, seed)
+            a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
+            wf = oracle.pack_interleaved(w1, w2)
+            w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
+        self.forms = ("mlp",) if mlp else ("separate",) if (w4 or mxf) else ("separate", "interleaved")
+        self.per_row = (6 if mlp else 4) * N * K
+
+        def call(form, M, rows):
+            if mxf:
+                oracle.swiglu_mx(amx[:M], *mxargs, rows=rows)
+            elif w4:
+                oracle.swiglu_w4(a4[:M], *w4args, rows=rows)
+            elif prod:   # RMSNorm and quantisation of all of A (the scale needs every row)
+                sA, aq = oracle.rmsnorm_quant_e4m3(xg[M][0], xg[M][1], RMS_EPS)
+                oracle.swiglu_e4m3(aq, w18, w28, sA, sc[1], sc[2], rows=rows)
+            elif mlp:
+                oracle.mlp_bf16(a[:M], w1, w2, w3, rows=rows)
+            elif fp8:
+                oracle.swiglu_e4m3(a8[:M], w18, w28, *sc, rows=rows)
+            elif form == "separate":
+                oracle.swiglu_bf16(a[:M], w1, w2, rows=rows)
+            else:
+                oracle.swiglu_interleaved_bf16(a[:M], wf, rows=rows)
+
+        self._call = call
+        self.calls = [(form, M) for form in self.forms for M in self.Ms]
+        f0, s0 = self._one(max(1, self.threads))   # calibration
+        self.rate = f0 / s0
+        # the least a sample of every call costs: one row each (the oracle
+        # decodes the weights on every call, whatever the row count)
+        self.min_all_s = self._one(1)[1]
+        self._next = 0
+
+    def _one(self, rows_per_call, calls=None):
+        import numpy as np
         t0 = time.perf_counter()
         flops = 0
-        for form in forms:
-            for M in Ms:
-                rows = np.sort(rng.integers(0, M, size=rows_per_call))
-                if mxf:
-                    oracle.swiglu_mx(amx[:M], *mxargs, rows=rows)
-                elif w4:
-                    oracle.swiglu_w4(a4[:M], *w4args, rows=rows)
-                elif prod:   # RMSNorm and quantisation of all of A (the scale needs every row)
-                    sA, aq = oracle.rmsnorm_quant_e4m3(xg[M][0], xg[M][1], RMS_EPS)
-                    oracle.swiglu_e4m3(aq, w18, w28, sA, sc[1], sc[2], rows=rows)
-                elif mlp:
-                    oracle.mlp_bf16(a[:M], w1, w2, w3, rows=rows)
-                elif fp8:
-                    oracle.swiglu_e4m3(a8[:M], w18, w28, *sc, rows=rows)
-                elif form == "separate":
-                    oracle.swiglu_bf16(a[:M], w1, w2, rows=rows)
-                else:
-                    oracle.swiglu_interleaved_bf16(a[:M], wf, rows=rows)
-                flops += per_row * rows_per_call
+        for form, M in calls or self.calls:
+            rows = np.sort(self.rng.integers(0, M, size=rows_per_call))
+            self._call(form, M, rows)
+            flops += self.per_row * rows_per_call
         return flops, time.perf_counter() - t0
 
-    f0, s0 = one(max(1, threads))               # calibration
-    rate = f0 / s0
-    rows = max(1, int(target_s * rate / (per_row * len(forms) * len(Ms))))
-    flops, secs = one(rows)
-    desc = (f"{rows} seeded rows of each of the {len(forms) * len(Ms)} calls (M in {list(Ms)}, "
-            f"{'/'.join(forms)}), all output columns, K={K}: {flops / 1e9:.1f} GFLOP in {secs:.1f} s")
-    return flops / secs / 1e12, threads, desc, secs
+    def sample(self, target_s: float):
+        """Time one sample of about target_s seconds (at least one row per
+        call).  Returns (TFLOP/s, seconds, description)."""
+        ncalls = len(self.calls)
+        rows = max(1, int(target_s * self.rate / (self.per_row * ncalls)))
+        flops, secs = self._one(rows)
+        desc = (f"{rows} seeded rows of each of the {ncalls} calls (M in {list(self.Ms)}, "
+                f"{'/'.join(self.forms)}), all output columns, K={self.K}: "
+                f"{flops / 1e9:.1f} GFLOP in {secs:.2f} s")
+        return flops / secs / 1e12, secs, desc
+
+    def sample_one_call(self, target_s: float):
+        """A smaller step: one call's seeded rows (the calls in turn).
+        Returns (flops, seconds)."""
+        form, M = self.calls[self._next % len(self.calls)]
+        self._next += 1
+        rows = max(1, int(target_s * self.rate / self.per_row))
+        return self._one(rows, [(form, M)])
+
+
+def oracle_sample(workload: str, target_s: float):
+    """One bounded sample of about target_s seconds (the cpu_baseline).
+    Returns (TFLOP/s, threads, description, seconds)."""
+    sampler = OracleSampler(workload)
+    v, secs, desc = sampler.sample(target_s)
+    return v, sampler.threads, desc, secs
 
 
 def run_reference(args, ws, rank):
+    """The oracle as it stands, on the host cores: inputs made and the rate
+    calibrated once, then every warm-up and timed step one row sample, sized
+    so that all steps together take about --cpu-seconds (at least one row of
+    each call per step, at most 6 s per step)."""
     if rank != 0:
         return None
-    target = args.cpu_seconds / max(1, args.steps + args.warmup)
-    target = max(0.2, min(target, 6.0))
-    import numpy as np  # noqa: F401
+    sampler = OracleSampler(args.workload)
+    target = min(args.cpu_seconds / max(1, args.steps + args.warmup), 6.0)
     vals = []
     desc = ""
-    threads = 0
-    for i in range(args.warmup + args.steps):
-        v, threads, desc, secs = oracle_sample(args.workload, target)
-        if i >= args.warmup:
-            vals.append((v, secs))
+    threads = sampler.threads
+    if target >= sampler.min_all_s:   # every step samples every call
+        for i in range(args.warmup + args.steps):
+            v, secs, desc = sampler.sample(target)
+            if i >= args.warmup:
+                vals.append((v, secs))
+    else:   # many steps: each step samples one call, the calls in turn
+        flops_t = 0
+        for i in range(args.warmup + args.steps):
+            f, secs = sampler.sample_one_call(target)
+            if i >= args.warmup:
+                vals.append((f / secs / 1e12, secs))
+                flops_t += f
+        desc = (f"{args.steps} steps of one call each (the {len(sampler.calls)} calls in turn, "
+                f"M in {list(sampler.Ms)}, {'/'.join(sampler.forms)}), seeded rows, all output "
+                f"columns, K={sampler.K}: {flops_t / 1e9:.1f} GFLOP")
     tot_flops = sum(v * s for v, s in vals)
     tot_s = sum(s for _, s in vals)
     value = tot_flops / tot_s

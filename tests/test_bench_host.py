@@ -99,3 +99,15 @@ def test_reference_arm_rank0_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 2
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
+
+
+def test_reference_arm_many_steps_sample_one_call_each():
+    # a per-step budget below one all-call sample: each step samples one call
+    # (in turn), so a long run stays bounded
+    r = _run_bench(["--impl", "reference", "--steps", "12", "--warmup", "2",
+                    "--workload", "qwen2.5-0.5b-m64", "--cpu-seconds", "0.001"],
+                   {"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode == 0, r.stderr
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    assert d["steps"] == 12 and d["warmup"] == 2 and d["value"] > 0
+    assert "steps of one call each" in d["cpu_baseline"]["sample"]
