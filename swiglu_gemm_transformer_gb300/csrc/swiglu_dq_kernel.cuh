@@ -12,19 +12,21 @@
 // the point: every CTA reads its 128 rows of A once for 128 output columns
 // (256 gate and up columns), so A's bytes per weight byte are half those of a
 // 64-column tile -- with 4-bit weights A is otherwise the larger stream.
-//   * warp 8 (one thread) streams each K step's A box into a short ring and
-//     warp 10 (one thread) the two matrices' code and scale boxes into a deep
-//     one (TMA): the weight stream is small per step, so many steps of it are
-//     in flight;
+//   * warp 8 (one thread) streams each K step's A box(es) into a short ring
+//     and warp 10 (one thread) the two matrices' code and scale boxes into a
+//     deep one (TMA): the weight stream is small per step, so many steps of
+//     it are in flight;
 //   * warps 0-7 decode each step's codes into one of two BF16 operand
 //     buffers ([64 K x 256] in the 128-byte-swizzled layout) and release the
 //     codes slot;
-//   * warp 9 (one thread) issues tcgen05.mma M=128 x N=256 x K=16, gate and
-//     up columns side by side in TMEM (columns [0,128) gate, [128,256) up),
-//     and frees the decoded buffer and the A slot through tcgen05.commit;
-//   * after the last K step warps 0-7 run the usual epilogue (TMEM loads,
-//     SiLU(g) * u in FP32, BF16, TMA stores through staging buffers that
-//     reuse the decoded buffers), applying NVFP4's per-tensor scales.
+//   * warp 9 (one thread) issues tcgen05.mma M=128 x N=256 x K=16 per row
+//     block, gate and up columns side by side in TMEM (block i: columns
+//     [256 i, 256 i + 128) gate, [256 i + 128, 256 i + 256) up), and frees the
+//     decoded buffer and the A slot through tcgen05.commit;
+//   * after the last K step warps 0-7 run the usual epilogue for each row
+//     block (TMEM loads, SiLU(g) * u in FP32, BF16, TMA stores through
+//     staging buffers that reuse the decoded buffers), applying NVFP4's
+//     per-tensor scales.
 // Every wait is bounded (timeout -> error word, abort flag, drain, TMEM freed).
 #pragma once
 
