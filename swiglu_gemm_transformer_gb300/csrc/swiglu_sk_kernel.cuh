@@ -24,10 +24,9 @@
 //     peer their partial gate/up sums of 16 of the peer's columns with
 //     st.async (16 bytes per store, counted on the peer's receive mbarrier),
 //     then wait for the peer's sums of their own 16 columns, add them, apply
-//     y = g * u / (1 + e^-g) in FP32 with one special-function operation per
-//     element, round to BF16 and store their 32 bytes of each row directly.
-//     With few rows this epilogue is not hidden behind MMAs, so its length
-//     is what the special-function unit and the exchange take.
+//     y = g * u / (1 + e^-g) in FP32, round to BF16 and store their 32 bytes
+//     of each row directly.  With few rows this epilogue is not hidden behind
+//     MMAs, so its length is what the exchange and the activation take.
 // Gate and up values never reach global memory.  One tile per cluster (no
 // persistent loop): the launcher sizes the grid to two CTAs per output tile.
 //
