@@ -883,10 +883,16 @@ class OracleSampler:
         self.calls = [(form, M) for form in self.forms for M in self.Ms]
         f0, s0 = self._one(max(1, self.threads))   # calibration
         self.rate = f0 / s0
-        # the least a sample of every call costs: one row each (the oracle
-        # decodes the weights on every call, whatever the row count)
-        self.min_all_s = self._one(1)[1]
+        self._min_all_s = None
         self._next = 0
+
+    @property
+    def min_all_s(self):
+        """The least a sample of every call costs: one row each (the oracle
+        decodes the weights on every call, whatever the row count)."""
+        if self._min_all_s is None:
+            self._min_all_s = self._one(1)[1]
+        return self._min_all_s
 
     def _one(self, rows_per_call, calls=None):
         import numpy as np
