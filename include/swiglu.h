@@ -67,13 +67,8 @@ typedef enum {
     /* one CTA per SM, 128-row tiles, 32 output columns per tile (small M: one
        tile per SM for N = 4864 on 152 SMs) */
     SWIGLU_VARIANT_1SM_N32 = 4,
-    /* the one-CTA variants in clusters of 2 or 4 CTAs on neighbouring column
-       blocks: each CTA loads 1/2 or 1/4 of the shared A tile and multicasts it
-       (small M, where every CTA otherwise re-reads the same A rows) */
-    SWIGLU_VARIANT_1SM_N32_MC2 = 5,
-    SWIGLU_VARIANT_1SM_N32_MC4 = 6,
-    SWIGLU_VARIANT_1SM_N64_MC2 = 7,
-    SWIGLU_VARIANT_1SM_N128_MC2 = 8,
+    /* 5-8: retired numbers, kept unused; passing one returns
+       SWIGLU_ERR_INVALID_ARG */
     /* split-K over a cluster of 2 CTAs (small M): each CTA multiplies half of
        the K steps of one 128-row x 64-column tile and the two partial gate/up
        accumulators are summed through distributed shared memory before the

@@ -13,14 +13,6 @@ cudaError_t launch_bf16_separate(int variant, const LaunchArgs &la) {
       return launch_tc<TileCfg<2, 64, false, 6>>(la);
     case SWIGLU_VARIANT_1SM_N32:
       return launch_tc<TileCfg<2, 32, false, 8>>(la);
-    case SWIGLU_VARIANT_1SM_N32_MC2:
-      return launch_tc<TileCfg<2, 32, false, 8, 2>>(la);
-    case SWIGLU_VARIANT_1SM_N32_MC4:
-      return launch_tc<TileCfg<2, 32, false, 8, 4>>(la);
-    case SWIGLU_VARIANT_1SM_N64_MC2:
-      return launch_tc<TileCfg<2, 64, false, 6, 2>>(la);
-    case SWIGLU_VARIANT_1SM_N128_MC2:
-      return launch_tc<TileCfg<4, 64, false, 4, 2>>(la);
     case SWIGLU_VARIANT_2SM_N128:
       return launch_pair<PairCfg<false, 6>>(la);
     default:

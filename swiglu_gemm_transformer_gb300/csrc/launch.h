@@ -27,7 +27,6 @@ struct VariantGeom {
   int b_swizzle_64;   // 1: weight boxes use the 64-byte swizzle (32-column boxes)
   int box_a;          // A box height (rows) per TMA copy
   int cluster;        // CTAs per tile (1, or 2 for the CTA-pair kernel)
-  int mc;             // CTAs sharing one A tile by multicast (1, 2 or 4)
 };
 
 VariantGeom variant_geom(int variant, bool interleaved);

@@ -18,49 +18,25 @@ inline void pdl_attr(cudaLaunchAttribute &a) {
 
 template <class C>
 cudaError_t launch_tc(const LaunchArgs &la) {
-  // Per-device one-time set-up: the dynamic shared-memory opt-in, and for
-  // clustered variants the number of clusters that can be resident at once.
+  // Per-device one-time set-up: the dynamic shared-memory opt-in.
   static std::atomic<uint64_t> configured{0};
-  static int max_clusters[64] = {0};
   const uint64_t bit = 1ull << (la.device & 63);
   auto kern = swiglu_bf16_tc_kernel<C>;
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[2];
-  pdl_attr(attr[0]);
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = C::MC;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(C::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = la.stream;
-  cfg.attrs = attr;
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (C::MC > 1) {
-      cfg.gridDim = dim3(C::MC * 32, 1, 1);
-      cfg.attrs = attr + 1;  // the occupancy query takes the cluster shape only
-      cfg.numAttrs = 1;
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      if (n < 1) return cudaErrorInvalidConfiguration;
-      max_clusters[la.device & 63] = n;
-      cfg.attrs = attr;
-    }
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  if (C::MC > 1) {
-    const int64_t units = int64_t(la.p.num_m_blk) * ((la.p.num_n_blk + C::MC - 1) / C::MC);
-    const int n = max_clusters[la.device & 63];
-    cfg.gridDim = dim3(C::MC * int(units < n ? units : n), 1, 1);
-    cfg.numAttrs = 2;
-  } else {
-    cfg.gridDim = dim3(la.grid, 1, 1);
-    cfg.numAttrs = 1;
-  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_attr(attr[0]);
+  cfg.gridDim = dim3(la.grid, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = la.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
 }
 

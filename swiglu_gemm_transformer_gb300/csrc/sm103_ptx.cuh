@@ -82,17 +82,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
-// 2-D tiled load written to the same shared-memory offset in every CTA of
-// `cta_mask`; each destination's mbarrier at offset `bar` counts the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                               int32_t c0, int32_t c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
-
 // Bring one 2-D tile into L2 only (no shared memory, no completion tracking).
 // Used once per descriptor at kernel start so the TMA unit holds the
 // descriptor before the first real copy; L2 is the coherence point of device
@@ -172,15 +161,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
                : "memory");
-}
-
-// As mma_commit, arriving on the barrier at offset `bar` in every CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // Warp: load 32 consecutive 32-bit columns of this warp's 32 TMEM lanes

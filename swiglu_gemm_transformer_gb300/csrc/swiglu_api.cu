@@ -110,6 +110,13 @@ int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The variants a caller may name (numbers 5-8 are retired and rejected).
+bool variant_known(int32_t v) {
+  return v == SWIGLU_VARIANT_AUTO || v == SWIGLU_VARIANT_1SM_N128 || v == SWIGLU_VARIANT_1SM_N64 ||
+         v == SWIGLU_VARIANT_2SM_N128 || v == SWIGLU_VARIANT_1SM_N32 ||
+         v == SWIGLU_VARIANT_1SM_N64_SK2;
+}
+
 // Kernel for the weight formats (INT4, MXFP8, NVFP4): 0 = the split-K
 // cluster kernel (64-column tiles; few rows and few columns, so that its
 // tiles fill the GPU), 1 = the wide kernel with one 128-row block per CTA,
@@ -148,7 +155,7 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, int64_t N,
              int64_t K, int32_t variant, bool interleaved, void *stream) {
-  if (variant < 0 || variant >= SWIGLU_VARIANT_COUNT_) return SWIGLU_ERR_INVALID_ARG;
+  if (!variant_known(variant)) return SWIGLU_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return SWIGLU_ERR_INVALID_ARG;
   if (M > kMaxDim || K > kMaxDim || 2 * N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return SWIGLU_OK;
@@ -551,20 +558,15 @@ namespace swiglu {
 
 VariantGeom variant_geom(int variant, bool interleaved) {
   // separate N32: two 32-column boxes (W1, W2); interleaved N32: one 64-column W_fused box
-  const VariantGeom n32 = interleaved ? VariantGeom{128, 32, 64, 64, 0, 128, 1, 1}
-                                      : VariantGeom{128, 32, 64, 32, 1, 128, 1, 1};
-  VariantGeom g;
   switch (variant) {
-    case SWIGLU_VARIANT_1SM_N64: return {128, 64, 64, 64, 0, 128, 1, 1};
-    case SWIGLU_VARIANT_1SM_N32: return n32;
-    case SWIGLU_VARIANT_1SM_N32_MC2: g = n32; g.mc = 2; g.box_a = 64; return g;
-    case SWIGLU_VARIANT_1SM_N32_MC4: g = n32; g.mc = 4; g.box_a = 32; return g;
-    case SWIGLU_VARIANT_1SM_N64_MC2: return {128, 64, 64, 64, 0, 64, 1, 2};
-    case SWIGLU_VARIANT_1SM_N128_MC2: return {128, 128, 64, 64, 0, 64, 1, 2};
-    case SWIGLU_VARIANT_2SM_N128: return {256, 128, 64, 64, 0, 128, 2, 1};
-    case SWIGLU_VARIANT_1SM_N64_SK2: return {128, 64, 64, 64, 0, 128, 2, 1};
+    case SWIGLU_VARIANT_1SM_N64: return {128, 64, 64, 64, 0, 128, 1};
+    case SWIGLU_VARIANT_1SM_N32:
+      return interleaved ? VariantGeom{128, 32, 64, 64, 0, 128, 1}
+                         : VariantGeom{128, 32, 64, 32, 1, 128, 1};
+    case SWIGLU_VARIANT_2SM_N128: return {256, 128, 64, 64, 0, 128, 2};
+    case SWIGLU_VARIANT_1SM_N64_SK2: return {128, 64, 64, 64, 0, 128, 2};
     case SWIGLU_VARIANT_1SM_N128:
-    default: return {128, 128, 64, 64, 0, 128, 1, 1};
+    default: return {128, 128, 64, 64, 0, 128, 1};
   }
 }
 
@@ -733,10 +735,6 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_1SM_N64: return "1sm_n64";
     case SWIGLU_VARIANT_2SM_N128: return "2sm_n128";
     case SWIGLU_VARIANT_1SM_N32: return "1sm_n32";
-    case SWIGLU_VARIANT_1SM_N32_MC2: return "1sm_n32_mc2";
-    case SWIGLU_VARIANT_1SM_N32_MC4: return "1sm_n32_mc4";
-    case SWIGLU_VARIANT_1SM_N64_MC2: return "1sm_n64_mc2";
-    case SWIGLU_VARIANT_1SM_N128_MC2: return "1sm_n128_mc2";
     case SWIGLU_VARIANT_1SM_N64_SK2: return "1sm_n64_sk2";
     default: return "?";
   }

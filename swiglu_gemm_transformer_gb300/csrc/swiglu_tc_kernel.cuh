@@ -50,13 +50,8 @@ namespace swiglu {
 
 // NB_ATOMS weight boxes of ATOM_COLS columns make the MMA's B operand.
 //   ATOM_COLS = 64: 128-byte swizzle; ATOM_COLS = 32: 64-byte swizzle.
-// MC > 1: clusters of MC CTAs on neighbouring column blocks of the same row
-// block share the A tile; each CTA loads 128/MC of its rows and multicasts
-// them to the whole cluster (A traffic per CTA divided by MC).
-template <int NB_ATOMS_, int ATOM_COLS_, bool INTERLEAVED_, int STAGES_, int MC_ = 1>
+template <int NB_ATOMS_, int ATOM_COLS_, bool INTERLEAVED_, int STAGES_>
 struct TileCfg {
-  static constexpr int MC = MC_;
-  static constexpr int A_PIECE_ROWS = 128 / MC_;
   static constexpr int NB_ATOMS = NB_ATOMS_;
   static constexpr int ATOM_COLS = ATOM_COLS_;
   static constexpr bool INTERLEAVED = INTERLEAVED_;
@@ -87,7 +82,6 @@ struct TileCfg {
   static_assert(MMA_N % 16 == 0 && MMA_N >= 64 && MMA_N <= 256, "MMA N");
   static_assert(INTERLEAVED || NB_ATOMS % 2 == 0, "separate form: half the boxes per weight");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(MC == 1 || MC == 2 || MC == 4, "cluster size");
 };
 
 template <class C>
@@ -112,19 +106,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Work unit: a cluster tile = one row block x MC neighbouring column blocks;
-  // CTA `rank` of the cluster takes column block ng * MC + rank.
-  const int rank = C::MC > 1 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
-  const int unit0 = C::MC > 1 ? static_cast<int>(ptx::cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int unit_step = C::MC > 1 ? static_cast<int>(ptx::num_clusters_x()) : static_cast<int>(gridDim.x);
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << C::MC) - 1u);
-  KParams pc = p;  // tile order over cluster tiles
-  pc.num_n_blk = (p.num_n_blk + C::MC - 1) / C::MC;
+  const int unit0 = static_cast<int>(blockIdx.x);
+  const int unit_step = static_cast<int>(gridDim.x);
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), C::MC);  // every CTA's MMA frees the stage
+      ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
@@ -143,10 +131,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  if (C::MC > 1)
-    ptx::cluster_sync();  // peers' barriers are initialised before any multicast
-  else
-    __syncthreads();
+  __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Everything above overlaps the previous kernel when launched with PDL.
@@ -157,7 +142,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ptx::tma_prefetch_2d(&tmB0, 0, 0);
     if (!C::INTERLEAVED) ptx::tma_prefetch_2d(&tmB1, 0, 0);
   }
-  const int num_units = pc.num_m_blk * pc.num_n_blk;
+  const int num_units = p.num_m_blk * p.num_n_blk;
   // The weight boxes of one stage (K step kb of column block nb).
   auto load_w = [&](uint32_t sb, uint32_t fb, int nb, int kb) {
     if (C::INTERLEAVED) {
@@ -182,11 +167,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (warp == C::PRODUCER_WARP && p.w_early && unit0 < num_units) {
     pre = p.num_k_blk < C::STAGES ? p.num_k_blk : C::STAGES;
     if (lane == 0) {
-      int mb, ng;
-      tile_coords(unit0, pc, mb, ng);
+      int mb, nb;
+      tile_coords(unit0, p, mb, nb);
       for (uint32_t s = 0; s < pre; ++s) {
         ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-        load_w(base + s * C::STAGE_BYTES + C::A_BYTES, full_bar(s), ng * C::MC + rank, (int)s);
+        load_w(base + s * C::STAGE_BYTES + C::A_BYTES, full_bar(s), nb, (int)s);
       }
     }
     __syncwarp();
@@ -200,9 +185,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t issued = 0;
       bool ok = true;
       for (int t = unit0; ok && t < num_units; t += unit_step) {
-        int mb, ng;
-        tile_coords(t, pc, mb, ng);
-        const int nb = ng * C::MC + rank;
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
         for (int kb = 0; kb < p.num_k_blk; ++kb) {
           const bool early = issued < pre;  // weights already on their way
           if (!early && !wait_bar(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, p.err,
@@ -214,11 +198,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t sb = sa + C::A_BYTES;
           const uint32_t fb = full_bar(stage);
           if (!early) ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          if (C::MC > 1)
-            ptx::tma_load_2d_mc(sa + rank * C::A_PIECE_ROWS * 128, &tmA, fb, kb * C::BK,
-                                mb * C::BM + rank * C::A_PIECE_ROWS, kMask);
-          else
-            ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
+          ptx::tma_load_2d(sa, &tmA, fb, kb * C::BK, mb * C::BM);
           if (!early) load_w(sb, fb, nb, kb);
           ++issued;
           if (++stage == C::STAGES) {
@@ -227,21 +207,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
       }
-      const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
       if (!ok) {
-        if (C::MC > 1) {
-          spin_ns(100000);  // peers' multicasts into this CTA land within microseconds
-        } else {
-          // Let the copies already in flight land before the CTA's shared
-          // memory is released: wait for the last min(issued, STAGES) loads.
-          for (uint32_t i = issued - n; i < issued; ++i)
-            wait_quiet(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
-        }
-      } else if (C::MC > 1) {
-        // Consume the MMA-completion arrivals still due from the peers, so no
-        // multicast arrive targets this CTA after it exits.
+        // Let the copies already in flight land before the CTA's shared
+        // memory is released: wait for the last min(issued, STAGES) loads.
+        const uint32_t n = issued < (uint32_t)C::STAGES ? issued : (uint32_t)C::STAGES;
         for (uint32_t i = issued - n; i < issued; ++i)
-          wait_quiet(empty_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
+          wait_quiet(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -276,10 +247,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 ptx::smem_desc(sb + kk * C::B_KSTEP, C::ATOM_BYTES, C::B_SBO, C::B_SWIZZLE);
             ptx::mma_f16(d, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (C::MC > 1)
-            ptx::mma_commit_mc(empty_bar(stage), kMask);  // the stage is free in every CTA
-          else
-            ptx::mma_commit(empty_bar(stage));
+          ptx::mma_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -307,9 +275,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint32_t stg_base = base + C::STG_OFF + warp * 2 * C::STG_BYTES;
     uint32_t abuf = 0, aphase = 0, it = 0;
     for (int t = unit0; t < num_units; t += unit_step) {
-      int mb, ng;
-      tile_coords(t, pc, mb, ng);
-      const int nb = ng * C::MC + rank;
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
       bool ok = wait_bar(accf_bar(abuf), aphase, p.timeout_ns, abort_flag, p.err,
                          WAIT_EPI_ACC_FULL);
       ok = __all_sync(0xffffffffu, ok);
@@ -331,10 +298,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
 
   ptx::tc_fence_before();
-  if (C::MC > 1)
-    ptx::cluster_sync();  // no peer multicasts into this CTA after it exits
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == C::MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
