@@ -428,13 +428,12 @@ int oracle_mlp_bf16(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
  *   - one scale for the whole tensor: s = max|a| / 448 (448 = the largest
  *     finite E4M3 value), rounded once to binary32 because the projection
  *     takes its scales as floats; s = 0 when every a is zero;
- *   - q = E4M3(a / s): round to nearest, ties to even, saturating at +-448;
- *     all codes are 0 when s = 0.  The code is an integer decided by
- *     floating point, and the page fixes no precision for it, so the decision
- *     is taken in the precision of the kernels: on the binary32 quotient of
- *     a (rounded to binary32) and s.  Where a and max|a| are both BF16 values
- *     that quotient often lands exactly on a midpoint between two codes even
- *     though the exact quotient (with s rounded) lies a hair to one side.
+ *   - q = E4M3(a / s): the exact quotient of a and the binary32 scale,
+ *     rounded to the nearest E4M3 value, ties to even, saturating at +-448,
+ *     as the OCP 8-bit floating point specification defines conversion to
+ *     E4M3 ("fn" variant); all codes are 0 when s = 0.  The quotient is taken
+ *     in double, which resolves every decision the exact quotient makes
+ *     except where it lies within 2^-53 of a midpoint.
  */
 
 /* Round a double to FP8 E4M3 ("fn" variant, see oracle_e4m3_to_f64), ties to
@@ -513,11 +512,8 @@ int oracle_quant_e4m3(const double *a, int64_t n, float *scale, uint8_t *q)
     }
     float s = (float)(amax / 448.0);
     *scale = s;
-    for (int64_t i = 0; i < n; ++i) {
-        /* the rounding decision is taken on the single-precision quotient */
-        float v = s > 0.0f ? (float)a[i] / s : 0.0f;
-        q[i] = s > 0.0f ? oracle_f64_to_e4m3((double)v) : 0;
-    }
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = s > 0.0f ? oracle_f64_to_e4m3(a[i] / (double)s) : 0;
     return 0;
 }
 

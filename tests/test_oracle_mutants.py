@@ -201,9 +201,10 @@ PRODUCER_MUTANTS = {
     "e4m3_no_saturation": ("if (a >= 448.0)\n        return (uint8_t)(sign | 0x7E);", ""),
     "e4m3_subnormal_spacing": ("if (q < -6)\n        q = -6;", "if (q < -7)\n        q = -7;"),
     "scale_not_448": ("float s = (float)(amax / 448.0);", "float s = (float)(amax / 240.0);"),
-    "quant_drops_sign": ("float v = s > 0.0f ? (float)a[i] / s : 0.0f;", "float v = s > 0.0f ? (float)fabs(a[i]) / s : 0.0f;"),
-    "quant_decides_in_double": ("q[i] = s > 0.0f ? oracle_f64_to_e4m3((double)v) : 0;",
-                                "q[i] = s > 0.0f ? oracle_f64_to_e4m3(a[i] / (double)s) : 0;"),
+    "quant_drops_sign": ("q[i] = s > 0.0f ? oracle_f64_to_e4m3(a[i] / (double)s) : 0;",
+                         "q[i] = s > 0.0f ? oracle_f64_to_e4m3(fabs(a[i]) / (double)s) : 0;"),
+    "quant_decides_in_binary32": ("q[i] = s > 0.0f ? oracle_f64_to_e4m3(a[i] / (double)s) : 0;",
+                                  "q[i] = s > 0.0f ? oracle_f64_to_e4m3((double)((float)a[i] / s)) : 0;"),
 }
 
 

@@ -20,9 +20,9 @@ than itself:
   the kernels share;
 * quantisation: the largest |a| maps to code +-448, every code is the nearest
   one (the error is at most half the local spacing), the rounding decision is
-  taken on the binary32 quotient (values closer to a midpoint than binary32
-  resolves round as the midpoint), an all-zero input gives scale 0 and zero
-  codes.
+  taken on the exact quotient (values a hair off a midpoint, closer than
+  binary32 resolves, still round to their own side), an all-zero input gives
+  scale 0 and zero codes.
 
 ``producer_pin_failures(lib)`` runs them against a loaded oracle library; the
 planted-mistake tests run it against mutated copies of the oracle.
@@ -170,13 +170,17 @@ def producer_pin_failures(lib):
     allv = np.sort(np.concatenate([-vals, vals]))
     idx = np.clip(np.searchsorted(allv, v), 1, allv.size - 1)
     gap = allv[idx] - allv[idx - 1]
-    if not np.all(np.abs(dq - v) <= gap / 2 + 2.0 ** -23 * np.abs(v)):
+    if not np.all(np.abs(dq - v) <= gap / 2 + 1e-12 * np.abs(v)):
         bad.append("a code is not the nearest")
-    # the decision is taken on the binary32 quotient: a value a hair above a
-    # midpoint (closer than binary32 resolves) rounds as the midpoint does
+    # The decision is taken on the exact quotient (OCP FP8: round to nearest
+    # even of the value itself).  With max|a| = 448 the scale is exactly 1;
+    # 1.0625 is the midpoint of codes 1.0 (0x38) and 1.125 (0x39), 1.1875 that
+    # of 1.125 and 1.25 (0x3A).  A hair above the first rounds up and a hair
+    # below the second rounds down, although binary32 would see both as exact
+    # midpoints and round them to the even codes 0x38 and 0xBA.
     _, qt = _quant(lib, [448.0, 1.0625 * (1 + 2.0 ** -30), -1.1875 * (1 - 2.0 ** -30)])
-    if not np.array_equal(qt, np.array([0x7E, 0x38, 0xBA], np.uint8)):
-        bad.append("quantisation decision not taken in binary32")
+    if not np.array_equal(qt, np.array([0x7E, 0x39, 0xB9], np.uint8)):
+        bad.append("quantisation decision not taken on the exact quotient")
     s0, q0 = _quant(lib, np.zeros(10))
     if s0 != 0.0 or q0.any():
         bad.append("zero input does not give scale 0")

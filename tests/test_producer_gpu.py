@@ -2,20 +2,27 @@
 of the weight quantiser against the oracle, and of the composed FP8 path
 (producer, then the fused FP8 projection).
 
-The codes are integers decided by floating point; both sides decide on a
-binary32 quotient.  Plain quantisation of BF16 values computes the same
-quotient on both sides (one correctly rounded division), so its codes and
-scale must be bit-identical.  After RMSNorm the kernel's binary32 value of a
-differs from the oracle's by rounding, so the rule there is bit-exact codes
-except where that arithmetic may fall on the other side of a midpoint: an element may take the other of the two codes around
-a / s only when a / s (oracle, double) lies within a relative distance
-delta of their midpoint, with delta the FP32 error bound of the kernel's
-arithmetic: the sum of K squares over K/32 sequential terms per lane plus a
-5-level shuffle tree (relative error <= (K/32 + 5) u, u = 2^-24), halved by
-the square root, plus about ten correctly rounded operations on each side
-(division, square root, reciprocal, products, the scale's division by 448):
-delta = (K/32 + 32) u covers it with room.  The scale must agree within the
-same relative bound.
+The codes are integers decided by floating point.  The oracle decides on the
+exact quotient a / s (OCP 8-bit floating point: round to nearest even of the
+value); the kernels decide in binary32.  So codes must be bit-identical except
+where binary32 arithmetic may fall on the other side of a midpoint: an element
+may take the other of the two codes around a / s only when a / s (oracle,
+double) lies within a relative distance delta of their midpoint, with delta
+the FP32 error bound of the kernel's arithmetic.
+
+* Plain quantisation of BF16 values: the kernel's quotient is one correctly
+  rounded binary32 division of the same a and s, so delta = u = 2^-24, and the
+  scale (max|x| / 448, one correctly rounded division) must be bit-identical.
+  With BF16 inputs and a BF16 maximum, many quotients lie within u of a
+  midpoint, where binary32 sees an exact tie; those elements may take either
+  neighbour.
+* After RMSNorm the kernel's binary32 value of a also differs from the
+  oracle's by rounding: the sum of K squares over K/32 sequential terms per
+  lane plus a 5-level shuffle tree (relative error <= (K/32 + 5) u), halved
+  by the square root, plus about ten correctly rounded operations on each
+  side (division, square root, reciprocal, products, the scale's division by
+  448): delta = (K/32 + 32) u covers it with room.  The scale must agree
+  within the same relative bound.
 """
 import numpy as np
 import pytest
@@ -49,22 +56,20 @@ def _decode(q):
     return _DEC[q]
 
 
-def assert_codes(q_gpu, s_gpu, a_ref, K, what, exact=False):
+def assert_codes(q_gpu, s_gpu, a_ref, K, what, plain=False):
     """q_gpu: uint8 codes, s_gpu: float scale; a_ref: oracle values (double).
-    exact: the kernel's quotient is the oracle's (plain quantisation of BF16
-    values: one correctly rounded binary32 division on both sides), so scale
-    and codes must be bit-identical."""
+    plain: quantisation of BF16 values without normalisation (the kernel's
+    quotient is one correctly rounded binary32 division, its scale one
+    correctly rounded binary32 division of the exact maximum)."""
     s_ref, q_ref = oracle.quant_e4m3(a_ref)
-    if exact:
-        assert s_gpu == s_ref, f"{what}: scale {s_gpu} vs {s_ref}"
-        n_bad = int((q_gpu != q_ref).sum())
-        assert n_bad == 0, f"{what}: {n_bad} codes differ"
-        return
-    delta = (K / 32 + 32) * U
+    delta = U if plain else (K / 32 + 32) * U
     if s_ref == 0.0:
         assert s_gpu == 0.0 and not q_gpu.any(), what
         return
-    assert abs(s_gpu - s_ref) <= delta * s_ref, f"{what}: scale {s_gpu} vs {s_ref}"
+    if plain:
+        assert s_gpu == s_ref, f"{what}: scale {s_gpu} vs {s_ref}"
+    else:
+        assert abs(s_gpu - s_ref) <= delta * s_ref, f"{what}: scale {s_gpu} vs {s_ref}"
     bad = q_gpu != q_ref
     n_bad = int(bad.sum())
     if n_bad == 0:
@@ -77,10 +82,10 @@ def assert_codes(q_gpu, s_gpu, a_ref, K, what, exact=False):
     ok = neighbours & near_mid & (np.sign(lo) * np.sign(hi) >= 0)
     assert ok.all(), (f"{what}: {int((~ok).sum())} of {q_gpu.size} codes differ away from a midpoint; "
                       f"first at {np.argwhere(bad)[~ok][0]}: v={v[~ok][0]!r} gpu={hi[~ok][0]} ref={lo[~ok][0]}")
-    # Within a row every value is a BF16 input times one FP32 factor, so far
-    # more values sit on (or within rounding of) an exact midpoint than a
-    # continuous distribution would put there; the per-element rule above is
-    # the criterion, this only catches a wholesale shift.
+    # Every value is a BF16 input times one FP32 factor, so far more values
+    # sit within rounding of an exact midpoint than a continuous distribution
+    # would put there; the per-element rule above is the criterion, this only
+    # catches a wholesale shift.
     assert n_bad <= max(4, 0.02 * q_gpu.size), f"{what}: {n_bad} near-midpoint flips is too many"
 
 
@@ -122,7 +127,7 @@ def test_weight_quant(sg, shape):
     _, W1, _ = si.make_bf16(1, N, K, seed=N + K)
     Wt = W1.t().contiguous()                  # K-major [N,K], the FP8 entry points' layout
     q, s = sg.swiglu_quant_fp8(Wt.to(DEV))
-    assert_codes(si.bits_u8(q.cpu()), float(s.item()), Wt.double().numpy(), K, f"quant {shape}", exact=True)
+    assert_codes(si.bits_u8(q.cpu()), float(s.item()), Wt.double().numpy(), K, f"quant {shape}", plain=True)
 
 
 def test_edge_cases(sg):
@@ -171,7 +176,11 @@ def test_argument_errors(sg):
 @pytest.mark.parametrize("shape", [(200, 264, 272), (512, 18944, 3584)], ids=lambda s: "x".join(map(str, s)))
 def test_composed_fp8_path(sg, form, shape):
     """Producer on the GPU, then the fused FP8 projection, against the oracle's
-    own producer and FP8 definition; weights quantised on each side."""
+    own producer and FP8 definition.  The weights are quantised on both sides
+    and the GPU's codes checked against the oracle's; the projection then
+    takes the oracle's weight codes and scales as its inputs, so that a valid
+    near-midpoint flip in a weight code (binary32 ties, see the module
+    docstring) does not move a whole column of Y away from the reference."""
     M, N, K = shape
     X, gamma = si.make_producer_inputs(M, K, seed=40 + M)
     _, W1, W2 = si.make_bf16(1, N, K, seed=41 + N)
@@ -180,10 +189,6 @@ def test_composed_fp8_path(sg, form, shape):
     Aq, sA = sg.swiglu_rmsnorm_quant_fp8(Xd, gd, 1e-6)
     W1q, s1 = sg.swiglu_quant_fp8(W1t)
     W2q, s2 = sg.swiglu_quant_fp8(W2t)
-    if form == "separate":
-        Y = sg.swiglu_fused_fp8(Aq, W1q, W2q, sA, s1, s2)
-    else:
-        Y = sg.swiglu_fused_interleaved_fp8(Aq, sg.swiglu_pack_interleaved_fp8(W1q, W2q), sA, s1, s2)
     rc, detail = sg.swiglu_device_status()
     assert rc == sg.OK, (sg.status_string(rc), detail)
 
@@ -193,18 +198,25 @@ def test_composed_fp8_path(sg, form, shape):
     s2o, W2qo = oracle.quant_e4m3(W2.double().numpy())
     # The codes: equal to the oracle's except near-midpoint flips (validated here).
     a_gpu = si.bits_u8(Aq.cpu())
-    w1_gpu = si.bits_u8(W1q.cpu()).T
-    w2_gpu = si.bits_u8(W2q.cpu()).T
     assert_codes(a_gpu, float(sA.item()), oracle.rmsnorm_bf16(si.bits_u16(X), si.bits_u16(gamma), 1e-6), K, "A")
-    assert_codes(w1_gpu, float(s1.item()), W1.double().numpy(), K, "W1", exact=True)
-    assert_codes(w2_gpu, float(s2.item()), W2.double().numpy(), K, "W2", exact=True)
-    # Y: element by element wherever both sides quantised the row of A and the
-    # column of W1, W2 identically (a flipped code is a valid rounding, but it
-    # moves its whole row or column of Y by one code step's worth).
+    assert_codes(si.bits_u8(W1q.cpu()).T, float(s1.item()), W1.double().numpy(), K, "W1", plain=True)
+    assert_codes(si.bits_u8(W2q.cpu()).T, float(s2.item()), W2.double().numpy(), K, "W2", plain=True)
+    # The projection on the GPU's A codes and the oracle's weight codes.
+    to_dev = lambda q: torch.from_numpy(np.ascontiguousarray(q.T)).view(torch.float8_e4m3fn).to(DEV)
+    W1o, W2o = to_dev(W1qo), to_dev(W2qo)
+    s1d = torch.tensor([s1o], dtype=torch.float32, device=DEV)
+    s2d = torch.tensor([s2o], dtype=torch.float32, device=DEV)
+    if form == "separate":
+        Y = sg.swiglu_fused_fp8(Aq, W1o, W2o, sA, s1d, s2d)
+    else:
+        Y = sg.swiglu_fused_interleaved_fp8(Aq, sg.swiglu_pack_interleaved_fp8(W1o, W2o), sA, s1d, s2d)
+    rc, detail = sg.swiglu_device_status()
+    assert rc == sg.OK, (sg.status_string(rc), detail)
+    # Y: element by element on every row whose A codes both sides chose alike
+    # (a flipped code is a valid rounding, but it moves its whole row of Y by
+    # one code step's worth).
     ref = oracle.swiglu_e4m3(Aqo, W1qo, W2qo, sAo, s1o, s2o, rows=rows)
     got = Y.double().cpu().numpy()[rows]
     same_rows = (a_gpu[rows] == Aqo[rows]).all(axis=1)
-    same_cols = (w1_gpu == W1qo).all(axis=0) & (w2_gpu == W2qo).all(axis=0)
-    assert same_rows.mean() > 0.9 and same_cols.mean() > 0.9
-    oracle.assert_parity(got[same_rows][:, same_cols], ref[same_rows][:, same_cols],
-                         f"rmsnorm+quant+fp8 {form} {shape}")
+    assert same_rows.mean() > 0.9
+    oracle.assert_parity(got[same_rows], ref[same_rows], f"rmsnorm+quant+fp8 {form} {shape}")
