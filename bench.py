@@ -1,17 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the fused SwiGLU projection on GB300.
 
-One step = the whole hot path over the Qwen-2.5-0.5B MLP workload
-(K=896, N=4864, M in {128, 512, 2048, 8192}), each M in both weight forms
-(separate W1/W2 and interleaved W_fused): eight fused-kernel launches.
-Metric: TFLOP/s = sum(4*M*N*K) / time.
+One step = the whole hot path over the Qwen-2.5-72B MLP workload
+(K=8192, N=29568, M in {2048, 8192, 16384}), each M in both weight forms
+(separate W1/W2 and interleaved W_fused): six fused-kernel launches.
+Metric: TFLOP/s = sum(4*M*N*K) / time.  ``--workload`` selects the other
+configurations (Qwen-2.5-0.5B and 7B, FP8, weight formats, the MLP block).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  ``value`` is device time of K back-to-back
 replays of a CUDA graph of the step, inputs resident in HBM; each call reads
 its own copy of the weights and its own A and writes its own Y, so every
-step touches ~390 MB (3x the 129 MB L2) and no call finds its inputs in L2.
+step touches ~9.9 GB at 72B (~390 MB at 0.5B, 3x the 129 MB L2) and no call
+finds its inputs in L2.
 ``e2e`` repeats the step through the public Python API with A copied in
 from pinned host memory and Y copied back every step.  ``--impl reference``
 times the CPU oracle (the deliberately slow reference arm) on a bounded
@@ -60,7 +62,7 @@ WORKLOADS = {
     "qwen2.5-0.5b-mlp": (896, 4864, (128, 512, 2048, 8192), 1),
     "qwen2.5-7b-mlp": (3584, 18944, (256, 1024, 4096), 2),
 }
-DEFAULT_WORKLOAD = "qwen2.5-0.5b"
+DEFAULT_WORKLOAD = "qwen2.5-72b"
 RMS_EPS = 1e-6   # RMSNorm epsilon of the producer workload (Qwen-2.5's value)
 W4_GROUP = 128   # K rows per INT4 scale group
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -134,7 +136,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception as e:  # no nvidia-smi: report what we have
             log(f"clock sampling unavailable: {e}")
             self.proc = None
@@ -438,15 +440,16 @@ class Workload:
             fn()
 
 
-def measure_calls(wl, stream, launches, factory=None):
+def measure_calls(wl, stream, launches, factory=None, pairs=None):
     """Average duration (us) of each call of the step, launched alone and back
     to back inside a CUDA graph, rotating over copies of its inputs so that
     the copies together exceed 2.5x the L2 size.  ``factory(form, M, v, bufs)``
-    builds the launch closure (default: the fused call through the C ABI)."""
+    builds the launch closure (default: the fused call through the C ABI);
+    ``pairs`` ((form, M, v), bufs) defaults to every call of the step."""
     import torch
     factory = factory or wl.launcher
     out = []
-    for (form, M, v), bufs in zip(wl.calls, wl.buffers):
+    for (form, M, v), bufs in (pairs or list(zip(wl.calls, wl.buffers))):
         per = wl.algorithmic_bytes(M)
         ncopy = max(2, min(24, math.ceil(2.5 * L2_BYTES / per)))
         copies = [bufs] + [tuple(t.clone() for t in bufs) for _ in range(ncopy - 1)]
@@ -592,6 +595,11 @@ def run_ours(args, ws, rank, local):
         roof = {"bound": "hbm", "achieved": dk["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(dk["gbs"] / peaks["hbm_gbs"], 4)}
     roof["traffic"] = load_traffic(kernel_key)
+    roof["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu "
+                            "capture of this kernel on the current sources (null otherwise); "
+                            "output bytes still dirty in L2 when the kernel ends are not yet "
+                            "written to DRAM and are not counted, so traffic can fall below the "
+                            "algorithmic bytes")
     roof["kernel"] = kernel_key
     roof["algorithmic_per_launch"] = (wl.flops_of(M) if dk["bound"] == "tensor"
                                       else wl.producer_bytes(M) if dk["variant"] == "rmsnorm_quant"
@@ -703,38 +711,42 @@ def run_e2e(args, wl, stream, ws):
                     "(pinned host memory), copies and kernels pipelined over three streams"}
 
 
-def unfused_fn(wl, form):
+def unfused_fn(wl):
     """The unfused computation of one call in plain torch: the gate and up
-    products as separate cuBLAS GEMMs (one GEMM on W_fused for the
-    interleaved form), then SiLU and the product as separate kernels."""
-    import torch
+    products as two cuBLAS GEMMs on the separate weights, then SiLU and the
+    product as separate kernels.  It is the common baseline of both fused
+    forms (one GEMM on W_fused followed by strided SiLU and product slices is
+    slower than the two GEMMs, so it would flatter the interleaved form)."""
     import torch.nn.functional as F
     if wl.kind == "mlp":
         return lambda A, W1, W2, W3: (F.silu(A @ W1) * (A @ W2)) @ W3
-    if form == "separate":
-        return lambda A, W1, W2: F.silu(A @ W1) * (A @ W2)
-
-    def interleaved(A, Wf):
-        D = A @ Wf
-        return F.silu(D[:, 0::2]) * D[:, 1::2]
-    return interleaved
+    return lambda A, W1, W2: F.silu(A @ W1) * (A @ W2)
 
 
 def unfused_factory(wl, compiled=False):
     """Launch-closure factory for measure_calls running the unfused path
-    (eager, or the torch.compile'd version of the same function).  The result
-    goes to a tensor the graph's memory pool provides, as in a model."""
+    (eager, or the torch.compile'd version of the same function) on the
+    separate-form buffers of a call.  The result goes to a tensor the graph's
+    memory pool provides, as in a model."""
     import torch
-    fns = {}
+    f = unfused_fn(wl)
+    if compiled:
+        f = torch.compile(f, dynamic=False, fullgraph=True)
 
     def factory(form, M, v, bufs):
-        if form not in fns:
-            f = unfused_fn(wl, form)
-            fns[form] = torch.compile(f, dynamic=False, fullgraph=True) if compiled else f
-        f = fns[form]
-        ins = bufs[:4] if wl.kind == "mlp" else bufs[:3] if form == "separate" else bufs[:2]
+        ins = bufs[:4] if wl.kind == "mlp" else bufs[:3]
         return lambda: f(*ins)
     return factory
+
+
+def unfused_pairs(wl):
+    """One ((form, M, v), bufs) per distinct M, on separate-form (or MLP)
+    buffers: the unfused baseline is timed once per M and serves both forms."""
+    seen = {}
+    for (form, M, v), bufs in zip(wl.calls, wl.buffers):
+        if form in ("separate", "mlp") and M not in seen:
+            seen[M] = ((form, M, v), bufs)
+    return seen
 
 
 def fusion_report(wl, fused_us, eager_us, hbm_gbs):
@@ -765,9 +777,15 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
     if wl.fp8 or wl.kind in ("w4", "mx"):
         return None
     factory = unfused_factory(wl)
-    eager_us = measure_calls(wl, stream, args.call_launches, factory)
+    base = unfused_pairs(wl)
+    if any(M not in base for (_, M, _) in wl.calls):
+        return None   # a step restricted to interleaved calls has no baseline buffers
+    by_m = dict(zip(base, measure_calls(wl, stream, args.call_launches, factory,
+                                        list(base.values()))))
+    eager_us = [by_m[M] for (_, M, _) in wl.calls]
 
-    fns = [factory(form, M, v, bufs) for (form, M, v), bufs in zip(wl.calls, wl.buffers)]
+    # the eager step: every call of the fused step replaced by the two-GEMM path
+    fns = [factory(*base[M]) for (_, M, _) in wl.calls]
 
     def step():
         for f in fns:
@@ -787,8 +805,8 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
     what = ("torch eager: (silu(A@W1) * (A@W2)) @ W3 (cuBLAS)" if wl.kind == "mlp" else
-            "torch eager: A@W1, A@W2 (cuBLAS; one A@W_fused GEMM for the interleaved form), "
-            "silu, mul")
+            "torch eager: A@W1, A@W2 (two cuBLAS GEMMs on the separate weights), silu, mul; "
+            "the common baseline of both fused forms")
     out = {"eager": {"what": what, "ms_per_step": round(ms, 5),
                      "tflops": round(wl.flops / (ms * 1e-3) / 1e12, 2),
                      "per_call_us": [round(u, 3) for u in eager_us]},
@@ -805,10 +823,14 @@ def run_compile_context(args, wl, stream, fused_us):
     if "TRITON_PTXAS_PATH" not in os.environ and os.path.exists("/usr/local/cuda/bin/ptxas"):
         os.environ["TRITON_PTXAS_PATH"] = "/usr/local/cuda/bin/ptxas"
     t0 = time.time()
+    base = unfused_pairs(wl)
     try:
-        comp_us = measure_calls(wl, stream, args.call_launches, unfused_factory(wl, compiled=True))
+        by_m = dict(zip(base, measure_calls(wl, stream, args.call_launches,
+                                            unfused_factory(wl, compiled=True),
+                                            list(base.values()))))
     except Exception as e:  # report, do not fail the benchmark line
         return {"error": f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"}
+    comp_us = [by_m[M] for (_, M, _) in wl.calls]
     return {"what": f"torch.compile(fullgraph=True, dynamic=False) of the eager function, "
                     f"torch {torch.__version__}",
             "compile_and_time_s": round(time.time() - t0, 1),
@@ -983,8 +1005,8 @@ def run_reference(args, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", default="auto",

@@ -282,7 +282,8 @@ int swiglu_mlp(const void *A, const void *W1, const void *W2, const void *W3, co
  *     and otherwise the down projection runs without splitting K;
  *   - the first call on a device looks up the area's device address, a
  *     host-side set-up step; make that first call before any stream capture
- *     that would include it;
+ *     that would include it.  The address is kept per device and looked up
+ *     again when the device's context changes (after cudaDeviceReset);
  *   - all calls on a device share the one area, which keeps what the last call
  *     left in it; nothing in it needs to start at zero (each call writes all
  *     it later reads), but calls whose GPU work overlaps in time (unordered

@@ -269,7 +269,28 @@ def mlp_bf16(A, W1, W2, W3, R=None, rows=None, with_y: bool = False):
     return (Z, Y) if with_y else Z
 
 
-from .check import parity_report, assert_parity  # noqa: E402,F401
+from .check import parity_report, assert_parity, bf16_rounding_slack  # noqa: E402,F401
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Decode an array of BF16 bit patterns (exact)."""
+    b = _u16(bits)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def mlp_rounding_slack(A, W1, W2, W3, rows=None) -> np.ndarray:
+    """Per element of the MLP block's Z [nrows, H]: how far Z may move when
+    every element of Y whose exact value lies within the kernel's FP32 error
+    bound of a BF16 rounding midpoint rounds to the other neighbour:
+    sum over f of slack(Y[m,f]) * |W3[f,h]| (``bf16_rounding_slack``).  G, U
+    and Y come from the definition; the sums of absolute products from the
+    definition on the inputs' absolute values (sign bits cleared)."""
+    A, W1, W2, W3 = _u16(A), _u16(W1), _u16(W2), _u16(W3)
+    G, U, Y = swiglu_bf16(A, W1, W2, rows=rows, with_gate_up=True)
+    clear = lambda b: np.ascontiguousarray(b & np.uint16(0x7FFF))
+    Ga, Ua, _ = swiglu_bf16(clear(A), clear(W1), clear(W2), rows=rows, with_gate_up=True)
+    s = bf16_rounding_slack(Y, G, U, Ga, Ua, A.shape[1])
+    return s @ np.abs(bf16_bits_to_f64(W3))
 
 
 # ---- the producer: RMSNorm and per-tensor E4M3 quantisation ----------------

@@ -12,6 +12,7 @@ PyTorch supplies device memory and the current CUDA stream.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -112,6 +113,24 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _on_tensor_device(fn):
+    """Run an entry point with the tensors' CUDA device current (the library
+    works on the current device: its launches, per-device state and the
+    no-allocation scratch area); all tensor arguments must share one device."""
+    @functools.wraps(fn)
+    def call(*args, **kw):
+        import torch
+        ts = [a for a in list(args) + list(kw.values()) if isinstance(a, torch.Tensor)]
+        devs = {t.device for t in ts}
+        if len(devs) > 1:
+            raise ValueError(f"{fn.__name__}: tensors on several devices: {sorted(map(str, devs))}")
+        if ts and ts[0].is_cuda:
+            with torch.cuda.device(ts[0].device):
+                return fn(*args, **kw)
+        return fn(*args, **kw)
+    return call
+
+
 def _need(t, name, dtype=None, ndim=2):
     import torch
     if not isinstance(t, torch.Tensor):
@@ -125,6 +144,7 @@ def _need(t, name, dtype=None, ndim=2):
     return t
 
 
+@_on_tensor_device
 def swiglu_fused(A, W1, W2, Y=None, *, variant: int = VARIANT_AUTO, stream=None):
     """Y = SiLU(A @ W1) * (A @ W2) with separate [K,N] weights; returns Y."""
     import torch
@@ -146,6 +166,7 @@ def swiglu_fused(A, W1, W2, Y=None, *, variant: int = VARIANT_AUTO, stream=None)
     return Y
 
 
+@_on_tensor_device
 def swiglu_fused_interleaved(A, Wfused, Y=None, *, variant: int = VARIANT_AUTO, stream=None):
     """Y[m,n] = SiLU(D[m,2n]) * D[m,2n+1] with D = A @ Wfused, Wfused [K,2N]; returns Y."""
     import torch
@@ -167,6 +188,7 @@ def swiglu_fused_interleaved(A, Wfused, Y=None, *, variant: int = VARIANT_AUTO, 
     return Y
 
 
+@_on_tensor_device
 def swiglu_pack_interleaved(W1, W2, Wfused=None, *, stream=None):
     """Wfused[k,2n] = W1[k,n], Wfused[k,2n+1] = W2[k,n]; returns Wfused [K,2N]."""
     import torch
@@ -198,6 +220,7 @@ def _scale(s, name):
     return s.data_ptr()
 
 
+@_on_tensor_device
 def swiglu_fused_fp8(Aq, W1t, W2t, sA, sW1, sW2, Y=None, *, stream=None):
     """Y = SiLU(sA*sW1 * Aq@W1t.T) * (sA*sW2 * Aq@W2t.T); Aq [M,K], W1t/W2t [N,K] E4M3."""
     import torch
@@ -219,6 +242,7 @@ def swiglu_fused_fp8(Aq, W1t, W2t, sA, sW1, sW2, Y=None, *, stream=None):
     return Y
 
 
+@_on_tensor_device
 def swiglu_fused_interleaved_fp8(Aq, Wfused_t, sA, sW1, sW2, Y=None, *, stream=None):
     """FP8 interleaved form: Wfused_t [2N,K] (even rows gate, odd rows up)."""
     import torch
@@ -240,6 +264,7 @@ def swiglu_fused_interleaved_fp8(Aq, Wfused_t, sA, sW1, sW2, Y=None, *, stream=N
     return Y
 
 
+@_on_tensor_device
 def swiglu_pack_interleaved_fp8(W1t, W2t, Wfused_t=None, *, stream=None):
     """Wfused_t[2n,:] = W1t[n,:], Wfused_t[2n+1,:] = W2t[n,:] (E4M3, K-major)."""
     import torch
@@ -272,6 +297,7 @@ def _quant_outputs(X, Xq, s):
     return Xq, s
 
 
+@_on_tensor_device
 def swiglu_rmsnorm_quant_fp8(X, gamma=None, eps: float = 1e-6, Aq=None, sA=None, *, stream=None):
     """RMSNorm of the rows of X (BF16 [M,K], gamma BF16 [K] or None) then
     per-tensor E4M3 quantisation; returns (Aq, sA) for swiglu_fused_fp8."""
@@ -290,6 +316,7 @@ def swiglu_rmsnorm_quant_fp8(X, gamma=None, eps: float = 1e-6, Aq=None, sA=None,
     return Aq, sA
 
 
+@_on_tensor_device
 def swiglu_quant_fp8(X, Xq=None, s=None, *, stream=None):
     """Per-tensor E4M3 quantisation of a BF16 [M,K] matrix; returns (Xq, s)."""
     import torch
@@ -301,6 +328,7 @@ def swiglu_quant_fp8(X, Xq=None, s=None, *, stream=None):
     return Xq, s
 
 
+@_on_tensor_device
 def swiglu_fused_w4(A, W1q, S1, W2q, S2, Y=None, *, group: int = 128, stream=None):
     """Y = SiLU(A @ W1) * (A @ W2) with INT4 weights: W1q/W2q uint8 [K, N/2]
     (two codes per byte along N), S1/S2 BF16 [K/group, N]."""
@@ -335,6 +363,7 @@ def _out(A, N, Y):
     return Y
 
 
+@_on_tensor_device
 def swiglu_fused_mxfp8(A, C1, S1, C2, S2, Y=None, *, stream=None):
     """Y = SiLU(A @ W1) * (A @ W2), W = E4M3(C) * 2^(S - 127) per 32 K rows:
     C1/C2 uint8 [K,N], S1/S2 uint8 [K/32,N]."""
@@ -353,6 +382,7 @@ def swiglu_fused_mxfp8(A, C1, S1, C2, S2, Y=None, *, stream=None):
     return Y
 
 
+@_on_tensor_device
 def swiglu_fused_nvfp4(A, C1, S1, g1, C2, S2, g2, Y=None, *, stream=None):
     """Y = SiLU(A @ W1) * (A @ W2), W = E2M1(C) * E4M3(S) * g per 16 K rows:
     C1/C2 uint8 [K,N/2] (two codes per byte), S1/S2 uint8 [K/16,N] E4M3,
@@ -382,6 +412,7 @@ def _workspace(nbytes, device, workspace):
     return workspace, workspace.numel() * workspace.element_size()
 
 
+@_on_tensor_device
 def swiglu_linear(X, W, R=None, Z=None, *, workspace=None, stream=None):
     """Z = X @ W (+ R); X [M,K], W [K,N], R [M,N] or None; BF16.
 
@@ -412,6 +443,7 @@ def swiglu_linear(X, W, R=None, Z=None, *, workspace=None, stream=None):
     return Z
 
 
+@_on_tensor_device
 def swiglu_mlp(A, W1, W2, W3, R=None, Z=None, *, workspace=None, stream=None):
     """Z = BF16(SiLU(A @ W1) * (A @ W2)) @ W3 (+ R); A [M,H], W1/W2 [H,F], W3 [F,H]."""
     import torch
@@ -436,6 +468,7 @@ def swiglu_mlp(A, W1, W2, W3, R=None, Z=None, *, workspace=None, stream=None):
     return Z
 
 
+@_on_tensor_device
 def swiglu_mlp_noalloc(A, W1, W2, W3, R, Z, *, stream=None):
     """swiglu_mlp without any device allocation, for callers that may not
     allocate: Y lives in the library's fixed 32 MiB scratch area.  Z must be

@@ -1,6 +1,4 @@
 // k_bf16_sk.cu -- the split-K cluster kernel for small M, both weight forms.
-#include <atomic>
-
 #include "launch.h"
 #include "swiglu_sk_kernel.cuh"
 
@@ -9,14 +7,13 @@ namespace {
 
 template <class C>
 cudaError_t launch_sk(const LaunchArgs &la) {
-  static std::atomic<uint64_t> configured{0};
-  const uint64_t bit = 1ull << (la.device & 63);
+  static PerDeviceOnce once;
   auto kern = swiglu_bf16_sk_kernel<C>;
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
+  if (once.needed(la.device, la.ctx_gen)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    once.done(la.device, la.ctx_gen);
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];

@@ -338,20 +338,19 @@ __global__ void __launch_bounds__(kSmemThreads) rows_smem_kernel(
 template <bool NORM, bool GAMMA>
 cudaError_t launch_rows_smem(const void *X, const uint4 *g, float eps, void *Q, float *s,
                              int64_t M, int K, uint32_t *err, uint64_t timeout_ns,
-                             cudaStream_t st) {
-  static std::atomic<uint64_t> configured{0};
+                             uint64_t ctx_gen, cudaStream_t st) {
+  static PerDeviceOnce once;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
+  if (once.needed(dev, ctx_gen)) {
     e = cudaFuncSetAttribute(rows_smem_kernel<NORM, GAMMA, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMaxBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(rows_smem_kernel<NORM, GAMMA, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMaxBytes);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    once.done(dev, ctx_gen);
   }
   const int64_t blocks = (M + kSmemRows - 1) / kSmemRows;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
@@ -385,11 +384,11 @@ cudaError_t launch_producer(const void *X, const void *gamma, float eps, void *Q
                             int64_t M, int K, cudaStream_t st) {
   uint32_t *err = nullptr;
   int sms = 0;
-  uint64_t timeout_ns = 0;
-  if (device_info(&err, &sms, &timeout_ns) != SWIGLU_OK) return cudaErrorUnknown;
+  uint64_t timeout_ns = 0, ctx_gen = 0;
+  if (device_info(&err, &sms, &timeout_ns, &ctx_gen) != SWIGLU_OK) return cudaErrorUnknown;
   if (M > 0 && int64_t(kSmemRows) * K * 2 <= kSmemMaxBytes)
     return launch_rows_smem<NORM, GAMMA>(X, static_cast<const uint4 *>(gamma), eps, Q, s, M, K,
-                                         err, timeout_ns, st);
+                                         err, timeout_ns, ctx_gen, st);
   cudaError_t e = cudaMemsetAsync(s, 0, sizeof(float), st);
   if (e != cudaSuccess || M == 0) return e;
   // longer rows: the loop kernels

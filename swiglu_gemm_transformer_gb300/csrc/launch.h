@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "swiglu_tc_kernel.cuh"
 #include "tc_common.cuh"
 
@@ -17,7 +19,26 @@ struct LaunchArgs {
   KParams p;
   int grid;
   int device;
+  // Generation of the device's context the call runs in: it changes when the
+  // context is replaced (e.g. after cudaDeviceReset), which drops every
+  // function attribute set on the old one.
+  uint64_t ctx_gen;
   cudaStream_t stream;
+};
+
+// One-time launch set-up per device (function attributes such as the
+// dynamic shared-memory opt-in), redone when the device's context changes.
+// Objects of this class live in static storage (zero-initialised);
+// generations start at 1.
+class PerDeviceOnce {
+ public:
+  bool needed(int device, uint64_t gen) const {
+    return gen_[device & 63].load(std::memory_order_acquire) != gen;
+  }
+  void done(int device, uint64_t gen) { gen_[device & 63].store(gen, std::memory_order_release); }
+
+ private:
+  std::atomic<uint64_t> gen_[64];
 };
 
 // Tile geometry of each BF16 variant (SWIGLU_VARIANT_*), for host-side planning.
@@ -39,7 +60,7 @@ cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la);
 // wf: 1 INT4, 2 MXFP8, 3 NVFP4 (weight_decode.cuh); m_blocks: 128-row blocks
 // per CTA (1, or 2 with la.p.num_m_blk counting 256-row blocks)
 cudaError_t launch_dq_kernel(int wf, int m_blocks, const LaunchArgs &la);
-int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns);
+int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *ctx_gen);
 cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf, int64_t n_elems,
                                         int sm_count, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t *err, cudaStream_t s);

@@ -1,8 +1,6 @@
 // launch_tc.cuh -- one launcher per tcgen05 kernel configuration.
 #pragma once
 
-#include <atomic>
-
 #include "launch.h"
 #include "swiglu_tc2_kernel.cuh"
 
@@ -19,14 +17,13 @@ inline void pdl_attr(cudaLaunchAttribute &a) {
 template <class C>
 cudaError_t launch_tc(const LaunchArgs &la) {
   // Per-device one-time set-up: the dynamic shared-memory opt-in.
-  static std::atomic<uint64_t> configured{0};
-  const uint64_t bit = 1ull << (la.device & 63);
+  static PerDeviceOnce once;
   auto kern = swiglu_bf16_tc_kernel<C>;
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
+  if (once.needed(la.device, la.ctx_gen)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    once.done(la.device, la.ctx_gen);
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
@@ -44,9 +41,8 @@ cudaError_t launch_tc(const LaunchArgs &la) {
 // resident at once (queried once per device).
 template <class C>
 cudaError_t launch_pair(const LaunchArgs &la) {
-  static std::atomic<uint64_t> configured{0};
+  static PerDeviceOnce once;
   static int max_clusters[64] = {0};
-  const uint64_t bit = 1ull << (la.device & 63);
   auto kern = swiglu_bf16_pair_kernel<C>;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
@@ -60,7 +56,7 @@ cudaError_t launch_pair(const LaunchArgs &la) {
   cfg.stream = la.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
+  if (once.needed(la.device, la.ctx_gen)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -70,7 +66,7 @@ cudaError_t launch_pair(const LaunchArgs &la) {
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_clusters[la.device & 63] = n;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    once.done(la.device, la.ctx_gen);
   }
   // work units: output tiles x K slices
   const int64_t tiles =

@@ -28,6 +28,11 @@ struct DeviceState {
   int status = SWIGLU_OK;  // sticky result of the one-time set-up
   int sm_count = 0;
   uint32_t *err = nullptr;
+  // The context the set-up was done in (driver context id, 0 if unknown) and
+  // its generation number: a new context on the device (after
+  // cudaDeviceReset) gets a new generation, and the set-up is redone.
+  unsigned long long ctx_id = 0;
+  uint64_t gen = 0;
 };
 
 constexpr int kMaxDevices = 64;
@@ -39,6 +44,33 @@ std::atomic<int> g_weights_read_only{0};
 // SWIGLU_LINEAR_N environment variable, read once, sets it for tuning sweeps).
 std::atomic<int> g_linear_n{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+uint64_t g_next_gen = 1;  // guarded by g_mu
+
+void *driver_entry(const char *name, int version) {
+  cudaDriverEntryPointQueryResult q;
+  void *fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return fn;
+}
+
+// Process-unique id of the calling thread's current context; 0 when none is
+// current or the driver offers no id.
+unsigned long long current_ctx_id() {
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current && g_ctx_get_id && g_ctx_current(&c) == CUDA_SUCCESS && c != nullptr &&
+      g_ctx_get_id(c, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
 
 int device_state(DeviceState **out, int *dev_out) {
   int dev = -1;
@@ -48,8 +80,15 @@ int device_state(DeviceState **out, int *dev_out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(
+        driver_entry("cuTensorMapEncodeTiled", 12000));
+    if (!g_encode) return SWIGLU_ERR_CUDA;
+    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent", 4000));
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId", 12000));
+  }
   DeviceState &st = g_dev[dev];
-  if (!st.ready) {
+  if (!st.ready || current_ctx_id() != st.ctx_id) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -59,22 +98,15 @@ int device_state(DeviceState **out, int *dev_out) {
     }
     // The kernels are built for sm_103a only (arch-specific tcgen05 code).
     if (major != 10 || minor != 3) return SWIGLU_ERR_UNSUPPORTED;
+    // (also makes the device's primary context current on this thread)
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err), g_swiglu_err_word) !=
         cudaSuccess) {
       cudaGetLastError();
       return SWIGLU_ERR_CUDA;
     }
-    if (!g_encode) {
-      cudaDriverEntryPointQueryResult q;
-      void *fn = nullptr;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr) {
-        cudaGetLastError();
-        return SWIGLU_ERR_CUDA;
-      }
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    const unsigned long long id = current_ctx_id();
+    if (!st.ready || id != st.ctx_id) st.gen = g_next_gen++;
+    st.ctx_id = id;
     st.sm_count = sms;
     st.ready = true;
     if (const char *e = std::getenv("SWIGLU_LINEAR_N")) {
@@ -220,6 +252,7 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   if (tiles > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   la.grid = int(tiles < st->sm_count ? tiles : st->sm_count);  // one-CTA kernels
   la.device = dev;
+  la.ctx_gen = st->gen;
   la.stream = s;
   cudaError_t e = variant == SWIGLU_VARIANT_1SM_N64_SK2 ? launch_bf16_sk(interleaved, la)
                   : interleaved ? launch_bf16_interleaved(variant, la)
@@ -292,6 +325,7 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   p.w4_group = int32_t(G);
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
+  la.ctx_gen = st->gen;
   la.stream = s;
   const cudaError_t e = wide ? launch_dq_kernel(1, m_blocks, la) : launch_w4_sk(la);
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
@@ -367,6 +401,7 @@ int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const floa
   p.sW2 = g2;
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim / 2) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
+  la.ctx_gen = st->gen;
   la.stream = s;
   const cudaError_t e = wide ? launch_dq_kernel(nvfp4 ? 3 : 2, m_blocks, la) : launch_mx_sk(nvfp4, la);
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
@@ -437,6 +472,7 @@ int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, cons
   p.kb_per_split = p.num_k_blk;
   if (int64_t(p.num_m_blk) * p.num_n_blk > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
+  la.ctx_gen = st->gen;
   la.stream = s;
   return launch_fp8(interleaved, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
@@ -542,6 +578,7 @@ int run_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, 
   p.kb_per_split = pl.kb_per;
   if (int64_t(p.num_m_blk) * p.num_n_blk * p.k_splits > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   la.device = dev;
+  la.ctx_gen = st->gen;
   la.stream = s;
   if (launch_linear(pl.lin_n, la) != cudaSuccess) return SWIGLU_ERR_CUDA;
   if (pl.k_splits > 1 &&
@@ -570,9 +607,10 @@ VariantGeom variant_geom(int variant, bool interleaved) {
   }
 }
 
-// This device's error word, SM count and wait limit, for kernels launched
-// from other translation units (one-time per-device set-up on first use).
-int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns) {
+// This device's error word, SM count, wait limit and context generation, for
+// kernels launched from other translation units (per-device set-up on first
+// use, redone when the device's context changes).
+int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *ctx_gen) {
   DeviceState *st = nullptr;
   int dev = -1;
   int rc = device_state(&st, &dev);
@@ -580,6 +618,7 @@ int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns) {
   *err = st->err;
   *sm_count = st->sm_count;
   *timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  *ctx_gen = st->gen;
   return SWIGLU_OK;
 }
 

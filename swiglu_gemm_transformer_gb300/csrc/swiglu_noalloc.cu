@@ -16,6 +16,12 @@
 
 #include "swiglu.h"
 
+namespace swiglu {
+// The device's error word, SM count, wait limit and context generation
+// (swiglu_api.cu); the generation changes when the device's context does.
+int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *ctx_gen);
+}  // namespace swiglu
+
 namespace {
 
 // The scratch area: part of the library's device code, so every GPU the
@@ -26,10 +32,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
+uint64_t g_scratch_gen[kMaxDevices] = {0};  // context generation the address belongs to
 
 // Device address of the scratch area on the current device.  In host code the
 // array's name only stands in for it, so the address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached; a new context on the device
+// (after cudaDeviceReset) reloads the library's device code, so the lookup
+// is redone then.
 int scratch_on_current_device(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -37,14 +46,20 @@ int scratch_on_current_device(void **out) {
     return SWIGLU_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_UNSUPPORTED;
+  uint32_t *err = nullptr;
+  int sms = 0;
+  uint64_t timeout_ns = 0, gen = 0;
+  int rc = swiglu::device_info(&err, &sms, &timeout_ns, &gen);
+  if (rc != SWIGLU_OK) return rc;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_gen[dev] != gen) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return SWIGLU_ERR_CUDA;
     }
     g_scratch_ptr[dev] = p;
+    g_scratch_gen[dev] = gen;
   }
   *out = g_scratch_ptr[dev];
   return SWIGLU_OK;

@@ -5,20 +5,13 @@ element (small shapes) or on sampled rows (Qwen-2.5 shapes).
 The down projection uses the same acceptance rule as the fused projection.
 The MLP block rounds Y to BF16 in between; the kernel rounds from an FP32
 value and the oracle from the exact value, so near a rounding midpoint they
-may pick neighbouring BF16 values (both correct roundings).  Bound on how
-often that shows up in Z:
-  * the kernel's y carries a relative error of about three FP32 ulps
-    (eps ~ 1.8e-7: the FP32 accumulator's rounding and the fast exponential);
-  * a BF16 spacing is 2^-8..2^-7 of |y| (2^-7.5 on average), so a flip
-    happens with probability p ~ 2 eps 2^7.5 ~ 6.5e-5 per Y element;
-  * a flip moves y by one spacing; over F terms the spread of Z relative to
-    rms(Z) is r ~ sqrt(p) 2^-7.5 ~ 4.4e-5;
-  * for Gaussian-like Z, the share of elements with |Z| > 1e-2 rms(Z) whose
-    error exceeds 1 % of |Z| is about 64 r ~ 0.3 %.
-The MLP tests keep bound (1) on every element and allow at most 1 % of the
-significant elements over 1 % relative error (3x the estimate; the pages'
-cuBLAS baseline with BF16 intermediates shows 4.5-11 %, section "Contributi
-Chiave", item 3).
+may pick neighbouring BF16 values (both correct roundings), and such a flip
+moves every element of its row of Z by up to spacing * |W3[f,h]|.  The MLP
+tests keep bound (1) on every element, and every significant element must
+meet the 1 % rule (2) widened by its own slack: the sum over the Y elements
+of its row that lie within the kernel's error of a midpoint of that
+element's possible move (oracle.mlp_rounding_slack; the error model is in
+oracle.check.bf16_rounding_slack).  No element is exempt.
 """
 import numpy as np
 import pytest
@@ -89,8 +82,6 @@ def test_linear_split_matches_unsplit(sg):
     oracle.assert_parity(Z1.float().cpu().numpy(), Z2.double().cpu().numpy(), "split vs unsplit")
 
 
-MLP_SIG_MISMATCH = 1e-2  # derived in the module docstring
-
 MLP_CASES = [
     # (name, M, H, F, seed, residual)
     ("tiny", 7, 64, 136, 5, True),
@@ -112,8 +103,8 @@ def test_mlp(sg, case):
     Z = sg.swiglu_mlp(A.to(DEV), W1.to(DEV), W2.to(DEV), W3.to(DEV), R.to(DEV) if with_r else None)
     _status(sg)
     rows = None if M <= 512 else si.sample_rows(M, 128, 32, seed)
-    ref = oracle.mlp_bf16(si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2), si.bits_u16(W3),
-                          si.bits_u16(R) if with_r else None, rows=rows)
+    bits = [si.bits_u16(t) for t in (A, W1, W2, W3)]
+    ref = oracle.mlp_bf16(*bits, si.bits_u16(R) if with_r else None, rows=rows)
+    slack = oracle.mlp_rounding_slack(*bits, rows=rows)
     z = Z.float().cpu().numpy()
-    oracle.assert_parity(z if rows is None else z[rows], ref, f"mlp {name}",
-                         max_sig_mismatch_frac=MLP_SIG_MISMATCH)
+    oracle.assert_parity(z if rows is None else z[rows], ref, f"mlp {name}", sig_slack=slack)

@@ -42,6 +42,51 @@ def test_bf16_rounding_exact_on_doubles():
     assert oracle.f64_to_bf16(3 * 2.0 ** -134) == 0x0002         # tie to even (up)
 
 
+def test_rounding_slack_flags_only_values_near_a_midpoint():
+    # g = 40.x, u = 1: y = SiLU(g) = g to double precision.  BF16 values in
+    # [32, 64) are 2^-2 apart, so 40.125 is a rounding midpoint.  With K = 1,
+    # Gabs = |g| and Uabs = 1 the modelled error of y is about 1.5e-3: a value
+    # 2^-14 off the midpoint is flagged (slack = spacing + dy), values 2^-6
+    # off it or exactly representable are not.
+    g = np.array([40.125 + 2 ** -14, 40.25, 40.125 + 2 ** -6, 40.0])
+    s = oracle.bf16_rounding_slack(g, g, np.ones(4), np.abs(g), np.ones(4), 1)
+    assert 0.25 < s[0] < 0.26
+    assert s[1] == 0 and s[2] == 0 and s[3] == 0
+    # y = 0 exactly with u = 0 and Uabs = 0: nothing can move, slack 0
+    assert oracle.bf16_rounding_slack(np.zeros(1), np.ones(1), np.zeros(1), np.ones(1),
+                                      np.zeros(1), 1)[0] == 0.0
+
+
+def _other_bf16_neighbour(y, yb):
+    """The BF16 value next to yb on the side of y (y exact, yb = BF16(y))."""
+    ab = np.abs(yb)
+    m, e = np.frexp(ab)
+    above = np.ldexp(1.0, e - 8)
+    below = np.where(m == 0.5, above / 2, above)
+    up = np.abs(y) > ab
+    return np.sign(y) * np.where(up, ab + above, ab - below)
+
+
+def test_mlp_rounding_slack_covers_neighbour_roundings():
+    # Z computed with every flagged Y element rounded to its other BF16
+    # neighbour stays within the slack of the oracle's Z; rows are independent.
+    M, H, F = 9, 64, 96
+    A, W1, W2 = si.make_bf16(M, F, H, seed=13)
+    W3 = si.make_bf16(1, H, F, seed=14)[1]
+    a, w1, w2, w3 = (si.bits_u16(t) for t in (A, W1, W2, W3))
+    Z, Yb = oracle.mlp_bf16(a, w1, w2, w3, with_y=True)
+    G, U, Y = oracle.swiglu_bf16(a, w1, w2, with_gate_up=True)
+    Ga, Ua, _ = oracle.swiglu_bf16(a & 0x7FFF, w1 & 0x7FFF, w2 & 0x7FFF, with_gate_up=True)
+    s = oracle.bf16_rounding_slack(Y, G, U, Ga, Ua, H)
+    assert 0 < np.count_nonzero(s) < s.size // 4
+    yb = oracle.bf16_bits_to_f64(Yb)
+    flipped = np.where(s > 0, _other_bf16_neighbour(Y, yb), yb)
+    Z_other = flipped @ oracle.bf16_bits_to_f64(w3)
+    B = oracle.mlp_rounding_slack(a, w1, w2, w3)
+    assert np.all(np.abs(Z_other - Z) <= B + 1e-12 * np.abs(Z))
+    assert np.array_equal(oracle.mlp_rounding_slack(a, w1, w2, w3, rows=[8, 2]), B[[8, 2]])
+
+
 @pytest.mark.parametrize("with_r", [False, True])
 def test_linear_against_numpy(with_r):
     M, N, K = 37, 72, 56

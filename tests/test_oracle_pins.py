@@ -255,10 +255,17 @@ def test_parity_report_flags_errors():
     assert not oracle.parity_report(nan, ref)["ok"]
 
 
-def test_parity_report_mismatch_fraction():
+def test_parity_report_per_element_slack():
     ref = np.linspace(1, 2, 1000)
     y = ref.copy()
     y[:2] *= 1.011              # 2 of 1000 significant elements 1.1 % off, inside bound (1)
     assert not oracle.parity_report(y, ref)["ok"]
-    assert not oracle.parity_report(y, ref, max_sig_mismatch_frac=1e-3)["ok"]
-    assert oracle.parity_report(y, ref, max_sig_mismatch_frac=2e-3)["ok"]
+    slack = np.zeros_like(ref)
+    slack[0] = 0.002            # explains the first element's excess only
+    assert not oracle.parity_report(y, ref, sig_slack=slack)["ok"]
+    slack[1] = 0.002
+    assert oracle.parity_report(y, ref, sig_slack=slack)["ok"]
+    # slack widens rule (2) only: bound (1) still holds every element
+    far = ref.copy()
+    far[500] *= 1.03
+    assert not oracle.parity_report(far, ref, sig_slack=np.full_like(ref, 1.0))["ok"]

@@ -3,11 +3,14 @@ memory (a plugin handed only its tensors, a runtime whose memory is planned
 before it runs).
 
 swiglu_mlp_noalloc keeps Y in a fixed scratch area inside the library instead
-of a caller-provided workspace.  Called through the C ABI, its result must
-match that of swiglu_mlp (the existing entry point, given a workspace that
-torch allocates) within the acceptance rule the other tests use, on two calls
-in a row with different shapes and data (the scratch area keeps the previous
-call's contents), and a size whose Y does not fit must be rejected.
+of a caller-provided workspace.  Called through the C ABI on two calls in a
+row with different shapes and data (the scratch area keeps the previous
+call's contents), its result must meet the MLP block's acceptance rule
+against the oracle's MLP block (the rule of the other MLP tests, with the
+per-element slack for BF16 rounding of the intermediate Y), and must match
+that of swiglu_mlp (the existing entry point, given a workspace that torch
+allocates) within the same rule.  A size whose Y does not fit must be
+rejected.
 
 The file name makes pytest collect it last, so that a run stopping at the
 first failure has already run every other test.
@@ -40,7 +43,7 @@ def _case(M, H, F, seed, with_r):
     R = None
     if with_r:
         R = torch.randn(M, H, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
-    return tuple(t.to(DEV) if t is not None else None for t in (A, W1, W2, W3, R))
+    return (A, W1, W2, W3, R)
 
 
 def _noalloc_c_abi(sg, A, W1, W2, W3, R):
@@ -55,19 +58,25 @@ def _noalloc_c_abi(sg, A, W1, W2, W3, R):
     return Z
 
 
-def test_noalloc_matches_mlp_on_two_calls_in_a_row(sg):
+def test_noalloc_matches_oracle_and_mlp_on_two_calls_in_a_row(sg):
     cases = [(128, 896, 4864, 11, True), (200, 264, 520, 12, False)]
     results = []
     for M, H, F, seed, with_r in cases:      # two calls back to back, no sync between
-        args = _case(M, H, F, seed, with_r)
-        results.append((_noalloc_c_abi(sg, *args), args))
+        host = _case(M, H, F, seed, with_r)
+        dev = tuple(t.to(DEV) if t is not None else None for t in host)
+        results.append((_noalloc_c_abi(sg, *dev), host, dev))
     rc, detail = sg.swiglu_device_status()
     assert rc == sg.OK, (sg.status_string(rc), detail)
-    for Z, (A, W1, W2, W3, R) in results:
-        want = sg.swiglu_mlp(A, W1, W2, W3, R)          # the existing entry point
+    for Z, (A, W1, W2, W3, R), dev in results:
+        z = Z.double().cpu().numpy()
+        bits = [si.bits_u16(t) for t in (A, W1, W2, W3)]
+        ref = oracle.mlp_bf16(*bits, si.bits_u16(R) if R is not None else None)
+        slack = oracle.mlp_rounding_slack(*bits)
+        oracle.assert_parity(z, ref, "noalloc vs oracle", sig_slack=slack)
+        want = sg.swiglu_mlp(*dev)                       # the existing entry point
         torch.cuda.synchronize()
-        oracle.assert_parity(Z.double().cpu().numpy(), want.double().cpu().numpy(),
-                             "noalloc vs swiglu_mlp")
+        oracle.assert_parity(z, want.double().cpu().numpy(), "noalloc vs swiglu_mlp",
+                             sig_slack=2 * slack)
 
 
 def test_noalloc_rejects_y_beyond_the_scratch(sg):
