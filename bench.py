@@ -785,7 +785,7 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
     eager_us = [by_m[M] for (_, M, _) in wl.calls]
 
     # the eager step: every call of the fused step replaced by the two-GEMM path
-    fns = [factory(*base[M]) for (_, M, _) in wl.calls]
+    fns = [factory(*base[M][0], base[M][1]) for (_, M, _) in wl.calls]
 
     def step():
         for f in fns:
@@ -1000,6 +1000,68 @@ def run_reference(args, ws, rank):
     }
 
 
+# ----------------------------------------------------------------------------- variant sweep
+
+SWEEP_BF16 = ("qwen2.5-0.5b-m64", "qwen2.5-0.5b", "qwen2.5-7b", "qwen2.5-72b")
+SWEEP_WEIGHTS = ("qwen2.5-0.5b-w4", "qwen2.5-7b-w4", "qwen2.5-0.5b-mxfp8", "qwen2.5-7b-mxfp8",
+                 "qwen2.5-0.5b-nvfp4", "qwen2.5-7b-nvfp4")
+SWEEP_VARIANTS = ("1sm_n128", "1sm_n64", "1sm_n32", "2sm_n128", "1sm_n64_sk2")
+
+
+def run_sweep(args):
+    """Every BF16 variant for every (M, N, K) and weight form of the BF16
+    configurations, and every weight-format kernel for the INT4/MXFP8/NVFP4
+    configurations, each timed alone like the per-call durations of the main
+    run (back-to-back launches in a CUDA graph on rotating input copies).
+    Writes the table the variant choice is checked against."""
+    import torch
+    import swiglu_gemm_transformer_gb300 as sg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = sg.lib()
+    stream = torch.cuda.Stream(device=dev)
+    entries = []
+    sampler = ClockSampler(0)
+    sampler.start()
+    t0 = time.time()
+    names = [w for w in args.sweep_workloads.split(",") if w] or list(SWEEP_BF16 + SWEEP_WEIGHTS)
+    for name in names:
+        wl = Workload(name, dev)
+        for (form, M, v), bufs in zip(wl.calls, wl.buffers):
+            us = {}
+            if wl.kind == "bf16":
+                for vn in SWEEP_VARIANTS:
+                    us[vn] = round(measure_calls(wl, stream, args.call_launches, None,
+                                                 [((form, M, sg.VARIANTS[vn]), bufs)])[0], 3)
+                auto = sg.variant_name(v)
+            else:
+                auto = sg.WEIGHT_KERNELS[sg.swiglu_select_weight_kernel(M, wl.N)]
+                for k, kn in enumerate(sg.WEIGHT_KERNELS):
+                    sg.swiglu_set_weight_kernel(k)
+                    try:
+                        us[kn] = round(measure_calls(wl, stream, args.call_launches, None,
+                                                     [((form, M, v), bufs)])[0], 3)
+                    finally:
+                        sg.swiglu_set_weight_kernel(-1)
+            rc, detail = sg.swiglu_device_status(stream)
+            if rc != sg.OK:
+                raise RuntimeError(f"device status in the sweep: {sg.status_string(rc)} ({detail})")
+            entries.append({"workload": name, "kind": wl.kind, "form": form, "M": M, "N": wl.N,
+                            "K": wl.K, "us": us, "auto": auto})
+            log(f"sweep {name} {form} M={M}: auto {auto}, {us}")
+        del wl
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    props = torch.cuda.get_device_properties(dev)
+    return {"_note": "Per-call device time (us) of every BF16 variant and every weight-format "
+                     "kernel, each timed alone: back-to-back launches in a CUDA graph over "
+                     "rotating input copies (> 2.5x L2). Written by bench.py --sweep; the "
+                     "variant choice is tested against it.",
+            "gpu": props.name, "sm_count": props.multi_processor_count,
+            "torch": torch.__version__, "clocks": clocks,
+            "seconds": round(time.time() - t0, 1), "entries": entries}
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -1021,12 +1083,23 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compile-context", action="store_true",
                     help="skip timing the unfused function under torch.compile (context)")
+    ap.add_argument("--sweep", default="",
+                    help="time every variant of every configuration and write the table to this file")
+    ap.add_argument("--sweep-workloads", default="",
+                    help="comma-separated workloads for --sweep (default: all BF16 and weight formats)")
     ap.add_argument("--only", default="",
                     help="restrict the step to calls FORM:M[,FORM:M...] (profiling a single kernel)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     ws, rank, local = dist_env()
+
+    if args.sweep:
+        table = run_sweep(args)
+        with open(args.sweep, "w") as f:
+            json.dump(table, f, indent=1)
+        log(f"wrote {args.sweep}")
+        return
 
     if args.impl == "reference":
         out = run_reference(args, ws, rank)

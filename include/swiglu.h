@@ -244,6 +244,11 @@ int swiglu_quant_fp8(const void *X, void *Xq, float *s, int64_t M, int64_t K, vo
  *       output tiles to occupy the GPU (small M); swiglu_linear_workspace_size()
  *       gives the bytes wanted.  NULL or too small is valid: the product then
  *       runs without splitting K (same result up to summation order).
+ *       When the product's 128 x 64 output tiles, spread over clusters of 4
+ *       or 8 CTAs that each take a slice of K, fit one wave of the GPU (e.g.
+ *       M <= 128 with N <= 1216 on 152 SMs), the slices' partial sums are
+ *       added in distributed shared memory inside each cluster and no
+ *       workspace is used (the size query returns 0).
  * K and N multiples of 8; other rules as above.
  */
 uint64_t swiglu_linear_workspace_size(int64_t M, int64_t N, int64_t K);
@@ -314,6 +319,13 @@ int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved);
  * ceil(M/256) * ceil(N/128) >= 0.9 * #SMs).  -1 for negative sizes.
  * Host-only (GB300's 152 SMs when no device is visible). */
 int swiglu_select_weight_kernel(int64_t M, int64_t N);
+
+/* Forces the kernel of the weight-format entry points for later calls
+ * (process-wide): 0, 1 or 2 as swiglu_select_weight_kernel numbers them, or
+ * -1 (the default) for the library's choice by shape.  For sweeps and tests;
+ * swiglu_select_weight_kernel reports the forced kernel while one is set.
+ * Returns SWIGLU_ERR_INVALID_ARG for other values. */
+int swiglu_set_weight_kernel(int32_t kernel);
 
 /* Short name of a variant ("1sm_n128", ...); "?" for an unknown value. */
 const char *swiglu_variant_name(int32_t variant);

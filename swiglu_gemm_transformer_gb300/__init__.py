@@ -49,6 +49,7 @@ EXPORTS = {
     "swiglu_mlp_noalloc": ("ppppp p lll p", ctypes.c_int),
     "swiglu_select_variant": ("lll i", ctypes.c_int),
     "swiglu_select_weight_kernel": ("ll", ctypes.c_int),
+    "swiglu_set_weight_kernel": ("i", ctypes.c_int),
     "swiglu_variant_name": ("i", ctypes.c_char_p),
     "swiglu_status_string": ("i", ctypes.c_char_p),
     "swiglu_device_status": ("p P", ctypes.c_int),
@@ -500,6 +501,12 @@ def swiglu_select_weight_kernel(M: int, N: int) -> int:
     """0 split-K cluster kernel, 1 wide kernel, 2 wide kernel with two row
     blocks per CTA: the kernel the INT4/MXFP8/NVFP4 entry points run."""
     return lib().swiglu_select_weight_kernel(M, N)
+
+
+def swiglu_set_weight_kernel(kernel: int):
+    """Force the weight-format kernel (0 split-K, 1 wide, 2 wide with two row
+    blocks per CTA) for later calls, or -1 for the library's choice."""
+    _check("swiglu_set_weight_kernel", lib().swiglu_set_weight_kernel(int(kernel)))
 
 
 def swiglu_device_status(stream=None):

@@ -5,12 +5,57 @@
 #include <cuda_bf16.h>
 
 #include "launch_tc.cuh"
+#include "swiglu_linsk_kernel.cuh"
 
 namespace swiglu {
 
 cudaError_t launch_linear(int lin_n, const LaunchArgs &la) {
   return lin_n == 256 ? launch_pair<PairCfg<true, 6, false, true, 256>>(la)
                       : launch_pair<PairCfg<true, 8, false, true, 128>>(la);
+}
+
+namespace {
+
+// The split-K cluster down projection: one 128 x 64 output tile per cluster
+// of CS CTAs (la.p.num_m_blk x la.p.num_n_blk tiles).
+template <int CS>
+cudaError_t launch_linsk(const LaunchArgs &la) {
+  using C = LinSkCfg<CS>;
+  static PerDeviceOnce once;
+  auto kern = swiglu_linsk_kernel<C>;
+  if (once.needed(la.device, la.ctx_gen)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    once.done(la.device, la.ctx_gen);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  const int64_t tiles = int64_t(la.p.num_m_blk) * la.p.num_n_blk;  // one tile per cluster
+  cfg.gridDim = dim3(static_cast<unsigned>(CS * tiles), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = la.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.p);
+}
+
+}  // namespace
+
+cudaError_t launch_linear_sk(int cs, const LaunchArgs &la) {
+  switch (cs) {
+    case 2: return launch_linsk<2>(la);
+    case 4: return launch_linsk<4>(la);
+    case 8: return launch_linsk<8>(la);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Z = BF16(sum_s ws[s] + R): four columns per thread (N is a multiple of 8),

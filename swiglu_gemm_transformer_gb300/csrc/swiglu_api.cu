@@ -40,9 +40,19 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_weights_read_only{0};
+// Weight-format kernel: -1 = chosen by shape, 0/1/2 forces one (sweeps, tests).
+std::atomic<int> g_weight_kernel_forced{-1};
+// Row blocks that walk the column blocks together in the CTA-pair kernels'
+// tile order: 0 = the default (8), else the SWIGLU_GROUP_M environment
+// variable's value, read once (for tuning sweeps).
+std::atomic<int> g_group_m{0};
 // Down-projection tile width: 0 = chosen by shape; 128 or 256 forces it (the
 // SWIGLU_LINEAR_N environment variable, read once, sets it for tuning sweeps).
 std::atomic<int> g_linear_n{0};
+// Split-K cluster down projection: -1 = chosen by shape, 0 = never, 2/4/8 =
+// that cluster size whenever its grid fits one wave (SWIGLU_LINEAR_SK, read
+// once, for tuning sweeps).
+std::atomic<int> g_linear_sk{-1};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 using CtxGetCurrentFn = CUresult (*)(CUcontext *);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
@@ -113,6 +123,14 @@ int device_state(DeviceState **out, int *dev_out) {
       const long v = std::strtol(e, nullptr, 10);
       if (v == 128 || v == 256) g_linear_n.store(int(v), std::memory_order_relaxed);
     }
+    if (const char *e = std::getenv("SWIGLU_GROUP_M")) {
+      const long v = std::strtol(e, nullptr, 10);
+      if (v >= 1 && v <= 4096) g_group_m.store(int(v), std::memory_order_relaxed);
+    }
+    if (const char *e = std::getenv("SWIGLU_LINEAR_SK")) {
+      const long v = std::strtol(e, nullptr, 10);
+      if (v == 0 || v == 2 || v == 4 || v == 8) g_linear_sk.store(int(v), std::memory_order_relaxed);
+    }
   }
   *out = &st;
   *dev_out = dev;
@@ -142,6 +160,11 @@ int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t 
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+int pair_group_m() {
+  const int g = g_group_m.load(std::memory_order_relaxed);
+  return g > 0 ? g : 8;
+}
+
 // The variants a caller may name (numbers 5-8 are retired and rejected).
 bool variant_known(int32_t v) {
   return v == SWIGLU_VARIANT_AUTO || v == SWIGLU_VARIANT_1SM_N128 || v == SWIGLU_VARIANT_1SM_N64 ||
@@ -155,6 +178,8 @@ bool variant_known(int32_t v) {
 // 2 = the wide kernel with two (M > 128 and that grid still fills about one
 // wave: one decode of each weight step then serves 256 rows).
 int weight_kernel(int64_t M, int64_t N, int sm_count) {
+  const int forced = g_weight_kernel_forced.load(std::memory_order_relaxed);
+  if (forced >= 0) return forced;
   if (M <= 128 && 2 * cdiv(N, 64) <= sm_count) return 0;
   if (M > 128 && 10 * cdiv(M, 256) * cdiv(N, 128) >= 9 * int64_t(sm_count)) return 2;
   return 1;
@@ -171,6 +196,10 @@ int choose_variant(int64_t M, int64_t N, int64_t K, bool /*interleaved*/, int sm
   // Two 128-row blocks of 64-column tiles in one wave (M = 256, N = 4864:
   // 8.4 us against 9.8 us for the CTA-pair tiles).
   if (M <= 256 && cdiv(M, 128) * cdiv(N, 64) <= sm_count) return SWIGLU_VARIANT_1SM_N64;
+  // Up to one wave of 128 x 128 tiles (0.5B, M = 512: 152 tiles on 152 SMs):
+  // one tile per SM over all of K, 10.6 us against 10.9 us for the CTA-pair
+  // tiles (measured variant table).
+  if (M > 128 && cdiv(M, 128) * cdiv(N, 128) <= sm_count) return SWIGLU_VARIANT_1SM_N128;
   // Larger M: one 256x128 tile per CTA pair halves the weight bytes each SM
   // streams per K step (32 KB instead of 48 KB).
   if (M > 128) return SWIGLU_VARIANT_2SM_N128;
@@ -240,7 +269,7 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
   p.num_m_blk = int32_t(cdiv(M, g.bm));
   p.num_n_blk = int32_t(cdiv(N, g.bn));
   p.num_k_blk = int32_t(cdiv(K, g.bk));
-  const int gm = g.cluster == 2 ? 8 : 16;
+  const int gm = g.cluster == 2 ? pair_group_m() : 16;
   p.group_m = p.num_m_blk < gm ? p.num_m_blk : gm;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
@@ -462,7 +491,7 @@ int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, cons
   p.num_m_blk = int32_t(cdiv(M, 256));
   p.num_n_blk = int32_t(cdiv(N, 128));
   p.num_k_blk = int32_t(cdiv(K, 128));
-  p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
+  p.group_m = p.num_m_blk < pair_group_m() ? p.num_m_blk : pair_group_m();
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
   p.sA = sA;
@@ -481,14 +510,39 @@ int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, cons
 // ---- the down projection: Z = X W (+ R) ----------------------------------------
 
 struct LinearPlan {
+  int sk_cs;       // > 0: the split-K cluster kernel with this many CTAs per tile
   int lin_n;       // output columns per CTA-pair tile (256 or 128)
   int k_splits;    // K slices (1 = no split)
   int kb_per;      // 64-deep K steps per slice
   uint64_t ws_bytes;
 };
 
+// Cluster size of the split-K cluster down projection for this shape, or 0.
+// Its 128 x 64 tiles, each spread over a cluster whose CTAs take one K
+// slice each, must fit one wave; a larger cluster spreads the product over
+// more SMs and each CTA's slice is shorter.
+int linear_sk_cluster(int64_t M, int64_t N, int64_t K, int sm_count) {
+  const int forced = g_linear_sk.load(std::memory_order_relaxed);
+  if (forced == 0) return 0;
+  const int64_t tiles = cdiv(M, 128) * cdiv(N, 64);
+  const int64_t nk = cdiv(K, 64);
+  for (int cs : {8, 4, 2}) {
+    if (forced > 0 && cs != forced) continue;
+    if (tiles * cs <= sm_count && nk >= cs && (forced > 0 || cs >= 4)) return cs;
+  }
+  return 0;
+}
+
 LinearPlan plan_linear(int64_t M, int64_t N, int64_t K, int sm_count) {
   LinearPlan pl;
+  pl.sk_cs = linear_sk_cluster(M, N, K, sm_count);
+  if (pl.sk_cs > 0) {   // no workspace: the partial sums are reduced in the cluster
+    pl.lin_n = 64;
+    pl.k_splits = pl.sk_cs;
+    pl.kb_per = int(cdiv(cdiv(K, 64), pl.sk_cs));
+    pl.ws_bytes = 0;
+    return pl;
+  }
   const int forced = g_linear_n.load(std::memory_order_relaxed);
   // 256-column tiles (the pair's weight halves of 128 columns, 32 KB per CTA
   // per K step) keep the tensor pipe fed; measured faster than 128 even when
@@ -546,6 +600,34 @@ int run_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, 
     return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
   }
   LinearPlan pl = plan_linear(M, N, K, st->sm_count);
+  if (pl.sk_cs > 0) {
+    LaunchArgs la;
+    std::memset(&la, 0, sizeof la);
+    const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    rc = encode_2d(&la.a, BF16, X, K, M, K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == SWIGLU_OK)
+      rc = encode_2d(&la.b0, BF16, W, N, K, 2 * N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != SWIGLU_OK) return rc;
+    KParams &p = la.p;
+    p.M = int32_t(M);
+    p.N = int32_t(N);
+    p.K = int32_t(K);
+    p.num_m_blk = int32_t(cdiv(M, 128));
+    p.num_n_blk = int32_t(cdiv(N, 64));
+    p.num_k_blk = int32_t(cdiv(K, 64));
+    p.group_m = p.num_m_blk;
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.err = st->err;
+    p.R = R;
+    p.Y = Z;
+    p.k_splits = pl.sk_cs;
+    p.kb_per_split = pl.kb_per;
+    p.w_early = g_weights_read_only.load(std::memory_order_relaxed);
+    la.device = dev;
+    la.ctx_gen = st->gen;
+    la.stream = s;
+    return launch_linear_sk(pl.sk_cs, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  }
   if (pl.k_splits > 1 &&
       (ws == nullptr || ws_bytes < pl.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 15u) ||
        overlaps(ws, pl.ws_bytes, Z, z_bytes) || overlaps(ws, pl.ws_bytes, X, uint64_t(M) * K * 2))) {
@@ -569,7 +651,7 @@ int run_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, 
   p.num_m_blk = int32_t(cdiv(M, 256));
   p.num_n_blk = int32_t(cdiv(N, pl.lin_n));
   p.num_k_blk = int32_t(cdiv(K, 64));
-  p.group_m = p.num_m_blk < 8 ? p.num_m_blk : 8;
+  p.group_m = p.num_m_blk < pair_group_m() ? p.num_m_blk : pair_group_m();
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.err = st->err;
   p.R = R;
@@ -765,6 +847,12 @@ int swiglu_select_variant(int64_t M, int64_t N, int64_t K, int32_t interleaved) 
 int swiglu_select_weight_kernel(int64_t M, int64_t N) {
   if (M < 0 || N < 0) return -1;
   return weight_kernel(M, N, device_sm_count());
+}
+
+int swiglu_set_weight_kernel(int32_t kernel) {
+  if (kernel < -1 || kernel > 2) return SWIGLU_ERR_INVALID_ARG;
+  g_weight_kernel_forced.store(kernel, std::memory_order_relaxed);
+  return SWIGLU_OK;
 }
 
 const char *swiglu_variant_name(int32_t variant) {

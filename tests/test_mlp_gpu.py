@@ -44,8 +44,13 @@ def _status(sg):
     assert rc == sg.OK, f"device status {sg.status_string(rc)} detail {detail}"
 
 
+# Few output tiles (small M) run the split-K cluster kernel: (63, 136, 200),
+# (257, 392, 264), (300, 512, 1000), (200, 896, 4864) with 4 CTAs per tile,
+# (128, 896, 4864), (100, 264, 520) and (64, 72, 4864) (a ragged last tile)
+# with 8; the others the CTA-pair kernel.
 @pytest.mark.parametrize("shape", [(1, 8, 8), (63, 136, 200), (257, 392, 264), (300, 512, 1000),
-                                   (128, 896, 4864), (200, 896, 4864), (2048, 3584, 1024)],
+                                   (128, 896, 4864), (200, 896, 4864), (2048, 3584, 1024),
+                                   (100, 264, 520), (64, 72, 4864)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("with_r", [False, True])
 @pytest.mark.parametrize("with_ws", [True, False])
@@ -60,15 +65,16 @@ def test_linear(sg, shape, with_r, with_ws):
     oracle.assert_parity(Z.float().cpu().numpy(), ref, f"linear {shape} r={with_r} ws={with_ws}")
 
 
-def test_linear_in_place_residual(sg):
-    M, N, K = 130, 264, 136
+@pytest.mark.parametrize("shape", [(130, 264, 136), (100, 264, 520)], ids=["pair", "cluster"])
+def test_linear_in_place_residual(sg, shape):
+    M, N, K = shape
     X, W, _ = si.make_bf16(M, N, K, seed=1)
     R = _residual(M, N, 2)
     Zd = R.clone().to(DEV)
     sg.swiglu_linear(X.to(DEV), W.to(DEV), Zd, Zd)
     _status(sg)
     ref = oracle.linear_bf16(si.bits_u16(X), si.bits_u16(W), si.bits_u16(R))
-    oracle.assert_parity(Zd.float().cpu().numpy(), ref, "in-place residual")
+    oracle.assert_parity(Zd.float().cpu().numpy(), ref, f"in-place residual {shape}")
 
 
 def test_linear_split_matches_unsplit(sg):
