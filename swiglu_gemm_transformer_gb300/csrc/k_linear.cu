@@ -16,11 +16,11 @@ cudaError_t launch_linear(int lin_n, const LaunchArgs &la) {
 
 namespace {
 
-// The split-K cluster down projection: one 128 x 64 output tile per cluster
+// The split-K cluster down projection: one 128 x BN output tile per cluster
 // of CS CTAs (la.p.num_m_blk x la.p.num_n_blk tiles).
-template <int CS>
+template <int CS, int BN>
 cudaError_t launch_linsk(const LaunchArgs &la) {
-  using C = LinSkCfg<CS>;
+  using C = LinSkCfg<CS, BN>;
   static PerDeviceOnce once;
   auto kern = swiglu_linsk_kernel<C>;
   if (once.needed(la.device, la.ctx_gen)) {
@@ -49,11 +49,19 @@ cudaError_t launch_linsk(const LaunchArgs &la) {
 
 }  // namespace
 
-cudaError_t launch_linear_sk(int cs, const LaunchArgs &la) {
+cudaError_t launch_linear_sk(int cs, int bn, const LaunchArgs &la) {
+  if (bn == 128) {
+    switch (cs) {
+      case 2: return launch_linsk<2, 128>(la);
+      case 4: return launch_linsk<4, 128>(la);
+      case 8: return launch_linsk<8, 128>(la);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (cs) {
-    case 2: return launch_linsk<2>(la);
-    case 4: return launch_linsk<4>(la);
-    case 8: return launch_linsk<8>(la);
+    case 2: return launch_linsk<2, 64>(la);
+    case 4: return launch_linsk<4, 64>(la);
+    case 8: return launch_linsk<8, 64>(la);
     default: return cudaErrorInvalidValue;
   }
 }

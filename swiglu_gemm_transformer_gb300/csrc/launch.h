@@ -66,8 +66,8 @@ cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf
 cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t *err, cudaStream_t s);
 cudaError_t launch_fp8(bool interleaved, const LaunchArgs &la);
 cudaError_t launch_linear(int lin_n, const LaunchArgs &la);
-// cs: CTAs per cluster (2, 4 or 8); la.p tiles are 128 x 64
-cudaError_t launch_linear_sk(int cs, const LaunchArgs &la);
+// cs: CTAs per cluster (2, 4 or 8); bn: tile width (64 or 128); la.p tiles are 128 x bn
+cudaError_t launch_linear_sk(int cs, int bn, const LaunchArgs &la);
 cudaError_t launch_splitk_reduce(const float *ws, int splits, const void *R, void *Z, int64_t M,
                                  int64_t N, int sm_count, cudaStream_t s);
 cudaError_t launch_pack_rows_interleaved_u8(const void *W1t, const void *W2t, void *Wft,

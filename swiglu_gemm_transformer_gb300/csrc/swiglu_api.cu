@@ -50,9 +50,11 @@ std::atomic<int> g_group_m{0};
 // SWIGLU_LINEAR_N environment variable, read once, sets it for tuning sweeps).
 std::atomic<int> g_linear_n{0};
 // Split-K cluster down projection: -1 = chosen by shape, 0 = never, 2/4/8 =
-// that cluster size whenever its grid fits one wave (SWIGLU_LINEAR_SK, read
-// once, for tuning sweeps).
+// that cluster size whenever its grid fits one wave (SWIGLU_LINEAR_SK), and
+// 0 = either tile width, 64 or 128 = that one (SWIGLU_LINEAR_SKN); both read
+// once, for tuning sweeps.
 std::atomic<int> g_linear_sk{-1};
+std::atomic<int> g_linear_skn{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 using CtxGetCurrentFn = CUresult (*)(CUcontext *);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
@@ -130,6 +132,10 @@ int device_state(DeviceState **out, int *dev_out) {
     if (const char *e = std::getenv("SWIGLU_LINEAR_SK")) {
       const long v = std::strtol(e, nullptr, 10);
       if (v == 0 || v == 2 || v == 4 || v == 8) g_linear_sk.store(int(v), std::memory_order_relaxed);
+    }
+    if (const char *e = std::getenv("SWIGLU_LINEAR_SKN")) {
+      const long v = std::strtol(e, nullptr, 10);
+      if (v == 64 || v == 128) g_linear_skn.store(int(v), std::memory_order_relaxed);
     }
   }
   *out = &st;
@@ -511,33 +517,46 @@ int run_fp8(const void *A, const void *B0, const void *B1, const float *sA, cons
 
 struct LinearPlan {
   int sk_cs;       // > 0: the split-K cluster kernel with this many CTAs per tile
+  int sk_bn;       //      and output tiles of 128 x sk_bn
   int lin_n;       // output columns per CTA-pair tile (256 or 128)
   int k_splits;    // K slices (1 = no split)
   int kb_per;      // 64-deep K steps per slice
   uint64_t ws_bytes;
 };
 
-// Cluster size of the split-K cluster down projection for this shape, or 0.
-// Its 128 x 64 tiles, each spread over a cluster whose CTAs take one K
-// slice each, must fit one wave; a larger cluster spreads the product over
-// more SMs and each CTA's slice is shorter.
-int linear_sk_cluster(int64_t M, int64_t N, int64_t K, int sm_count) {
+// Cluster size (return value, 0 = not used) and tile width (*bn) of the
+// split-K cluster down projection for this shape.  Its 128 x bn tiles, each
+// spread over a cluster whose CTAs take one K slice each, must fit one wave.
+// In order of preference: 64-column tiles over 8 or 4 CTAs (short K slices,
+// many SMs), then 128-column tiles over 4 or 2 (X read by half as many
+// tiles), then 64-column tiles over 2.  Clusters of 2 are used only for
+// short K (at most 96 steps of 64): with long K the CTA-pair kernel with a
+// workspace reduction measured faster (7B, M = 128: 36.8 us against 44.6).
+int linear_sk_cluster(int64_t M, int64_t N, int64_t K, int sm_count, int *bn) {
   const int forced = g_linear_sk.load(std::memory_order_relaxed);
+  const int forced_n = g_linear_skn.load(std::memory_order_relaxed);
   if (forced == 0) return 0;
-  const int64_t tiles = cdiv(M, 128) * cdiv(N, 64);
   const int64_t nk = cdiv(K, 64);
-  for (int cs : {8, 4, 2}) {
+  static const int kOrder[5][2] = {{8, 64}, {4, 64}, {4, 128}, {2, 128}, {2, 64}};
+  for (const auto &o : kOrder) {
+    const int cs = o[0], w = o[1];
     if (forced > 0 && cs != forced) continue;
-    if (tiles * cs <= sm_count && nk >= cs && (forced > 0 || cs >= 4)) return cs;
+    if (forced_n > 0 && w != forced_n) continue;
+    const int64_t tiles = cdiv(M, 128) * cdiv(N, w);
+    if (tiles * cs > sm_count || nk < cs) continue;
+    if (cs == 2 && forced <= 0 && nk > 96) continue;
+    *bn = w;
+    return cs;
   }
   return 0;
 }
 
 LinearPlan plan_linear(int64_t M, int64_t N, int64_t K, int sm_count) {
   LinearPlan pl;
-  pl.sk_cs = linear_sk_cluster(M, N, K, sm_count);
+  pl.sk_bn = 64;
+  pl.sk_cs = linear_sk_cluster(M, N, K, sm_count, &pl.sk_bn);
   if (pl.sk_cs > 0) {   // no workspace: the partial sums are reduced in the cluster
-    pl.lin_n = 64;
+    pl.lin_n = pl.sk_bn;
     pl.k_splits = pl.sk_cs;
     pl.kb_per = int(cdiv(cdiv(K, 64), pl.sk_cs));
     pl.ws_bytes = 0;
@@ -613,7 +632,7 @@ int run_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, 
     p.N = int32_t(N);
     p.K = int32_t(K);
     p.num_m_blk = int32_t(cdiv(M, 128));
-    p.num_n_blk = int32_t(cdiv(N, 64));
+    p.num_n_blk = int32_t(cdiv(N, pl.sk_bn));
     p.num_k_blk = int32_t(cdiv(K, 64));
     p.group_m = p.num_m_blk;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
@@ -626,7 +645,7 @@ int run_linear(const void *X, const void *W, const void *R, void *Z, int64_t M, 
     la.device = dev;
     la.ctx_gen = st->gen;
     la.stream = s;
-    return launch_linear_sk(pl.sk_cs, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+    return launch_linear_sk(pl.sk_cs, pl.sk_bn, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
   }
   if (pl.k_splits > 1 &&
       (ws == nullptr || ws_bytes < pl.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 15u) ||

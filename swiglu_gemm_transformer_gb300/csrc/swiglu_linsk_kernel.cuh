@@ -9,14 +9,14 @@
 //
 // With few rows (the decode-sized M <= 128 of the Qwen-2.5 MLPs) the product
 // has few output tiles: 0.5B's H = 896 output columns are 14 tiles of 64.
-// Each 128-row x 64-column tile goes to a cluster of CS CTAs (CS = 8, 4 or
-// 2), and CTA r multiplies its CS-th of the K steps:
-//   * warp 8 streams X[128 x 64] and W[64 x 64] per K step into a
+// Each 128-row x BN-column tile (BN = 64 or 128) goes to a cluster of CS
+// CTAs (CS = 8, 4 or 2), and CTA r multiplies its CS-th of the K steps:
+//   * warp 8 streams X[128 x 64] and W[64 x BN] per K step into a
 //     STAGES-deep ring (TMA, 128-byte swizzle), warp 9 issues
-//     tcgen05.mma M=128 x N=64 (FP32 accumulators in tensor memory);
+//     tcgen05.mma M=128 x N=BN (FP32 accumulators in tensor memory);
 //   * reduce-scatter over the cluster: CTA r keeps output columns
-//     [r KEEP, (r+1) KEEP) of the tile, KEEP = 64 / CS.  Eight epilogue
-//     warps (four TMEM lane groups x two 32-column halves) read their
+//     [r KEEP, (r+1) KEEP) of the tile, KEEP = BN / CS.  Eight epilogue
+//     warps (four TMEM lane groups x two BN/2-column halves) read their
 //     partial sums and send each peer its KEEP columns with st.async
 //     (16-byte stores into the peer's shared memory, counted on the peer's
 //     receive mbarrier); the warps that hold the kept columns wait for the
@@ -42,22 +42,26 @@ namespace swiglu {
 
 enum : uint32_t { WAIT_LINSK_RECV = 8 };
 
-template <int CS_>
+template <int CS_, int BN_ = 64>
 struct LinSkCfg {
   static constexpr int CS = CS_;                 // CTAs per cluster (K slices)
   static constexpr int BM = 128;                 // rows per tile (MMA M)
-  static constexpr int BN = 64;                  // output columns per tile (MMA N)
+  static constexpr int BN = BN_;                 // output columns per tile (MMA N)
   static constexpr int BK = 64;                  // K per stage
   static constexpr int KEEP = BN / CS;           // output columns each CTA finishes
+  static constexpr int HALF = BN / 2;            // accumulator columns per epilogue warp
   static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-  static constexpr int B_BYTES = BK * BN * 2;    // 8 KB, one 128-byte-swizzled box
+  static constexpr int ATOM_BYTES = BK * 64 * 2; // one 64-column, 128-byte-swizzled weight box
+  static constexpr int B_BYTES = BK * BN * 2;    // BN / 64 boxes
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 8;
   // Receive buffer: the CS - 1 peers' partial sums of the kept columns, for
   // all 128 rows: slot s (sender rank s, or s + 1 at and above this CTA's
   // rank), row i, KEEP floats.
-  static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
   static constexpr int RECV_BYTES = (CS - 1) * BM * KEEP * 4;
+  // as many stages as fit beside it (at most 8)
+  static constexpr int STAGES_FIT = (227 * 1024 - RECV_BYTES - 2048) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
+  static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], acc_full, recv, drain
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
@@ -65,10 +69,12 @@ struct LinSkCfg {
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr int THREADS = 32 * 10;
-  static constexpr int TMEM_COLS = 64;
+  static constexpr int TMEM_COLS = BN;
   static constexpr uint32_t IDESC = ptx::idesc_bf16(BM, BN, false, true);
   static_assert(CS == 2 || CS == 4 || CS == 8, "cluster size");
-  static_assert(KEEP % 8 == 0, "kept columns: whole 16-byte BF16 groups");
+  static_assert(BN == 64 || BN == 128, "tile width");
+  static_assert(KEEP % 8 == 0 && HALF % KEEP == 0, "kept columns: whole 16-byte BF16 groups");
+  static_assert(STAGES >= 4, "pipeline depth");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -137,8 +143,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0)
       for (uint32_t s = 0; s < pre; ++s) {
         ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-        ptx::tma_load_2d(base + s * C::STAGE_BYTES + C::A_BYTES, &tmW, full_bar(s), nb * C::BN,
-                         (kb0 + static_cast<int>(s)) * C::BK);
+        for (int j = 0; j < C::BN / 64; ++j)
+          ptx::tma_load_2d(base + s * C::STAGE_BYTES + C::A_BYTES + j * C::ATOM_BYTES, &tmW,
+                           full_bar(s), nb * C::BN + 64 * j, (kb0 + static_cast<int>(s)) * C::BK);
       }
     __syncwarp();
   }
@@ -160,7 +167,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t fb = full_bar(stage);
         if (!early) ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
         ptx::tma_load_2d(sa, &tmX, fb, kb * C::BK, mb * C::BM);
-        if (!early) ptx::tma_load_2d(sa + C::A_BYTES, &tmW, fb, nb * C::BN, kb * C::BK);
+        if (!early)
+          for (int j = 0; j < C::BN / 64; ++j)
+            ptx::tma_load_2d(sa + C::A_BYTES + j * C::ATOM_BYTES, &tmW, fb, nb * C::BN + 64 * j,
+                             kb * C::BK);
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
@@ -191,10 +201,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           // X: K-major, 128-byte swizzle, 16 K-elements = 32 bytes along a row;
-          // W: MN-major, one 64-column box, 8-row K groups 1024 bytes apart,
-          // one MMA's 16 K-rows = 2048 bytes.
+          // W: MN-major, 64-column boxes ATOM_BYTES apart, 8-row K groups
+          // 1024 bytes apart, one MMA's 16 K-rows = 2048 bytes.
           const uint64_t adesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
-          const uint64_t bdesc = ptx::smem_desc(sb + kk * 2048, C::B_BYTES, 1024, ptx::SW_128B);
+          const uint64_t bdesc = ptx::smem_desc(sb + kk * 2048, C::ATOM_BYTES, 1024, ptx::SW_128B);
           ptx::mma_f16(tmem_base, adesc, bdesc, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
         }
         ptx::mma_commit(empty_bar(stage));
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-7)
     // Warp (q, h) owns rows [32q, 32q+32) (its TMEM lanes) and accumulator
-    // columns [32h, 32h+32), i.e. the column groups g (KEEP wide) with
+    // columns [h HALF, (h+1) HALF), i.e. the column groups g (KEEP wide) with
     // g / (CS/2) == h.  It sends group g to CTA g for every g != rank; the
     // warp whose half holds group `rank` finishes those columns.
     const int q = warp & 3;
@@ -225,17 +235,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // sending to it: give their stores time to land before it leaves.
     if (!ok && live(q)) spin_ns(100000);
     if (ok && live(q)) {
-      float v[32];
+      float v[C::HALF];
       if (have_acc) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + 32u * h, r);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence(r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(C::HALF * h + 32 * c), r);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[i]);
+        }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        for (int i = 0; i < C::HALF; ++i) v[i] = 0.0f;
       }
       float acc[C::KEEP];  // the kept columns' partial sums (warp h == rank / GPH)
 #pragma unroll

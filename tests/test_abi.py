@@ -171,10 +171,10 @@ def test_workspace_sizes(lib):
     # 8 CTAs whose partial sums meet in distributed shared memory: no workspace
     assert lib.swiglu_linear_workspace_size(128, 896, 4864) == 0
     assert lib.swiglu_mlp_workspace_size(128, 896, 4864) == 128 * 4864 * 2
-    # 7B, M = 128: 56 tiles do not fit clusters of 4 in one wave -> CTA pairs,
-    # K split into slices whose FP32 partial sums go to the workspace
-    n = lib.swiglu_linear_workspace_size(128, 3584, 18944)
-    assert n > 0 and n % (128 * 3584 * 4) == 0
-    assert lib.swiglu_mlp_workspace_size(128, 3584, 18944) == 128 * 18944 * 2 + n
+    # 7B, M = 512: 112 tiles of 128 x 128 do not fit clusters in one wave ->
+    # CTA pairs, K split into slices whose FP32 partial sums go to the workspace
+    n = lib.swiglu_linear_workspace_size(512, 3584, 18944)
+    assert n > 0 and n % (512 * 3584 * 4) == 0
+    assert lib.swiglu_mlp_workspace_size(512, 3584, 18944) == 512 * 18944 * 2 + n
     assert lib.swiglu_linear_workspace_size(8192, 896, 4864) == 0      # enough tiles: no split
     assert lib.swiglu_linear_workspace_size(0, 896, 4864) == 0

@@ -44,13 +44,16 @@ def _status(sg):
     assert rc == sg.OK, f"device status {sg.status_string(rc)} detail {detail}"
 
 
-# Few output tiles (small M) run the split-K cluster kernel: (63, 136, 200),
-# (257, 392, 264), (300, 512, 1000), (200, 896, 4864) with 4 CTAs per tile,
-# (128, 896, 4864), (100, 264, 520) and (64, 72, 4864) (a ragged last tile)
-# with 8; the others the CTA-pair kernel.
+# Few output tiles (small M) run the split-K cluster kernel: 64-column tiles
+# over 4 CTAs for (63, 136, 200), (257, 392, 264), (300, 512, 1000) and
+# (200, 896, 4864), over 8 for (128, 896, 4864), (100, 264, 520) and
+# (64, 72, 4864) (a ragged last tile); 128-column tiles over 4 CTAs for
+# (512, 896, 4864) and (128, 2600, 1000) (a ragged last tile), over 2 for
+# (1024, 896, 4864); the others run the CTA-pair kernel.
 @pytest.mark.parametrize("shape", [(1, 8, 8), (63, 136, 200), (257, 392, 264), (300, 512, 1000),
                                    (128, 896, 4864), (200, 896, 4864), (2048, 3584, 1024),
-                                   (100, 264, 520), (64, 72, 4864)],
+                                   (100, 264, 520), (64, 72, 4864), (512, 896, 4864),
+                                   (128, 2600, 1000), (1024, 896, 4864)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("with_r", [False, True])
 @pytest.mark.parametrize("with_ws", [True, False])
