@@ -117,6 +117,47 @@ def load_traffic(kernel_key: str):
     return ent.get("dram_bytes_per_launch")
 
 
+# Kernel sources a traffic record depends on, by kernel family.
+TRAFFIC_SOURCES = {
+    "pair": ["sm103_ptx.cuh", "tc_common.cuh", "swiglu_tc2_kernel.cuh", "swiglu_tc_kernel.cuh",
+             "launch_tc.cuh", "launch.h", "k_bf16_separate.cu", "k_bf16_interleaved.cu",
+             "swiglu_api.cu"],
+    "sk": ["k_bf16_sk.cu", "launch.h", "sm103_ptx.cuh", "swiglu_api.cu", "swiglu_sk_kernel.cuh",
+           "tc_common.cuh", "weight_decode.cuh"],
+}
+
+
+def record_traffic(csv_path: str, kernel_key: str, family: str, capture: str):
+    """Write one traffic record from an ncu CSV of dram__bytes_read.sum and
+    dram__bytes_write.sum (one captured launch), stamped with the digest of
+    the current kernel sources.  Run right after the capture, on the sources
+    it was taken on."""
+    import csv
+    vals = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f)]
+    hdr = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    for r in rows[hdr + 1:]:
+        d = dict(zip(rows[hdr], r))
+        if d.get("Metric Name") in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[d["Metric Unit"]]
+            vals[d["Metric Name"]] = int(round(float(d["Metric Value"].replace(",", "")) * scale))
+    rd, wr = vals["dram__bytes_read.sum"], vals["dram__bytes_write.sum"]
+    try:
+        with open(TRAFFIC_FILE) as f:
+            table = json.load(f)
+    except FileNotFoundError:
+        table = {}
+    srcs = TRAFFIC_SOURCES[family]
+    table[kernel_key] = {"dram_bytes_per_launch": rd + wr, "dram_read_bytes": rd,
+                         "dram_write_bytes": wr, "sources": srcs,
+                         "source_digest": source_digest(srcs), "capture": capture}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(table, f, indent=2)
+        f.write("\n")
+    return table[kernel_key]
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle sampling while the timed region runs."""
 
@@ -811,9 +852,37 @@ def run_context(args, wl, stream, fused_us, hbm_gbs):
                      "tflops": round(wl.flops / (ms * 1e-3) / 1e12, 2),
                      "per_call_us": [round(u, 3) for u in eager_us]},
            "fusion": fusion_report(wl, fused_us, eager_us, hbm_gbs)}
+    one = one_gemm_context(args, wl, stream)
+    if one is not None:
+        out["one_gemm_same_weight_bytes"] = one
     if not args.no_compile_context:
         out["compile"] = run_compile_context(args, wl, stream, fused_us)
     return out
+
+
+def one_gemm_context(args, wl, stream):
+    """A library floor for reading the same bytes: one cuBLAS GEMM A @ W_fused
+    ([K, 2N], the gate and up weights side by side) per call, timed like the
+    fused calls.  It reads the weights the fused call reads, once, and writes
+    the [M, 2N] product unfused (twice Y's bytes); for small M, where the
+    weights dominate, it is what a tuned library takes to stream them."""
+    import torch
+    if wl.kind != "bf16":
+        return None
+    pairs = {}
+    for (form, M, v), bufs in zip(wl.calls, wl.buffers):
+        if form == "interleaved" and M not in pairs:
+            pairs[M] = ((form, M, v), bufs)
+    if any(M not in pairs for (_, M, _) in wl.calls):
+        return None
+
+    def factory(form, M, v, bufs):
+        A, Wf = bufs[0], bufs[1]
+        return lambda: torch.matmul(A, Wf)
+    by_m = dict(zip(pairs, measure_calls(wl, stream, args.call_launches, factory,
+                                         list(pairs.values()))))
+    return {"what": "cuBLAS A @ W_fused (one GEMM over the same weight bytes, [M, 2N] output)",
+            "per_call_us": [round(by_m[M], 3) for (_, M, _) in wl.calls]}
 
 
 def run_compile_context(args, wl, stream, fused_us):
@@ -1088,12 +1157,18 @@ def main():
                     help="time every variant of every configuration and write the table to this file")
     ap.add_argument("--sweep-workloads", default="",
                     help="comma-separated workloads for --sweep (default: all BF16 and weight formats)")
+    ap.add_argument("--record-traffic", nargs=4, metavar=("CSV", "KERNEL_KEY", "FAMILY", "CAPTURE"),
+                    help="write a traffic record from an ncu CSV (no GPU work)")
     ap.add_argument("--only", default="",
                     help="restrict the step to calls FORM:M[,FORM:M...] (profiling a single kernel)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     ws, rank, local = dist_env()
+
+    if args.record_traffic:
+        print(json.dumps(record_traffic(*args.record_traffic)))
+        return
 
     if args.sweep:
         table = run_sweep(args)
