@@ -1074,7 +1074,7 @@ def run_reference(args, ws, rank):
 SWEEP_BF16 = ("qwen2.5-0.5b-m64", "qwen2.5-0.5b", "qwen2.5-7b", "qwen2.5-72b")
 SWEEP_WEIGHTS = ("qwen2.5-0.5b-w4", "qwen2.5-7b-w4", "qwen2.5-0.5b-mxfp8", "qwen2.5-7b-mxfp8",
                  "qwen2.5-0.5b-nvfp4", "qwen2.5-7b-nvfp4")
-SWEEP_VARIANTS = ("1sm_n128", "1sm_n64", "1sm_n32", "2sm_n128", "1sm_n64_sk2", "2sm_n64")
+SWEEP_VARIANTS = ("1sm_n128", "1sm_n64", "1sm_n32", "2sm_n128", "1sm_n64_sk2")
 
 
 def run_sweep(args):
@@ -1141,8 +1141,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", default="auto",
-                    choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n64_sk2",
-                             "2sm_n64"))
+                    choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n64_sk2"))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--call-launches", type=int, default=96,
                     help="launches per call when timing calls one by one")

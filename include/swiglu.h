@@ -74,12 +74,7 @@ typedef enum {
        accumulators are summed through distributed shared memory before the
        activation; all of a CTA's weight and A bytes fit in flight at once */
     SWIGLU_VARIANT_1SM_N64_SK2 = 9,
-    /* CTA pair, 256-row tiles of 64 output columns (gate 64 + up 64 in one
-       MMA): twice the tiles of SWIGLU_VARIANT_2SM_N128, so a pair's next tile
-       hides the previous tile's epilogue when the larger tiles would fill the
-       GPU only once (mid M) */
-    SWIGLU_VARIANT_2SM_N64 = 10,
-    SWIGLU_VARIANT_COUNT_ = 11
+    SWIGLU_VARIANT_COUNT_ = 10
 } swiglu_variant;
 
 /*

@@ -15,8 +15,6 @@ cudaError_t launch_bf16_interleaved(int variant, const LaunchArgs &la) {
       return launch_tc<TileCfg<1, 64, true, 8>>(la);
     case SWIGLU_VARIANT_2SM_N128:
       return launch_pair<PairCfg<true, 6>>(la);
-    case SWIGLU_VARIANT_2SM_N64:
-      return launch_pair<PairCfg<true, 8, false, false, 256, 64>>(la);
     default:
       return cudaErrorInvalidValue;
   }

@@ -15,8 +15,6 @@ cudaError_t launch_bf16_separate(int variant, const LaunchArgs &la) {
       return launch_tc<TileCfg<2, 32, false, 8>>(la);
     case SWIGLU_VARIANT_2SM_N128:
       return launch_pair<PairCfg<false, 6>>(la);
-    case SWIGLU_VARIANT_2SM_N64:
-      return launch_pair<PairCfg<false, 8, false, false, 256, 64>>(la);
     default:
       return cudaErrorInvalidValue;
   }

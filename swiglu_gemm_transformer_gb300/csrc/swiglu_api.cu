@@ -175,7 +175,7 @@ int pair_group_m() {
 bool variant_known(int32_t v) {
   return v == SWIGLU_VARIANT_AUTO || v == SWIGLU_VARIANT_1SM_N128 || v == SWIGLU_VARIANT_1SM_N64 ||
          v == SWIGLU_VARIANT_2SM_N128 || v == SWIGLU_VARIANT_1SM_N32 ||
-         v == SWIGLU_VARIANT_1SM_N64_SK2 || v == SWIGLU_VARIANT_2SM_N64;
+         v == SWIGLU_VARIANT_1SM_N64_SK2;
 }
 
 // Kernel for the weight formats (INT4, MXFP8, NVFP4): 0 = the split-K
@@ -702,7 +702,6 @@ VariantGeom variant_geom(int variant, bool interleaved) {
       return interleaved ? VariantGeom{128, 32, 64, 64, 0, 128, 1}
                          : VariantGeom{128, 32, 64, 32, 1, 128, 1};
     case SWIGLU_VARIANT_2SM_N128: return {256, 128, 64, 64, 0, 128, 2};
-    case SWIGLU_VARIANT_2SM_N64: return {256, 64, 64, 64, 0, 128, 2};
     case SWIGLU_VARIANT_1SM_N64_SK2: return {128, 64, 64, 64, 0, 128, 2};
     case SWIGLU_VARIANT_1SM_N128:
     default: return {128, 128, 64, 64, 0, 128, 1};
@@ -883,7 +882,6 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_2SM_N128: return "2sm_n128";
     case SWIGLU_VARIANT_1SM_N32: return "1sm_n32";
     case SWIGLU_VARIANT_1SM_N64_SK2: return "1sm_n64_sk2";
-    case SWIGLU_VARIANT_2SM_N64: return "2sm_n64";
     default: return "?";
   }
 }

@@ -36,14 +36,13 @@ namespace swiglu {
 // FP8 = false: BF16 operands, weights MN-major ([K,N] row-major), 64 K per stage.
 // FP8 = true : E4M3 operands, weights K-major ([N,K] row-major), 128 K per stage;
 //              the epilogue applies the per-tensor scales.
-// LINEAR = false: the fused SwiGLU epilogue (MMA N = 2 FUSED_N = FUSED_N gate
-//                 + FUSED_N up columns, FUSED_N = 128 or 64 output columns per
-//                 tile).
+// LINEAR = false: the fused SwiGLU epilogue (MMA N = 256 = 128 gate + 128 up
+//                 columns, 128 output columns per tile).
 // LINEAR = true : a plain product Z = X W (+ R) with LIN_N output columns per
 //                 tile (MMA N = LIN_N = 256 or 128); the weight block of one
 //                 tile is split between the two CTAs like the interleaved form.
 template <bool INTERLEAVED_, int STAGES_, bool FP8_ = false, bool LINEAR_ = false,
-          int LIN_N = 256, int FUSED_N = 128>
+          int LIN_N = 256>
 struct PairCfg {
   static constexpr bool LINEAR = LINEAR_;
   static constexpr bool INTERLEAVED = INTERLEAVED_ || LINEAR_;  // one weight matrix
@@ -53,8 +52,8 @@ struct PairCfg {
   static constexpr int BK = FP8 ? 128 : 64;      // K per stage: 128 bytes of each A row
   static constexpr int MMA_K = FP8 ? 32 : 16;    // K of one MMA instruction (32 bytes)
   static constexpr int MMA_M = 256;
-  static constexpr int MMA_N = LINEAR ? LIN_N : 2 * FUSED_N;  // accumulator columns per tile
-  static constexpr int BN = LINEAR ? LIN_N : FUSED_N;         // output columns per tile
+  static constexpr int MMA_N = LINEAR ? LIN_N : 256;  // accumulator columns per tile
+  static constexpr int BN = LINEAR ? LIN_N : 128;     // output columns per tile
   static constexpr int A_BYTES = BM * 128;       // 16 KB
   // BF16: MN-major boxes of 64 columns x 64 K-rows (MMA_N/128 of them per
   // CTA); FP8: one K-major box of this CTA's 128 weight rows x 128 K bytes.
@@ -62,7 +61,6 @@ struct PairCfg {
   static constexpr int B_ATOMS = FP8 ? 1 : MMA_N / 128;
   static_assert(!(LINEAR && FP8), "linear mode is BF16");
   static_assert(LIN_N == 256 || LIN_N == 128, "linear tile width");
-  static_assert(FUSED_N == 128 || (FUSED_N == 64 && !FP8), "fused tile width");
   static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
   static constexpr int EPI_WARPS = 8;
