@@ -1141,7 +1141,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", default="auto",
-                    choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n64_sk2"))
+                    choices=("auto", "1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n64_sk2",
+                             "2sm_swap"))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--call-launches", type=int, default=96,
                     help="launches per call when timing calls one by one")

@@ -74,7 +74,14 @@ typedef enum {
        accumulators are summed through distributed shared memory before the
        activation; all of a CTA's weight and A bytes fit in flight at once */
     SWIGLU_VARIANT_1SM_N64_SK2 = 9,
-    SWIGLU_VARIANT_COUNT_ = 10
+    /* M <= 128 only: the transposed product on CTA pairs (tcgen05
+       cta_group::2 with the weights on the MMA's M side, M = 128 weight rows,
+       and A's rows on its N side, half in each CTA); each pair makes 64
+       output columns for all rows over all of K, so a CTA's whole K range of
+       weights and A fits in flight at once and no partial sums are
+       exchanged */
+    SWIGLU_VARIANT_2SM_SWAP = 10,
+    SWIGLU_VARIANT_COUNT_ = 11
 } swiglu_variant;
 
 /*

@@ -22,9 +22,10 @@ LIB_PATH = os.path.join(_HERE, "libswiglu_gb300.so")
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
 VARIANT_AUTO, VARIANT_1SM_N128, VARIANT_1SM_N64, VARIANT_2SM_N128, VARIANT_1SM_N32 = range(5)
 VARIANT_1SM_N64_SK2 = 9   # 5-8 are retired numbers the library rejects
+VARIANT_2SM_SWAP = 10
 VARIANTS = {"auto": VARIANT_AUTO, "1sm_n128": VARIANT_1SM_N128, "1sm_n64": VARIANT_1SM_N64,
             "2sm_n128": VARIANT_2SM_N128, "1sm_n32": VARIANT_1SM_N32,
-            "1sm_n64_sk2": VARIANT_1SM_N64_SK2}
+            "1sm_n64_sk2": VARIANT_1SM_N64_SK2, "2sm_swap": VARIANT_2SM_SWAP}
 
 EXPORTS = {
     # name: (argtypes, restype)

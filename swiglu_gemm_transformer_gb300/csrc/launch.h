@@ -55,6 +55,8 @@ VariantGeom variant_geom(int variant, bool interleaved);
 cudaError_t launch_bf16_separate(int variant, const LaunchArgs &la);
 cudaError_t launch_bf16_interleaved(int variant, const LaunchArgs &la);
 cudaError_t launch_bf16_sk(bool interleaved, const LaunchArgs &la);
+// rows: 64 or 128 rows of A per CTA pair (M <= rows); la.p.num_n_blk pairs of 64 columns
+cudaError_t launch_bf16_swab(bool interleaved, int rows, const LaunchArgs &la);
 cudaError_t launch_w4_sk(const LaunchArgs &la);
 cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la);
 // wf: 1 INT4, 2 MXFP8, 3 NVFP4 (weight_decode.cuh); m_blocks: 128-row blocks

@@ -175,7 +175,7 @@ int pair_group_m() {
 bool variant_known(int32_t v) {
   return v == SWIGLU_VARIANT_AUTO || v == SWIGLU_VARIANT_1SM_N128 || v == SWIGLU_VARIANT_1SM_N64 ||
          v == SWIGLU_VARIANT_2SM_N128 || v == SWIGLU_VARIANT_1SM_N32 ||
-         v == SWIGLU_VARIANT_1SM_N64_SK2;
+         v == SWIGLU_VARIANT_1SM_N64_SK2 || v == SWIGLU_VARIANT_2SM_SWAP;
 }
 
 // Kernel for the weight formats (INT4, MXFP8, NVFP4): 0 = the split-K
@@ -220,9 +220,52 @@ int choose_variant(int64_t M, int64_t N, int64_t K, bool /*interleaved*/, int sm
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
+// The swapped-operand CTA-pair kernel (M <= 128): one pair per 64 output
+// columns, A's rows padded to 64 or 128 (half in each CTA of the pair).
+int run_bf16_swab(const void *A, const void *B0, const void *B1, void *Y, int64_t M, int64_t N,
+                  int64_t K, bool interleaved, DeviceState *st, int dev, cudaStream_t s) {
+  if (M > 128) return SWIGLU_ERR_UNSUPPORTED;
+  const int rows = M <= 64 ? 64 : 128;
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof la);
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, rows / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == SWIGLU_OK) {
+    if (interleaved) {
+      rc = encode_2d(&la.b0, BF16, B0, 2 * N, K, 4 * N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+      la.b1 = la.b0;
+    } else {
+      rc = encode_2d(&la.b0, BF16, B0, N, K, 2 * N, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+      if (rc == SWIGLU_OK)
+        rc = encode_2d(&la.b1, BF16, B1, N, K, 2 * N, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+  }
+  if (rc == SWIGLU_OK)
+    rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != SWIGLU_OK) return rc;
+  KParams &p = la.p;
+  p.M = int32_t(M);
+  p.N = int32_t(N);
+  p.K = int32_t(K);
+  p.num_m_blk = 1;
+  p.num_n_blk = int32_t(cdiv(N, 64));
+  p.num_k_blk = int32_t(cdiv(K, 64));
+  p.group_m = 1;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.err = st->err;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blk;
+  p.Y = Y;
+  la.device = dev;
+  la.ctx_gen = st->gen;
+  la.stream = s;
+  return launch_bf16_swab(interleaved, rows, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
 int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, int64_t N,
              int64_t K, int32_t variant, bool interleaved, void *stream) {
   if (!variant_known(variant)) return SWIGLU_ERR_INVALID_ARG;
+  if (variant == SWIGLU_VARIANT_2SM_SWAP && M > 128) return SWIGLU_ERR_UNSUPPORTED;
   if (M < 0 || N < 0 || K < 0) return SWIGLU_ERR_INVALID_ARG;
   if (M > kMaxDim || K > kMaxDim || 2 * N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return SWIGLU_OK;
@@ -247,6 +290,8 @@ int run_bf16(const void *A, const void *B0, const void *B1, void *Y, int64_t M, 
     return cudaMemsetAsync(Y, 0, y_bytes, s) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
   }
   if (variant == SWIGLU_VARIANT_AUTO) variant = choose_variant(M, N, K, interleaved, st->sm_count);
+  if (variant == SWIGLU_VARIANT_2SM_SWAP)
+    return run_bf16_swab(A, B0, B1, Y, M, N, K, interleaved, st, dev, s);
   const VariantGeom g = variant_geom(variant, interleaved);
   const CUtensorMapSwizzle bsw =
       g.b_swizzle_64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
@@ -882,6 +927,7 @@ const char *swiglu_variant_name(int32_t variant) {
     case SWIGLU_VARIANT_2SM_N128: return "2sm_n128";
     case SWIGLU_VARIANT_1SM_N32: return "1sm_n32";
     case SWIGLU_VARIANT_1SM_N64_SK2: return "1sm_n64_sk2";
+    case SWIGLU_VARIANT_2SM_SWAP: return "2sm_swap";
     default: return "?";
   }
 }

@@ -103,6 +103,8 @@ def test_fused_argument_validation(lib, args, want):
 def test_bad_variant_rejected(lib):
     assert lib.swiglu_fused_ex(A_, W1_, W2_, Y_, 64, 64, 64, 77, None) == sg.ERR_INVALID_ARG
     assert lib.swiglu_fused_interleaved_ex(A_, W1_, Y_, 64, 64, 64, -1, None) == sg.ERR_INVALID_ARG
+    # the swapped-operand kernel takes at most 128 rows
+    assert lib.swiglu_fused_ex(A_, W1_, W2_, Y_, 129, 64, 64, sg.VARIANT_2SM_SWAP, None) == sg.ERR_UNSUPPORTED
     for retired in (5, 6, 7, 8):   # numbers of withdrawn variants stay unused
         assert lib.swiglu_fused_ex(A_, W1_, W2_, Y_, 64, 64, 64, retired, None) == sg.ERR_INVALID_ARG
         assert lib.swiglu_fused_interleaved_ex(A_, W1_, Y_, 64, 64, 64, retired, None) == sg.ERR_INVALID_ARG

@@ -56,7 +56,9 @@ def _check(Y, A, W1, W2, rows=None, what=""):
 
 
 FORMS = ["separate", "interleaved"]
-VARIANTS = ["1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n64_sk2"]
+VARIANTS = ["1sm_n128", "1sm_n64", "2sm_n128", "1sm_n32", "1sm_n64_sk2", "2sm_swap"]
+# rows of A the swapped-operand pair kernel takes (one 128-row group per pair)
+SWAP_MAX_M = 128
 
 SMALL_SHAPES = [
     # (M, N, K): tails in every dimension, several tiles
@@ -77,9 +79,31 @@ SMALL_SHAPES = [
 @pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_small_shapes_full_compare(sg, form, variant, shape):
     M, N, K = shape
+    if variant == "2sm_swap" and M > SWAP_MAX_M:
+        pytest.skip("the swapped-operand kernel takes at most 128 rows")
     A, W1, W2 = si.make_bf16(M, N, K, seed=M + N + K)
     Y = _run(sg, form, A, W1, W2, sg.VARIANTS[variant])
     _check(Y, A, W1, W2, what=f"{form} {variant} {shape}")
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("shape", [(64, 4864, 896), (128, 4864, 896), (100, 200, 1000),
+                                   (33, 4872, 904)], ids=lambda s: "x".join(map(str, s)))
+def test_swap_kernel_full_compare(sg, form, shape):
+    """The swapped-operand pair kernel on the 0.5B shapes (every element) and
+    on ragged ones: a half-empty last pair of columns, K not a multiple of 64,
+    rows not a multiple of 32."""
+    M, N, K = shape
+    A, W1, W2 = si.make_bf16(M, N, K, seed=M + 3 * N + K)
+    Y = _run(sg, form, A, W1, W2, sg.VARIANT_2SM_SWAP)
+    _check(Y, A, W1, W2, what=f"swap {form} {shape}")
+
+
+def test_swap_kernel_rejects_more_than_128_rows(sg):
+    A, W1, W2 = (t.to(DEV) for t in si.make_bf16(129, 64, 64, seed=1))
+    with pytest.raises(sg.SwigluError) as e:
+        sg.swiglu_fused(A, W1, W2, variant=sg.VARIANT_2SM_SWAP)
+    assert e.value.status == sg.ERR_UNSUPPORTED
 
 
 def test_pack_is_bit_exact(sg):
