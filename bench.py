@@ -1074,7 +1074,8 @@ def run_reference(args, ws, rank):
 SWEEP_BF16 = ("qwen2.5-0.5b-m64", "qwen2.5-0.5b", "qwen2.5-7b", "qwen2.5-72b")
 SWEEP_WEIGHTS = ("qwen2.5-0.5b-w4", "qwen2.5-7b-w4", "qwen2.5-0.5b-mxfp8", "qwen2.5-7b-mxfp8",
                  "qwen2.5-0.5b-nvfp4", "qwen2.5-7b-nvfp4")
-SWEEP_VARIANTS = ("1sm_n128", "1sm_n64", "1sm_n32", "2sm_n128", "1sm_n64_sk2")
+SWEEP_VARIANTS = ("1sm_n128", "1sm_n64", "1sm_n32", "2sm_n128", "1sm_n64_sk2", "2sm_swap")
+SWEEP_MAX_M = {"2sm_swap": 128}   # variants that take a bounded number of rows
 
 
 def run_sweep(args):
@@ -1100,6 +1101,8 @@ def run_sweep(args):
             us = {}
             if wl.kind == "bf16":
                 for vn in SWEEP_VARIANTS:
+                    if M > SWEEP_MAX_M.get(vn, M):
+                        continue
                     us[vn] = round(measure_calls(wl, stream, args.call_launches, None,
                                                  [((form, M, sg.VARIANTS[vn]), bufs)])[0], 3)
                 auto = sg.variant_name(v)
