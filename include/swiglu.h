@@ -334,6 +334,17 @@ int swiglu_select_weight_kernel(int64_t M, int64_t N);
  * Returns SWIGLU_ERR_INVALID_ARG for other values. */
 int swiglu_set_weight_kernel(int32_t kernel);
 
+/* Tile schedule of the CTA-pair kernels (process-wide) when a call has more
+ * work units (output tiles, times K slices) than pairs fit on the device:
+ * 1 (the default) = dynamic: the grid holds one 2-CTA cluster per unit and
+ * every running pair, after its own unit, cancels clusters that have not
+ * started (cluster launch control) and computes their units, so units run in
+ * about launch order and tiles that share A rows and weight columns meet in
+ * L2; 0 = static: one wave of pairs, pair c computing units c, c + pairs, ...
+ * Results are identical.  For comparisons and tests; returns
+ * SWIGLU_ERR_INVALID_ARG for other values. */
+int swiglu_set_pair_schedule(int32_t dynamic);
+
 /* Short name of a variant ("1sm_n128", ...); "?" for an unknown value. */
 const char *swiglu_variant_name(int32_t variant);
 
@@ -346,6 +357,10 @@ const char *swiglu_status_string(int32_t status);
  * the last call (its CTA stopped early, so that launch's Y is incomplete), or
  * SWIGLU_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
  * NULL it receives a code naming the wait that gave up (0 if none).
+ * While a timeout stays recorded (until this call clears it), launches of the
+ * CTA-pair kernel that run more than one wave of tiles skip their work, so a
+ * kernel that keeps timing out ends within about one time limit instead of
+ * one per wave; read the status after any call whose result matters.
  */
 int swiglu_device_status(void *stream, uint32_t *detail);
 

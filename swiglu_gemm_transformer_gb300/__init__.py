@@ -51,6 +51,7 @@ EXPORTS = {
     "swiglu_select_variant": ("lll i", ctypes.c_int),
     "swiglu_select_weight_kernel": ("ll", ctypes.c_int),
     "swiglu_set_weight_kernel": ("i", ctypes.c_int),
+    "swiglu_set_pair_schedule": ("i", ctypes.c_int),
     "swiglu_variant_name": ("i", ctypes.c_char_p),
     "swiglu_status_string": ("i", ctypes.c_char_p),
     "swiglu_device_status": ("p P", ctypes.c_int),
@@ -508,6 +509,12 @@ def swiglu_set_weight_kernel(kernel: int):
     """Force the weight-format kernel (0 split-K, 1 wide, 2 wide with two row
     blocks per CTA) for later calls, or -1 for the library's choice."""
     _check("swiglu_set_weight_kernel", lib().swiglu_set_weight_kernel(int(kernel)))
+
+
+def swiglu_set_pair_schedule(dynamic: int):
+    """Tile schedule of the CTA-pair kernels when a call has more units than
+    resident pairs: 1 dynamic (cluster launch control, the default), 0 static."""
+    _check("swiglu_set_pair_schedule", lib().swiglu_set_pair_schedule(int(dynamic)))
 
 
 def swiglu_device_status(stream=None):

@@ -63,6 +63,9 @@ cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la);
 // per CTA (1, or 2 with la.p.num_m_blk counting 256-row blocks)
 cudaError_t launch_dq_kernel(int wf, int m_blocks, const LaunchArgs &la);
 int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *ctx_gen);
+// CTA-pair kernels: whether launches with more units than resident pairs use
+// the dynamic unit schedule.
+bool pair_dynamic_schedule();
 cudaError_t launch_pack_interleaved_u16(const void *W1, const void *W2, void *Wf, int64_t n_elems,
                                         int sm_count, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t *err, cudaStream_t s);

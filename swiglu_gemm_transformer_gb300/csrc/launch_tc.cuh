@@ -72,10 +72,15 @@ cudaError_t launch_pair(const LaunchArgs &la) {
   const int64_t tiles =
       int64_t(la.p.num_m_blk) * la.p.num_n_blk * (la.p.k_splits > 1 ? la.p.k_splits : 1);
   const int n = max_clusters[la.device & 63];
-  const int clusters = int(tiles < n ? tiles : n);
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  // One wave: one cluster per unit, static.  More units than resident pairs:
+  // the dynamic schedule (one cluster per unit, taken over by running pairs)
+  // unless turned off; else one wave of pairs walking the units statically.
+  KParams p = la.p;
+  p.dyn_sched = tiles > n && tiles <= (int64_t(1) << 30) && pair_dynamic_schedule() ? 1 : 0;
+  const int64_t clusters = p.dyn_sched ? tiles : (tiles < n ? tiles : n);
+  cfg.gridDim = dim3(unsigned(2 * clusters), 1, 1);
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, la.p);
+  return cudaLaunchKernelEx(&cfg, kern, la.a, la.b0, la.b1, la.y, p);
 }
 
 }  // namespace swiglu

@@ -261,6 +261,60 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Relaxed arrive (no memory ordering) on an mbarrier anywhere in the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Relaxed arrive.expect_tx on an mbarrier anywhere in the cluster.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster_relaxed(uint32_t cluster_addr,
+                                                                      uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;"
+               ::"r"(cluster_addr), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+// ---- cluster launch control --------------------------------------------------
+
+// Ask the hardware to cancel the launch of one cluster of this grid that has
+// not started yet.  The 16-byte response is written at `resp` in every CTA of
+// this cluster, and 16 bytes are counted (complete_tx) on the mbarrier at
+// `bar` in each of them.  Issue by one thread of the cluster; after one
+// response that reports no cancellation, issue no more.
+__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+      ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Decode a response: true when a cluster was cancelled, with the x index of
+// its first CTA in `first_x`.
+__device__ __forceinline__ bool clc_response(uint32_t resp, int &first_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .b64 lo, hi;\n\t.reg .pred p;\n\t"
+      "ld.shared.v2.b64 {lo, hi}, [%2];\n\t"
+      "mov.b128 r, {lo, hi};\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  first_x = static_cast<int>(x);
+  return ok != 0;
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");

@@ -55,6 +55,10 @@ std::atomic<int> g_linear_n{0};
 // once, for tuning sweeps.
 std::atomic<int> g_linear_sk{-1};
 std::atomic<int> g_linear_skn{0};
+// CTA-pair kernels with more units than resident pairs: 1 = dynamic unit
+// schedule (cluster launch control), 0 = static (swiglu_set_pair_schedule;
+// the SWIGLU_PAIR_SCHED=static environment variable, read once, sets 0).
+std::atomic<int> g_pair_dyn{1};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 using CtxGetCurrentFn = CUresult (*)(CUcontext *);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
@@ -132,6 +136,9 @@ int device_state(DeviceState **out, int *dev_out) {
     if (const char *e = std::getenv("SWIGLU_LINEAR_SK")) {
       const long v = std::strtol(e, nullptr, 10);
       if (v == 0 || v == 2 || v == 4 || v == 8) g_linear_sk.store(int(v), std::memory_order_relaxed);
+    }
+    if (const char *e = std::getenv("SWIGLU_PAIR_SCHED")) {
+      if (std::strcmp(e, "static") == 0) g_pair_dyn.store(0, std::memory_order_relaxed);
     }
     if (const char *e = std::getenv("SWIGLU_LINEAR_SKN")) {
       const long v = std::strtol(e, nullptr, 10);
@@ -768,6 +775,8 @@ int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *c
   return SWIGLU_OK;
 }
 
+bool pair_dynamic_schedule() { return g_pair_dyn.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace swiglu
 
 extern "C" {
@@ -916,6 +925,12 @@ int swiglu_select_weight_kernel(int64_t M, int64_t N) {
 int swiglu_set_weight_kernel(int32_t kernel) {
   if (kernel < -1 || kernel > 2) return SWIGLU_ERR_INVALID_ARG;
   g_weight_kernel_forced.store(kernel, std::memory_order_relaxed);
+  return SWIGLU_OK;
+}
+
+int swiglu_set_pair_schedule(int32_t dynamic) {
+  if (dynamic != 0 && dynamic != 1) return SWIGLU_ERR_INVALID_ARG;
+  g_pair_dyn.store(dynamic, std::memory_order_relaxed);
   return SWIGLU_OK;
 }
 

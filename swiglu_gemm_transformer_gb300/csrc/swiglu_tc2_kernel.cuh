@@ -22,6 +22,14 @@
 // density, section "Definizione del Problema") use tcgen05.mma.kind::f8f6f4
 // with K-major weights; the epilogue multiplies the gate and up accumulators
 // by sA*sW1 and sA*sW2 before SiLU.
+// Unit schedule: with more units than resident pairs the grid holds one
+// cluster per unit, and a running pair, after its own unit, cancels clusters
+// that have not started yet (cluster launch control) and takes over their
+// units.  The units therefore run in about launch order however far the
+// pairs drift apart, which keeps the tiles that share A rows and weight
+// columns close together in time, and so in L2.  The leader's producer thread
+// requests the next unit while the current one loads; the 16-byte response
+// lands in both CTAs and every role reads it from a small ring.
 // Waits are bounded as in the one-CTA kernel.
 #pragma once
 
@@ -66,9 +74,15 @@ struct PairCfg {
   static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 64;
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // unit-schedule responses: a ring of SCHED_D 16-byte slots
+  static constexpr int SCHED_D = 4;
+  static constexpr int RESP_OFF = STG_OFF + EPI_WARPS * 2 * STG_BYTES;
+  static constexpr int BAR_OFF = RESP_OFF + SCHED_D * 16;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SCHED_D;
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
+  // readers of every response: both producers, the MMA thread and the
+  // epilogue warps of both CTAs
+  static constexpr int SCHED_READERS = 2 + 1 + 2 * EPI_WARPS;
   static constexpr int TMEM_COLS = 2 * MMA_N;
   static constexpr int PRODUCER_WARP = EPI_WARPS;
   static constexpr int MMA_WARP = EPI_WARPS + 1;
@@ -95,8 +109,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto accf_bar = [&](int b) { return bars + 8u * (2 * C::STAGES + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (2 * C::STAGES + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 4);
+  // response slot s: filled (both CTAs) / read by all readers (leader only)
+  auto schf_bar = [&](uint32_t s) { return bars + 8u * (2 * C::STAGES + 5 + s); };
+  auto sche_bar = [&](uint32_t s) { return bars + 8u * (2 * C::STAGES + 5 + C::SCHED_D + s); };
+  auto resp = [&](uint32_t s) { return base + C::RESP_OFF + 16u * s; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile uint32_t *skip_word = tmem_slot + 2;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -114,7 +133,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ptx::mbar_init(acce_bar(b), 2 * C::EPI_WARPS);
     }
     ptx::mbar_init(drain_bar, 1);
+    for (uint32_t i = 0; i < (uint32_t)C::SCHED_D; ++i) {
+      ptx::mbar_init(schf_bar(i), 1);
+      ptx::mbar_init(sche_bar(i), C::SCHED_READERS);
+    }
     *abort_flag = 0;
+    // Dynamic schedule: while a timeout is recorded, the clusters that start
+    // do no work (the leader decides for both CTAs), so a kernel that keeps
+    // timing out ends within about one time limit, not one per unit.
+    *skip_word = (p.dyn_sched && rank == 0 && *(volatile const uint32_t *)p.err != 0u) ? 1u : 0u;
     ptx::fence_barrier_init();
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(rank == 0 || C::INTERLEAVED ? &tmB0 : &tmB1);
@@ -145,6 +172,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     kb0 = ks * p.kb_per_split;
     kb1 = min(p.num_k_blk, kb0 + p.kb_per_split);
   };
+  // This pair's first unit (-1: none).  Response r of the dynamic schedule
+  // (ring slot r % SCHED_D) names the unit after the r-th one.
+  const bool dyn = p.dyn_sched != 0;
+  const int first_unit =
+      dyn && ptx::ld_shared_cluster_u32(ptx::mapa_shared(ptx::smem_u32(tmem_slot + 2), 0)) != 0u
+          ? -1
+          : cid;
+  // The unit after `t`, the r-th unit of this pair; false if a wait gave up.
+  // Called by one thread of each reading role.
+  auto next_unit = [&](int t, uint32_t r, int &nxt) -> bool {
+    if (!dyn) {
+      nxt = t + ncl < num_tiles ? t + ncl : -1;
+      return true;
+    }
+    const uint32_t s = r % C::SCHED_D;
+    // The response lands through the async proxy with complete_tx on this
+    // CTA's own barrier (as a TMA copy does), so a CTA-scope wait sees it.
+    if (!wait_bar(schf_bar(s), (r / C::SCHED_D) & 1u, p.timeout_ns, abort_flag, p.err,
+                  WAIT_SCHED_FULL))
+      return false;
+    int x = 0;
+    nxt = ptx::clc_response(resp(s), x) ? (x >> 1) : -1;
+    // Release the slot.  The decode above consumed the loaded response, so
+    // the read is complete before this arrive issues: no fence is needed (a
+    // cluster-scope release here cost ~0.6 us per unit on short-K shapes).
+    ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(sche_bar(s), 0));
+    return true;
+  };
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -152,7 +207,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const CUtensorMap *tmB = (C::INTERLEAVED || rank == 0) ? &tmB0 : &tmB1;
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
-      for (int t = cid; ok && t < num_tiles; t += ncl) {
+      // Leader, dynamic schedule: request the unit after the r-th one into
+      // slot r % SCHED_D once every reader has released that slot's previous
+      // response.  A request follows only a response that named a unit.
+      auto request = [&](uint32_t r) -> bool {
+        const uint32_t s = r % C::SCHED_D;
+        if (!wait_bar(sche_bar(s), ((r / C::SCHED_D) & 1u) ^ 1u, p.timeout_ns, abort_flag, p.err,
+                      WAIT_SCHED_EMPTY))
+          return false;
+        // Each CTA's barrier expects the 16 response bytes; the peer's arrive
+        // may land before or after the response (the transaction count may
+        // go negative in between).
+        ptx::mbar_arrive_expect_tx(schf_bar(s), 16);
+        ptx::mbar_arrive_expect_tx_cluster_relaxed(ptx::mapa_shared(schf_bar(s), 1), 16);
+        ptx::clc_try_cancel_all(resp(s), schf_bar(s));
+        return true;
+      };
+      int t = first_unit;
+      for (uint32_t r = 0; ok && t >= 0; ++r) {
+        if (dyn && rank == 0 && !request(r)) {
+          ok = false;
+          break;
+        }
         int mb, nb, ks, kb0, kb1;
         unit_coords(t, mb, nb, ks, kb0, kb1);
         const int arow = mb * 2 * C::BM + static_cast<int>(rank) * C::BM;
@@ -183,6 +259,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             phase ^= 1u;
           }
         }
+        if (ok) ok = next_unit(t, r, t);
       }
       if (ok) {
         // Consume the MMA-completion arrivals still due on this CTA's "empty"
@@ -201,7 +278,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
       bool ok = true;
-      for (int t = cid; ok && t < num_tiles; t += ncl) {
+      int t = first_unit;
+      for (uint32_t r = 0; ok && t >= 0; ++r) {
         int mb, nb, ks, kb0, kb1;
         unit_coords(t, mb, nb, ks, kb0, kb1);
         if (!wait_bar(acce_bar(abuf), aphase ^ 1u, p.timeout_ns, abort_flag, p.err,
@@ -247,6 +325,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           abuf = 0;
           aphase ^= 1u;
         }
+        ok = next_unit(t, r, t);
       }
       ptx::mma_commit_pair_mc(drain_bar, 0x1);
       wait_quiet(drain_bar, 0, p.timeout_ns);
@@ -265,7 +344,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       us = sa * *p.sW2;
     }
     uint32_t abuf = 0, aphase = 0, it = 0;
-    for (int t = cid; t < num_tiles; t += ncl) {
+    int t = first_unit;
+    for (uint32_t r = 0; t >= 0; ++r) {
       int mb, nb, ks, kb0, kb1;
       unit_coords(t, mb, nb, ks, kb0, kb1);
       bool ok = wait_bar(accf_bar(abuf), aphase, p.timeout_ns, abort_flag, p.err,
@@ -287,6 +367,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         abuf = 0;
         aphase ^= 1u;
       }
+      int nxt = -1;
+      ok = lane == 0 ? next_unit(t, r, nxt) : true;
+      if (!__all_sync(0xffffffffu, ok)) break;
+      t = __shfl_sync(0xffffffffu, nxt, 0);
     }
     // Shared memory must not be released while a store still reads it; the
     // stores' global writes complete before the grid does.

@@ -19,6 +19,8 @@ enum : uint32_t {
   WAIT_EPI_ACC_FULL = 4,
   WAIT_DRAIN = 5,
   WAIT_SELFTEST = 6,
+  WAIT_SCHED_FULL = 9,   // a pair kernel role waiting for the next unit's response
+  WAIT_SCHED_EMPTY = 10, // the pair's scheduler waiting for a response slot
 };
 
 constexpr uint32_t kErrTimeout = 5;  // == SWIGLU_ERR_TIMEOUT
@@ -46,7 +48,11 @@ struct KParams {
   void *Y;
   // INT4 weights: K rows per scale group (a multiple of 64).
   int32_t w4_group;
-  int32_t pad2_;
+  // CTA-pair kernels only: 1 = dynamic unit schedule (the grid holds one
+  // cluster per unit and running pairs take over the units of clusters that
+  // have not started, through cluster launch control); 0 = static (the grid
+  // holds at most one wave and pair c takes units c, c + clusters, ...).
+  int32_t dyn_sched;
 };
 
 // Bounded wait, slow path.  Returns false on timeout or when another role of

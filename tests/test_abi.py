@@ -121,6 +121,13 @@ def test_interleaved_and_pack_validation(lib):
     assert lib.swiglu_pack_interleaved(W1_, W2_, Y_, 0, 64, None) == sg.OK
 
 
+def test_pair_schedule_setter_validates(lib):
+    assert lib.swiglu_set_pair_schedule(2) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_set_pair_schedule(-1) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_set_pair_schedule(0) == sg.OK
+    assert lib.swiglu_set_pair_schedule(1) == sg.OK
+
+
 def test_timeout_setters_validate(lib):
     assert lib.swiglu_set_wait_timeout_ns(10) == sg.ERR_INVALID_ARG
     assert lib.swiglu_set_wait_timeout_ns(2_000_000_000) == sg.OK

@@ -195,6 +195,52 @@ def test_qwen_shapes_auto_variant(sg, case):
     torch.cuda.empty_cache()
 
 
+# ---- tile schedules of the CTA-pair kernel ---------------------------------------------------
+
+# More 256 x 128 tiles than CTA pairs fit on the device (3 x 31 = 93 > 76 on
+# 152 SMs), ragged in all three dimensions.
+SCHED_SHAPE = (600, 3896, 200)
+
+
+@pytest.mark.parametrize("form", FORMS)
+def test_pair_schedules_agree_with_oracle_and_each_other(sg, form):
+    """Dynamic (cluster launch control) and static schedules compute every
+    tile the same way: both match the oracle and each other bit for bit."""
+    M, N, K = SCHED_SHAPE
+    A, W1, W2 = si.make_bf16(M, N, K, seed=11)
+    rows = si.sample_rows(M, 128, 48, seed=11)
+    out = {}
+    try:
+        for dyn in (1, 0):
+            sg.swiglu_set_pair_schedule(dyn)
+            out[dyn] = _run(sg, form, A, W1, W2, sg.VARIANTS["2sm_n128"])
+    finally:
+        sg.swiglu_set_pair_schedule(1)
+    _check(out[1], A, W1, W2, rows=rows, what=f"dynamic {form}")
+    assert torch.equal(out[0].view(torch.int16), out[1].view(torch.int16))
+
+
+def test_dynamic_schedule_skips_while_a_timeout_is_recorded(sg):
+    """While a device-side timeout is recorded, a multi-wave CTA-pair launch
+    does no work (so a kernel that keeps timing out ends quickly); once the
+    status is read, the same call computes normally."""
+    M, N, K = SCHED_SHAPE
+    A, W1, W2 = si.make_bf16(M, N, K, seed=12)
+    Ad, W1d, W2d = A.to(DEV), W1.to(DEV), W2.to(DEV)
+    sentinel = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    Y = sentinel.clone()
+    sg.swiglu_selftest_wait_timeout(2000)  # records a timeout (a wait nothing completes)
+    torch.cuda.synchronize()
+    sg.swiglu_fused(Ad, W1d, W2d, Y, variant=sg.VARIANTS["2sm_n128"])
+    rc, detail = sg.swiglu_device_status()
+    assert rc == sg.ERR_TIMEOUT and detail == 6
+    assert torch.equal(Y, sentinel)
+    sg.swiglu_fused(Ad, W1d, W2d, Y, variant=sg.VARIANTS["2sm_n128"])
+    rc, _ = sg.swiglu_device_status()
+    assert rc == sg.OK
+    _check(Y, A, W1, W2, rows=si.sample_rows(M, 128, 48, seed=12), what="after the status read")
+
+
 # ---- failure detection ---------------------------------------------------------------------
 
 def test_bounded_wait_reports_timeout_and_context_survives(sg):
