@@ -268,8 +268,10 @@ class Workload:
         self.mxfmt = name.rsplit("-", 1)[1] if self.kind == "mx" else None
         self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
-        forms = (("mlp",) if self.kind == "mlp" else ("separate",) if self.kind in ("w4", "mx")
-                 else ("separate", "interleaved"))
+        # INT4: the [K, N/2] codes, and the K-major arrangement decoded into
+        # tensor memory (packed once at set-up, like a model load)
+        forms = (("mlp",) if self.kind == "mlp" else ("separate", "kmajor") if self.kind == "w4"
+                 else ("separate",) if self.kind == "mx" else ("separate", "interleaved"))
         self.host = {}
         for M in Ms:
             if self.producer:   # X and gamma in BF16; the FP8 weights of the same recipe
@@ -347,6 +349,9 @@ class Workload:
         dev, sg = self.dev, self.sg
         h = self.host[M]
         out = torch.empty(self.out_shape(M), dtype=torch.bfloat16, device=dev)
+        if self.kind == "w4" and form == "kmajor":   # (A, W1k, S1, W2k, S2, Y)
+            return (h[0].to(dev), sg.swiglu_pack_w4_kmajor(h[1].to(dev)), h[2].to(dev),
+                    sg.swiglu_pack_w4_kmajor(h[3].to(dev)), h[4].to(dev), out)
         if self.kind in ("w4", "mx"):
             return tuple(t.to(dev) for t in h) + (out,)
         if self.kind == "mlp":
@@ -378,6 +383,9 @@ class Workload:
         def check(name, rc):
             if rc:
                 raise sg.SwigluError(name, rc)
+        if self.kind == "w4" and form == "kmajor":
+            return lambda: check("swiglu_fused_w4_kmajor", lib.swiglu_fused_w4_kmajor(
+                d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, W4_GROUP, self._stream()))
         if self.kind == "w4":
             return lambda: check("swiglu_fused_w4", lib.swiglu_fused_w4(
                 d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, W4_GROUP, self._stream()))
@@ -435,6 +443,8 @@ class Workload:
     def api_call(self, form, M, v, bufs):
         """The same call through the public Python API; returns the output tensor."""
         sg = self.sg
+        if self.kind == "w4" and form == "kmajor":
+            return sg.swiglu_fused_w4_kmajor(*bufs[:5], bufs[5], group=W4_GROUP)
         if self.kind == "w4":
             return sg.swiglu_fused_w4(*bufs[:5], bufs[5], group=W4_GROUP)
         if self.kind == "mx" and self.mxfmt == "mxfp8":
@@ -466,11 +476,13 @@ class Workload:
             return 1
         return 2 + (1 if self.lib.swiglu_linear_workspace_size(M, self.K, self.N) > 0 else 0)
 
-    def variant_label(self, v, M):
+    def variant_label(self, v, M, form="separate"):
         if self.kind == "mlp":
             return "mlp"
         if self.producer:
             return "rmsnorm_quant+2sm_fp8"
+        if self.kind == "w4" and form == "kmajor":
+            return "w4_kmajor_tmem"
         if self.kind in ("w4", "mx"):   # the library's choice of kernel
             fmt = "w4" if self.kind == "w4" else self.mxfmt
             return f"{fmt}_{self.sg.WEIGHT_KERNELS[self.sg.swiglu_select_weight_kernel(M, self.N)]}"
@@ -612,7 +624,7 @@ def run_ours(args, ws, rank, local):
         r = roofline_entry(flops, abytes, us, peak_tf, peaks["hbm_gbs"])
         bound, achieved_tf, achieved_gbs = r["bound"], r["tflops"], r["gbs"]
         kernels.append({
-            "form": form, "M": M, "variant": "2sm_fp8" if wl.producer else wl.variant_label(v, M),
+            "form": form, "M": M, "variant": "2sm_fp8" if wl.producer else wl.variant_label(v, M, form),
             "us": round(us, 3),
             "tflops": round(achieved_tf, 1), "gbs": round(achieved_gbs, 1), "bound": bound,
             "frac_of_roofline": round(r["frac_of_roofline"], 4),
@@ -955,7 +967,8 @@ class OracleSampler:
             a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
             wf = oracle.pack_interleaved(w1, w2)
             w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
-        self.forms = ("mlp",) if mlp else ("separate",) if (w4 or mxf) else ("separate", "interleaved")
+        self.forms = (("mlp",) if mlp else ("separate", "kmajor") if w4 else ("separate",) if mxf
+                      else ("separate", "interleaved"))
         self.per_row = (6 if mlp else 4) * N * K
 
         def call(form, M, rows):
@@ -1103,6 +1116,8 @@ def run_sweep(args):
     for name in names:
         wl = Workload(name, dev)
         for (form, M, v), bufs in zip(wl.calls, wl.buffers):
+            if form == "kmajor":   # a separate entry point, not a choice among kernels
+                continue
             us = {}
             if wl.kind == "bf16":
                 for vn in SWEEP_VARIANTS:

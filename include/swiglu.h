@@ -178,6 +178,30 @@ int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *
                     void *stream);
 
 /*
+ * INT4 weights in a K-major layout, for few tokens (decode).  Same format and
+ * result as swiglu_fused_w4 (page section "Definizione del Problema"), with
+ * the codes rearranged once at model load by swiglu_pack_w4_kmajor:
+ *   Wk : uint8 [N, K/2]: row n holds column n's K codes, eight per 32-bit
+ *        little-endian word; word j holds codes k = 8j..8j+7 with code 8j+2i
+ *        in nibble i and code 8j+2i+1 in nibble 4+i (i = 0..3; nibble 0 = the
+ *        low four bits).
+ * swiglu_pack_w4_kmajor(Wq, Wk, K, N): Wq [K, N/2] in swiglu_fused_w4's layout
+ *   -> Wk; K a multiple of 8, N even, pointers 16-byte aligned, no overlap.
+ * swiglu_fused_w4_kmajor: Y = SiLU(A x W1) (.) (A x W2) from A [M,K], W1k,
+ *   W2k [N, K/2] (packed), S1, S2 [K/group, N] BF16 (as swiglu_fused_w4),
+ *   Y [M,N]; the same size rules as swiglu_fused_w4.  Runs the transposed
+ *   product (weights on the MMA's M side, tokens on its N side): one CTA per
+ *   128 weight columns over all of K, the codes decoded to BF16 straight into
+ *   tensor memory, the tensor core's A operand; tokens in passes of 64
+ *   (M <= 64) or 128.  Built for M <= 128; larger M repeats the decode per
+ *   128 tokens.
+ */
+int swiglu_pack_w4_kmajor(const void *Wq, void *Wk, int64_t K, int64_t N, void *stream);
+int swiglu_fused_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2k,
+                           const void *S2, void *Y, int64_t M, int64_t N, int64_t K,
+                           int64_t group, void *stream);
+
+/*
  * MXFP8 and NVFP4 weights (weight-only; the formats the GEMM page names for
  * Blackwell, read per the OCP Microscaling specification and NVIDIA's NVFP4):
  *   MXFP8: C1, C2: E4M3 codes, uint8 [K,N] row-major; S1, S2: E8M0 scales,

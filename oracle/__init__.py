@@ -85,6 +85,8 @@ def _load():
         lib.oracle_dequant_int4.argtypes = [p, p, i64, i64, i64, p]
         lib.oracle_dequant_int4.restype = ctypes.c_int
         lib.oracle_swiglu_w4.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p]
+        lib.oracle_pack_w4_kmajor.argtypes = [p, i64, i64, p]
+        lib.oracle_pack_w4_kmajor.restype = ctypes.c_int
         lib.oracle_swiglu_w4.restype = ctypes.c_int
         lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_e2m1_to_f64.restype = d
@@ -356,6 +358,16 @@ def dequant_int4(Wq, S, G: int) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_dequant_int4: K must be a multiple of G")
     return W
+
+
+def pack_w4_kmajor(Wq) -> np.ndarray:
+    """The K-major arrangement [N, K/2] of INT4 codes given as [K, N/2]."""
+    Wq = _u8(Wq)
+    K, half = Wq.shape
+    Wk = np.empty((2 * half, K // 2), dtype=np.uint8)
+    if _load().oracle_pack_w4_kmajor(_ptr(Wq), K, 2 * half, _ptr(Wk)) != 0:
+        raise ValueError("oracle_pack_w4_kmajor: K must be a multiple of 8")
+    return Wk
 
 
 def swiglu_w4(A, W1q, S1, W2q, S2, G: int, rows=None) -> np.ndarray:

@@ -551,6 +551,28 @@ int oracle_dequant_int4(const uint8_t *Wq, const uint16_t *S, int64_t K, int64_t
     return 0;
 }
 
+/* The K-major arrangement of the same INT4 codes (a storage order only; the
+ * values are unchanged): Wk [N, K/2] bytes, row n holding column n's codes;
+ * 32-bit little-endian word j of a row holds codes k = 8j..8j+7, code 8j+2i
+ * in nibble i and code 8j+2i+1 in nibble 4+i (i = 0..3), nibble p being bits
+ * [4p, 4p+4) of the word, i.e. the low half of byte p/2 when p is even. */
+int oracle_pack_w4_kmajor(const uint8_t *Wq, int64_t K, int64_t N, uint8_t *Wk)
+{
+    if (K < 0 || N < 0 || N % 2 != 0 || K % 8 != 0)
+        return -1;
+    for (int64_t i = 0; i < N * (K / 2); ++i)
+        Wk[i] = 0;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            uint8_t code = (uint8_t)((Wq[k * (N / 2) + n / 2] >> (4 * (n % 2))) & 0xF);
+            int64_t j = k / 8, r = k % 8;
+            int64_t nib = (r % 2 == 0) ? r / 2 : 4 + r / 2;
+            int64_t at = n * (K / 2) + 4 * j + nib / 2;
+            Wk[at] |= (uint8_t)(code << (4 * (nib % 2)));
+        }
+    return 0;
+}
+
 /* Y = SiLU(A W1) (.) (A W2) with W1, W2 given as INT4 + group scales. */
 int oracle_swiglu_w4(const uint16_t *A, const uint8_t *W1q, const uint16_t *S1,
                      const uint8_t *W2q, const uint16_t *S2, int64_t M, int64_t N, int64_t K,

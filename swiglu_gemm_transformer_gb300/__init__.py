@@ -40,6 +40,8 @@ EXPORTS = {
     "swiglu_rmsnorm_quant_fp8": ("pp f pp ll p", ctypes.c_int),
     "swiglu_quant_fp8": ("ppp ll p", ctypes.c_int),
     "swiglu_fused_w4": ("ppppp p lll l p", ctypes.c_int),
+    "swiglu_pack_w4_kmajor": ("pp ll p", ctypes.c_int),
+    "swiglu_fused_w4_kmajor": ("ppppp p lll l p", ctypes.c_int),
     "swiglu_fused_mxfp8": ("ppppp p lll p", ctypes.c_int),
     "swiglu_fused_nvfp4": ("pppppppp lll p", ctypes.c_int),
     "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
@@ -352,6 +354,44 @@ def swiglu_fused_w4(A, W1q, S1, W2q, S2, Y=None, *, group: int = 128, stream=Non
     rc = lib().swiglu_fused_w4(A.data_ptr(), W1q.data_ptr(), S1.data_ptr(), W2q.data_ptr(),
                                S2.data_ptr(), Y.data_ptr(), M, N, K, int(group), _stream(stream))
     _check("swiglu_fused_w4", rc)
+    return Y
+
+
+@_on_tensor_device
+def swiglu_pack_w4_kmajor(Wq, Wk=None, *, stream=None):
+    """INT4 codes [K, N/2] (swiglu_fused_w4's layout) -> the K-major layout
+    [N, K/2] that swiglu_fused_w4_kmajor reads."""
+    import torch
+    _need(Wq, "Wq", torch.uint8)
+    K, half = Wq.shape
+    N = 2 * half
+    if Wk is None:
+        Wk = torch.empty((N, K // 2), dtype=torch.uint8, device=Wq.device)
+    else:
+        _need(Wk, "Wk", torch.uint8)
+        if tuple(Wk.shape) != (N, K // 2):
+            raise ValueError("Wk must be [N, K/2]")
+    _check("swiglu_pack_w4_kmajor",
+           lib().swiglu_pack_w4_kmajor(Wq.data_ptr(), Wk.data_ptr(), K, N, _stream(stream)))
+    return Wk
+
+
+@_on_tensor_device
+def swiglu_fused_w4_kmajor(A, W1k, S1, W2k, S2, Y=None, *, group: int = 128, stream=None):
+    """swiglu_fused_w4 with the codes in the K-major layout [N, K/2] of
+    swiglu_pack_w4_kmajor (weights decoded into tensor memory)."""
+    import torch
+    _need(A, "A", torch.bfloat16)
+    _need(W1k, "W1k", torch.uint8), _need(W2k, "W2k", torch.uint8)
+    _need(S1, "S1", torch.bfloat16), _need(S2, "S2", torch.bfloat16)
+    M, K = A.shape
+    N = W1k.shape[0]
+    if W1k.shape[1] * 2 != K or W2k.shape != W1k.shape or S1.shape != (K // group, N) or S2.shape != S1.shape:
+        raise ValueError("shape mismatch")
+    Y = _out(A, N, Y)
+    rc = lib().swiglu_fused_w4_kmajor(A.data_ptr(), W1k.data_ptr(), S1.data_ptr(), W2k.data_ptr(),
+                                      S2.data_ptr(), Y.data_ptr(), M, N, K, int(group), _stream(stream))
+    _check("swiglu_fused_w4_kmajor", rc)
     return Y
 
 

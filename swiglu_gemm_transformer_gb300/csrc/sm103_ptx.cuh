@@ -163,6 +163,69 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// D(tmem) (+)= A(tmem) x B(smem desc), kind::f16, M = 128: row i of A in TMEM
+// lane i, column c holding the BF16 pair (k = 2c, 2c + 1) in its low and high
+// halves (K = 16 per instruction: 8 columns).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One K step of 64 with A from TMEM (kind::f16, M = 128): D (+)= A x B over
+// four K slices of 16, A 8 TMEM columns per slice, B's descriptor 32 bytes (2
+// in the descriptor's address field) further per slice.  `first` = 1 starts
+// the accumulator from zero.  One asm block keeps the issuing thread's
+// instruction count low.
+__device__ __forceinline__ void mma_f16_tmem_a_k64(uint32_t d, uint32_t a, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t first) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.eq.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 b1, %2, 2;\n\t"
+      "add.s64 b2, %2, 4;\n\t"
+      "add.s64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], b1, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], b2, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], b3, %3, t;\n\t}"
+      ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(first)
+      : "memory");
+}
+
+// Warp: store 32 consecutive 32-bit columns into this warp's 32 TMEM lanes
+// (thread i writes lane base+i).  Complete after tmem_wait_st().
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+      "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+      "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Warp: load 32 consecutive 32-bit columns of this warp's 32 TMEM lanes
 // (thread i gets lane base+i).  Values are valid after tmem_wait_ld().
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {

@@ -418,6 +418,68 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
+// INT4 weights in the K-major layout of swiglu_pack_w4_kmajor ([N, K/2]
+// bytes), decoded into tensor memory: one CTA per 128 weight columns, tokens
+// in passes of 64 or 128.
+int run_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2k,
+                  const void *S2, void *Y, int64_t M, int64_t N, int64_t K, int64_t G,
+                  void *stream) {
+  if (M < 0 || N < 0 || K < 0 || G <= 0) return SWIGLU_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SWIGLU_OK;
+  if (!Y) return SWIGLU_ERR_INVALID_ARG;
+  if (G % 64 != 0 || K % G != 0) return SWIGLU_ERR_UNSUPPORTED;
+  if (N % 32 != 0 || K % 8 != 0) return SWIGLU_ERR_MISALIGNED;
+  if (K > 0 && (!A || !W1k || !W2k || !S1 || !S2)) return SWIGLU_ERR_INVALID_ARG;
+  if (!aligned16(Y) || (K > 0 && (!aligned16(A) || !aligned16(W1k) || !aligned16(W2k) ||
+                                  !aligned16(S1) || !aligned16(S2))))
+    return SWIGLU_ERR_MISALIGNED;
+  const uint64_t y_bytes = uint64_t(M) * N * 2, a_bytes = uint64_t(M) * K * 2;
+  const uint64_t q_bytes = uint64_t(K) * N / 2, s_bytes = uint64_t(K / G) * N * 2;
+  if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, W1k, q_bytes) ||
+      overlaps(Y, y_bytes, W2k, q_bytes) || overlaps(Y, y_bytes, S1, s_bytes) ||
+      overlaps(Y, y_bytes, S2, s_bytes))
+    return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cudaMemsetAsync(Y, 0, y_bytes, s) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+
+  const int tok = M <= 64 ? 64 : 128;
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof la);
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
+  rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, uint32_t(tok), CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1k, K / 2, N, K / 2, 32, 128, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2k, K / 2, N, K / 2, 32, 128, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, BF16, S1, N, K / G, N * 2, 128, 1, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, BF16, S2, N, K / G, N * 2, 128, 1, NOSW);
+  if (rc == SWIGLU_OK) rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, uint32_t(tok / 4), NOSW);
+  if (rc != SWIGLU_OK) return rc;
+  KParams &p = la.p;
+  p.M = int32_t(M);
+  p.N = int32_t(N);
+  p.K = int32_t(K);
+  p.num_m_blk = int32_t(cdiv(M, tok));
+  p.num_n_blk = int32_t(cdiv(N, 128));
+  p.num_k_blk = int32_t(cdiv(K, 64));
+  p.group_m = 1;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.err = st->err;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blk;
+  p.Y = Y;
+  p.w4_group = int32_t(G);
+  la.device = dev;
+  la.ctx_gen = st->gen;
+  la.stream = s;
+  return launch_dqt(tok, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
 // MXFP8 (nvfp4 = false) or NVFP4 (true) weights: the split-K cluster kernel
 // with the matching decode stage.  g1, g2: NVFP4 per-tensor scales.
 int run_mx(bool nvfp4, const void *A, const void *C1, const void *S1, const float *g1,
@@ -837,6 +899,29 @@ int swiglu_fused_w4(const void *A, const void *W1q, const void *S1, const void *
                     const void *S2, void *Y, int64_t M, int64_t N, int64_t K, int64_t group,
                     void *stream) {
   return run_w4(A, W1q, S1, W2q, S2, Y, M, N, K, group, stream);
+}
+
+int swiglu_pack_w4_kmajor(const void *Wq, void *Wk, int64_t K, int64_t N, void *stream) {
+  if (K < 0 || N < 0) return SWIGLU_ERR_INVALID_ARG;
+  if (K > kMaxDim || N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
+  if (K == 0 || N == 0) return SWIGLU_OK;
+  if (!Wq || !Wk) return SWIGLU_ERR_INVALID_ARG;
+  if (N % 2 != 0 || K % 8 != 0) return SWIGLU_ERR_MISALIGNED;
+  if (!aligned16(Wq) || !aligned16(Wk)) return SWIGLU_ERR_MISALIGNED;
+  if (overlaps(Wk, uint64_t(K) * N / 2, Wq, uint64_t(K) * N / 2)) return SWIGLU_ERR_INVALID_ARG;
+  DeviceState *st = nullptr;
+  int dev = -1;
+  int rc = device_state(&st, &dev);
+  if (rc != SWIGLU_OK) return rc;
+  const cudaError_t e =
+      launch_pack_w4_kmajor(Wq, Wk, K, N, st->sm_count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+}
+
+int swiglu_fused_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2k,
+                           const void *S2, void *Y, int64_t M, int64_t N, int64_t K,
+                           int64_t group, void *stream) {
+  return run_w4_kmajor(A, W1k, S1, W2k, S2, Y, M, N, K, group, stream);
 }
 
 int swiglu_fused_mxfp8(const void *A, const void *C1, const void *S1, const void *C2,

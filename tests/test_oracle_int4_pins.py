@@ -112,3 +112,56 @@ def test_int4_recipe_round_trips():
     W = oracle.dequant_int4(si.bits_u8(Wq) if Wq.dtype != torch.uint8 else Wq.numpy(), si.bits_u16(S), 128)
     step = np.repeat(S.float().numpy(), 128, axis=0)
     assert np.all(np.abs(W - W1.double().numpy()) <= 0.5 * step + 2.0 ** -8 * np.abs(W) + 1e-30)
+
+
+# ---- the K-major arrangement of the codes (swiglu_pack_w4_kmajor's layout) -------------------
+
+def _kmajor(lib, Wq):
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    K, half = Wq.shape
+    Wk = np.zeros((2 * half, K // 2), dtype=np.uint8)
+    assert lib.oracle_pack_w4_kmajor(_ptr(Wq), K, 2 * half, _ptr(Wk)) == 0
+    return Wk
+
+
+def kmajor_pin_failures(lib):
+    """The K-major packer against what pins it:
+
+    * hand-worked (K = 8, N = 2): column 0 holds codes 1..8 down K, column 1
+      codes 15..8; word 0 of a column is nibbles (k0 k2 k4 k6 k1 k3 k5 k7) from
+      the low end, so column 0's bytes are 0x31 0x75 0x42 0x86 and column 1's
+      0xDF 0x9B 0xCE 0x8A (worked by hand from the layout's statement);
+    * read back the way the kernel reads it: (word >> 4i) & 0x000F000F is the
+      pair (8j + 2i, 8j + 2i + 1) in its low and high 16 bits, for every
+      column, word and i (random codes, an odd number of column pairs);
+    * every code appears exactly once (the multiset of nibbles is unchanged).
+    """
+    bad = []
+    c0 = np.arange(1, 9, dtype=np.uint8)
+    c1 = (15 - np.arange(8)).astype(np.uint8)
+    want = np.array([[0x31, 0x75, 0x42, 0x86], [0xDF, 0x9B, 0xCE, 0x8A]], dtype=np.uint8)
+    if not np.array_equal(_kmajor(lib, (c0 | (c1 << 4)).reshape(8, 1)), want):
+        bad.append("hand-worked K-major case")
+    rng = np.random.default_rng(11)
+    K, N = 64, 10
+    Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+    code = np.stack([Wq & 0xF, Wq >> 4], axis=2).reshape(K, N)  # code[k, n]
+    words = _kmajor(lib, Wq).view("<u4")  # [N, K/8]
+    ok = True
+    for n in range(N):
+        for j in range(K // 8):
+            for i in range(4):
+                pair = (int(words[n, j]) >> (4 * i)) & 0x000F000F
+                ok &= bool(pair & 0xF == code[8 * j + 2 * i, n])
+                ok &= bool(pair >> 16 == code[8 * j + 2 * i + 1, n])
+    if not ok:
+        bad.append("pairs (k, k + 1) in K order")
+    Wq = rng.integers(0, 256, size=(24, 7), dtype=np.uint8)
+    nib = lambda a: np.sort(np.concatenate([(a & 0xF).ravel(), (a >> 4).ravel()]))
+    if not np.array_equal(nib(Wq), nib(_kmajor(lib, Wq))):
+        bad.append("not a permutation of the codes")
+    return bad
+
+
+def test_kmajor_pack_pins():
+    assert kmajor_pin_failures(oracle._load()) == []

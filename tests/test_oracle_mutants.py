@@ -277,6 +277,29 @@ def test_planted_int4_mistake_is_caught(tmp_path, name):
     assert failures, f"pins did not catch mutant {name}"
 
 
+# Planted mistakes in the K-major INT4 arrangement, caught by its pins.
+KMAJOR_MUTANTS = {
+    "kmajor_natural_nibble_order": ("int64_t nib = (r % 2 == 0) ? r / 2 : 4 + r / 2;", "int64_t nib = r;"),
+    "kmajor_column_nibble_swapped": ("(Wq[k * (N / 2) + n / 2] >> (4 * (n % 2))) & 0xF",
+                                     "(Wq[k * (N / 2) + n / 2] >> (4 * (1 - n % 2))) & 0xF"),
+    "kmajor_halves_swapped": ("Wk[at] |= (uint8_t)(code << (4 * (nib % 2)));",
+                              "Wk[at] |= (uint8_t)(code << (4 * (1 - nib % 2)));"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(KMAJOR_MUTANTS))
+def test_planted_kmajor_mistake_is_caught(tmp_path, name):
+    from test_oracle_int4_pins import kmajor_pin_failures
+    src = open(SRC).read()
+    old, new = KMAJOR_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique in the oracle source"
+    lib = _build(tmp_path, name, src.replace(old, new, 1))
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.oracle_pack_w4_kmajor.argtypes = [p, i64, i64, p]
+    lib.oracle_pack_w4_kmajor.restype = ctypes.c_int
+    assert kmajor_pin_failures(lib), f"pins did not catch mutant {name}"
+
+
 # Planted mistakes in the MXFP8 / NVFP4 weight paths, caught by the MX pins.
 MX_MUTANTS = {
     "e8m0_bias": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),

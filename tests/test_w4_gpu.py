@@ -85,3 +85,55 @@ def test_w4_argument_errors(sg):
     assert lib.swiglu_fused_w4(*p, 4, 64, 0, 128, None) == sg.OK
     torch.cuda.synchronize()
     assert torch.all(Y == 0)
+
+
+# ---- K-major codes decoded into tensor memory (swiglu_fused_w4_kmajor) -----------------------
+
+def _run_kmajor(sg, M, N, K, G, seed, rows=None):
+    A, (W1q, S1), (W2q, S2) = si.make_w4(M, N, K, seed, G)
+    W1k = sg.swiglu_pack_w4_kmajor(W1q.to(DEV))
+    W2k = sg.swiglu_pack_w4_kmajor(W2q.to(DEV))
+    Y = sg.swiglu_fused_w4_kmajor(A.to(DEV), W1k, S1.to(DEV), W2k, S2.to(DEV), group=G)
+    rc, detail = sg.swiglu_device_status()
+    assert rc == sg.OK, (sg.status_string(rc), detail)
+    # the packer against the oracle's arrangement, byte for byte
+    assert np.array_equal(W1k.cpu().numpy(), oracle.pack_w4_kmajor(W1q.numpy()))
+    ref = oracle.swiglu_w4(si.bits_u16(A), W1q.numpy(), si.bits_u16(S1), W2q.numpy(),
+                           si.bits_u16(S2), G, rows=rows)
+    got = Y.double().cpu().numpy()
+    if rows is not None:
+        got = got[rows]
+    oracle.assert_parity(got, ref, f"w4 k-major {M}x{N}x{K} G={G}")
+
+
+@pytest.mark.parametrize("shape", [(1, 128, 64, 64), (17, 256, 192, 64), (64, 4864, 896, 128),
+                                   (65, 4896, 896, 128), (128, 1152, 448, 64),
+                                   # several 128-token passes, the last one ragged
+                                   (300, 640, 256, 128), (129, 256, 128, 128),
+                                   # ragged last column block (9760 = 76 x 128 + 32), one group
+                                   (100, 9760, 256, 256)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_w4_kmajor_shapes(sg, shape):
+    M, N, K, G = shape
+    _run_kmajor(sg, M, N, K, G, seed=3 * M + N + K)
+
+
+@pytest.mark.parametrize("M", [64, 128])
+def test_w4_kmajor_7b_shape_sampled(sg, M):
+    N, K = 18944, 3584
+    _run_kmajor(sg, M, N, K, 128, seed=4, rows=si.sample_rows(M, 64, 24, seed=4))
+
+
+def test_w4_kmajor_argument_errors(sg):
+    lib = sg.lib()
+    A = torch.zeros(4, 128, dtype=torch.bfloat16, device=DEV)
+    Wk = torch.zeros(64, 64, dtype=torch.uint8, device=DEV)
+    S = torch.zeros(1, 64, dtype=torch.bfloat16, device=DEV)
+    Y = torch.empty(4, 64, dtype=torch.bfloat16, device=DEV)
+    p = [t.data_ptr() for t in (A, Wk, S, Wk, S, Y)]
+    assert lib.swiglu_fused_w4_kmajor(*p, 4, 64, 128, 100, None) == sg.ERR_UNSUPPORTED
+    assert lib.swiglu_fused_w4_kmajor(*p, 4, 48, 128, 128, None) == sg.ERR_MISALIGNED
+    assert lib.swiglu_fused_w4_kmajor(p[0], p[1], p[2], p[3], p[4], p[0], 4, 64, 128, 128, None) == sg.ERR_INVALID_ARG
+    assert lib.swiglu_fused_w4_kmajor(*p, 0, 64, 128, 128, None) == sg.OK
+    assert lib.swiglu_pack_w4_kmajor(p[1], p[1], 128, 64, None) == sg.ERR_INVALID_ARG  # overlap
+    assert lib.swiglu_pack_w4_kmajor(p[1], Y.data_ptr(), 12, 64, None) == sg.ERR_MISALIGNED
