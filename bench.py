@@ -1154,6 +1154,71 @@ def run_sweep(args):
             "seconds": round(time.time() - t0, 1), "entries": entries}
 
 
+def run_small_m_floor(args):
+    """The floor under the 0.5B small-M calls: time, on this GPU and in the same
+    way as the per-call durations (back-to-back launches in a CUDA graph over
+    rotating input copies larger than L2), a read-only reduction over the
+    same weight bytes (one kernel reading W1 and W2 once), cuBLAS on the same
+    bytes (one GEMM A x [W1 W2], no activation), and the fused call."""
+    import torch
+    import swiglu_gemm_transformer_gb300 as sg
+    import swiglu_inputs as si
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sg.lib()
+    stream = torch.cuda.Stream(device=dev)
+    K, N, _, seed = WORKLOADS["qwen2.5-0.5b"]
+    peaks, src = load_peaks()
+    rows = []
+    for M in (64, 128):
+        A, W1, W2 = si.make_bf16(M, N, K, seed)
+        wbytes = 2 * K * N * 2
+        ncopy = max(2, min(32, math.ceil(2.5 * L2_BYTES / wbytes)))
+        sets = []
+        for _ in range(ncopy):
+            Wc = torch.cat([W1, W2], dim=1).to(dev)            # [K, 2N]: the same bytes
+            sets.append((A.to(dev), Wc, Wc[:, :N].contiguous(), Wc[:, N:].contiguous(),
+                         torch.empty(M, N, dtype=torch.bfloat16, device=dev)))
+
+        def timed(make):
+            fns = [make(*c) for c in sets]
+            reps = max(1, math.ceil(args.call_launches / ncopy))
+
+            def body():
+                for _ in range(reps):
+                    for f in fns:
+                        f()
+            with torch.cuda.stream(stream):
+                for f in fns:
+                    f()
+                g = capture(body, stream)
+                g.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+            e1.synchronize()
+            return 1e3 * e0.elapsed_time(e1) / (reps * ncopy)
+        read_us = timed(lambda a, wc, w1, w2, y: (lambda: torch.sum(wc, dtype=torch.float32)))
+        gemm_us = timed(lambda a, wc, w1, w2, y: (lambda: torch.matmul(a, wc)))
+        fused_us = timed(lambda a, wc, w1, w2, y: (lambda: sg.swiglu_fused(a, w1, w2, y)))
+        rc, detail = sg.swiglu_device_status(stream)
+        if rc != sg.OK:
+            raise RuntimeError(f"device status: {sg.status_string(rc)} ({detail})")
+        abytes = 2 * M * K + wbytes + 2 * M * N
+        rows.append({"M": M, "N": N, "K": K, "weight_bytes": wbytes, "algorithmic_bytes": abytes,
+                     "read_reduction_us": round(read_us, 3), "cublas_gemm_us": round(gemm_us, 3),
+                     "fused_us": round(fused_us, 3),
+                     "fused_frac_of_hbm": round(abytes / (fused_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                     "read_reduction_frac_of_hbm": round(wbytes / (read_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                     "variant": sg.variant_name(sg.lib().swiglu_select_variant(M, N, K, 0))})
+        log(f"small-M floor M={M}: {rows[-1]}")
+    props = torch.cuda.get_device_properties(dev)
+    return {"what": "floor under the 0.5B small-M calls (K=896, N=4864)", "gpu": props.name,
+            "hbm_gbs_peak": peaks["hbm_gbs"], "peak_source": src, "torch": torch.__version__,
+            "rows": rows}
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -1184,6 +1249,9 @@ def main():
                     help="write a traffic record from an ncu CSV (no GPU work)")
     ap.add_argument("--only", default="",
                     help="restrict the step to calls FORM:M[,FORM:M...] (profiling a single kernel)")
+    ap.add_argument("--small-m-floor", action="store_true",
+                    help="time the floor under the 0.5B small-M calls (read-only reduction and "
+                         "cuBLAS on the same weight bytes, and the fused call) and print it")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -1191,6 +1259,10 @@ def main():
 
     if args.record_traffic:
         print(json.dumps(record_traffic(*args.record_traffic)))
+        return
+
+    if args.small_m_floor:
+        print(json.dumps(run_small_m_floor(args)), flush=True)
         return
 
     if args.sweep:
