@@ -132,6 +132,9 @@ __device__ __forceinline__ static uint32_t pack_bf16x2(float lo, float hi) {
 //   it        : running staging-buffer counter of this warp.
 //   release   : cluster address of the barrier to arrive on once the warp has
 //               read the whole accumulator (frees the TMEM buffer for the MMA).
+//               The arrive is relaxed: the loads are complete (tcgen05.wait::ld)
+//               before it issues, so no release ordering is needed, and a
+//               cluster-scope release costs microseconds.
 //   gs, us    : scales applied to the gate and up accumulators (SCALED only).
 //   PAIRED    : separate form only; within every 8 accumulator columns the
 //               output columns lie in the order 0 4 1 5 2 6 3 7 (the order
@@ -148,7 +151,7 @@ __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, in
   if (c_begin >= c_end) {  // nothing to read in this tile: release at once
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_cluster(release);
+    if (lane == 0) ptx::mbar_arrive_cluster_relaxed(release);
     return;
   }
 #pragma unroll 1
@@ -178,7 +181,7 @@ __device__ __forceinline__ static void epilogue_tile(uint32_t tacc, int row0, in
     if (c == c_end - 1) {
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(release);
+      if (lane == 0) ptx::mbar_arrive_cluster_relaxed(release);
     }
     uint32_t packed[16];
     if (INTERLEAVED) {
@@ -237,7 +240,7 @@ __device__ __forceinline__ static void epilogue_tile_linear(uint32_t tacc, int r
   if (c_begin >= c_end) {
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_cluster(release);
+    if (lane == 0) ptx::mbar_arrive_cluster_relaxed(release);
     return;
   }
   const int row = row0 + lane;
@@ -261,7 +264,7 @@ __device__ __forceinline__ static void epilogue_tile_linear(uint32_t tacc, int r
     if (c == c_end - 1) {
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(release);
+      if (lane == 0) ptx::mbar_arrive_cluster_relaxed(release);
     }
     if (p.k_splits > 1) {
       if (row < p.M) {
