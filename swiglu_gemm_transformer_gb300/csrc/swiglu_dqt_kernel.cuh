@@ -30,7 +30,7 @@
 //     (1 + e^-g), and stores Y^T's [32 columns x TOK/4 tokens] block as Y's
 //     [TOK/4 rows x 32 columns] block with one TMA store.
 // More tokens than TOK: the CTA walks token blocks, decoding the codes again
-// for each (the decode is shorter than the MMAs of a step).
+// for each (later passes read them from L2).
 // Every wait is bounded as in the other kernels.
 #pragma once
 
@@ -79,6 +79,7 @@ struct DqtCfg {
   static_assert(C_BYTES % 128 == 0 && STG_BYTES % 128 == 0, "128-byte aligned copies");
   static_assert(A_STAGES == NBUF, "one barrier pair per tokens stage and decoded buffer");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(2 * SMEM_BYTES > 233472, "one CTA per SM (it holds all 512 TMEM columns)");
 };
 
 // Half a step: 32 K values of one column from 16 bytes of codes, 16 pairs.
