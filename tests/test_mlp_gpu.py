@@ -91,6 +91,27 @@ def test_linear_split_matches_unsplit(sg):
     oracle.assert_parity(Z1.float().cpu().numpy(), Z2.double().cpu().numpy(), "split vs unsplit")
 
 
+def test_linear_schedules_agree(sg):
+    """The pair kernel's linear mode on more tiles than pairs fit (8 x 14 tiles
+    of 256 x 256 here): the dynamic (cluster launch control) and static tile
+    schedules give the same Z bit for bit, and both match the oracle."""
+    M, N, K = 2048, 3584, 1024
+    X, W, _ = si.make_bf16(M, N, K, seed=21)
+    R = _residual(M, N, 22)
+    out = {}
+    try:
+        for dyn in (1, 0):
+            sg.swiglu_set_pair_schedule(dyn)
+            out[dyn] = sg.swiglu_linear(X.to(DEV), W.to(DEV), R.to(DEV))
+            _status(sg)
+    finally:
+        sg.swiglu_set_pair_schedule(1)
+    assert torch.equal(out[0].view(torch.int16), out[1].view(torch.int16))
+    rows = si.sample_rows(M, 256, 32, seed=21)
+    ref = oracle.linear_bf16(si.bits_u16(X), si.bits_u16(W), si.bits_u16(R), rows=rows)
+    oracle.assert_parity(out[1].float().cpu().numpy()[rows], ref, "linear, dynamic schedule")
+
+
 MLP_CASES = [
     # (name, M, H, F, seed, residual)
     ("tiny", 7, 64, 136, 5, True),
