@@ -93,3 +93,23 @@ def test_fp8_scales_are_applied(sg):
     Y2 = _run(sg, "separate", q, s2)
     oracle.assert_parity(Y2.float().cpu().numpy(), _ref(q, s2), "fp8 scaled")
     assert torch.equal(Y2.float(), 2.0 * Y1.float())
+
+
+@pytest.mark.parametrize("form", ["separate", "interleaved"])
+def test_fp8_schedules_agree(sg, form):
+    """The FP8 pair kernel on more tiles than pairs fit (3 x 31 tiles of 256 x
+    128, ragged in M, N and K): the dynamic and static tile schedules give the
+    same Y bit for bit, and both match the oracle."""
+    M, N, K = 600, 3904, 208
+    q, s = si.make_e4m3(M, N, K, seed=31)
+    out = {}
+    try:
+        for dyn in (1, 0):
+            sg.swiglu_set_pair_schedule(dyn)
+            out[dyn] = _run(sg, form, q, s)
+    finally:
+        sg.swiglu_set_pair_schedule(1)
+    assert torch.equal(out[0].view(torch.int16), out[1].view(torch.int16))
+    rows = si.sample_rows(M, 128, 32, seed=31)
+    oracle.assert_parity(out[1].float().cpu().numpy()[rows], _ref(q, s, rows=rows),
+                         f"fp8 {form}, dynamic schedule")
