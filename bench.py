@@ -1155,7 +1155,7 @@ def run_sweep(args):
 
 
 def run_small_m_floor(args):
-    """The floor under the 0.5B small-M calls: time, on this GPU and in the same
+    """The floor under the 0.5B small- and mid-M calls: time, on this GPU and in the same
     way as the per-call durations (back-to-back launches in a CUDA graph over
     rotating input copies larger than L2), a read-only reduction over the
     same weight bytes (one kernel reading W1 and W2 once), cuBLAS on the same
@@ -1170,7 +1170,7 @@ def run_small_m_floor(args):
     K, N, _, seed = WORKLOADS["qwen2.5-0.5b"]
     peaks, src = load_peaks()
     rows = []
-    for M in (64, 128):
+    for M in (64, 128, 512):
         A, W1, W2 = si.make_bf16(M, N, K, seed)
         wbytes = 2 * K * N * 2
         ncopy = max(2, min(32, math.ceil(2.5 * L2_BYTES / wbytes)))
@@ -1206,7 +1206,10 @@ def run_small_m_floor(args):
         if rc != sg.OK:
             raise RuntimeError(f"device status: {sg.status_string(rc)} ({detail})")
         abytes = 2 * M * K + wbytes + 2 * M * N
+        tflop = 4 * M * N * K / 1e12
         rows.append({"M": M, "N": N, "K": K, "weight_bytes": wbytes, "algorithmic_bytes": abytes,
+                     "fused_frac_of_tensor": round(tflop / (fused_us * 1e-6) / peaks["bf16_tflops"], 4),
+                     "cublas_frac_of_tensor": round(tflop / (gemm_us * 1e-6) / peaks["bf16_tflops"], 4),
                      "read_reduction_us": round(read_us, 3), "cublas_gemm_us": round(gemm_us, 3),
                      "fused_us": round(fused_us, 3),
                      "fused_frac_of_hbm": round(abytes / (fused_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
@@ -1214,7 +1217,7 @@ def run_small_m_floor(args):
                      "variant": sg.variant_name(sg.lib().swiglu_select_variant(M, N, K, 0))})
         log(f"small-M floor M={M}: {rows[-1]}")
     props = torch.cuda.get_device_properties(dev)
-    return {"what": "floor under the 0.5B small-M calls (K=896, N=4864)", "gpu": props.name,
+    return {"what": "floor under the 0.5B small- and mid-M calls (K=896, N=4864)", "gpu": props.name,
             "hbm_gbs_peak": peaks["hbm_gbs"], "peak_source": src, "torch": torch.__version__,
             "rows": rows}
 
