@@ -19,10 +19,12 @@
 //     column's BF16 pair (k, k + 1) -- exactly one 32-bit TMEM column of the A
 //     operand (row = TMEM lane, two K values per column);
 //   * sixteen decoding warps: warp w owns TMEM lanes [32 (w % 4), +32) (thread
-//     = weight column), decodes W1 (bit 2 of w clear) or W2, and the first or
-//     second 32 K values of each step (bit 3), stored with one tcgen05.st of
-//     16 columns into one of NBUF decoded buffers; four warps per SM
-//     sub-partition hide each other's latency; warp 16 streams the tokens and
+//     = weight column), decodes W1 (bit 2 of w clear) or W2, and every other
+//     K step (bit 3: the step's parity), all 64 K values of it, stored with
+//     one tcgen05.st of 32 columns into one of NBUF decoded buffers -- eight
+//     warps per step, so each warp's waits, fences and arrives serve twice
+//     the decode work of a half step; four warps per SM sub-partition hide
+//     each other's latency; warp 16 streams the tokens and
 //     warp 18 the codes and scales (TMA, two rings); per K step warp 17 issues
 //     four MMAs into the gate accumulator and warp 19 four into the up one;
 //   * the epilogue (the sixteen warps again) reads gate and up for its lanes
@@ -72,19 +74,22 @@ struct DqtCfg {
   // issuing it costs about as much as executing it
   static constexpr int DEC_WARPS = 16, PRODUCER_WARP = 16, MMA_WARP = 17, CODES_WARP = 18,
                        MMA2_WARP = 19;
+  static constexpr int DEC_PER_STEP = 8;  // warps decoding one step (the other eight take the next)
   static constexpr int THREADS = 32 * 20;
   static constexpr uint32_t IDESC = ptx::idesc_bf16(128, TOK, false, false);
   static_assert(TOK == 64 || TOK == 128, "tokens per pass");
   static_assert(2 * TOK <= BUF_COL0 && BUF_COL0 + NBUF * 64 <= TMEM_COLS, "TMEM map");
   static_assert(C_BYTES % 128 == 0 && STG_BYTES % 128 == 0, "128-byte aligned copies");
   static_assert(A_STAGES == NBUF, "one barrier pair per tokens stage and decoded buffer");
+  static_assert(C_STAGES % 2 == 0 && NBUF % 2 == 0, "a stage and a buffer serve steps of one parity");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(2 * SMEM_BYTES > 233472, "one CTA per SM (it holds all 512 TMEM columns)");
 };
 
-// Half a step: 32 K values of one column from 16 bytes of codes, 16 pairs.
+// Half a step: 32 K values of one column from 16 bytes of codes, 16 pairs
+// into r[0..15].
 __device__ __forceinline__ static void decode_kmajor_int4_half(const uint4 &w, uint32_t s_bits,
-                                                               uint32_t (&r)[16]) {
+                                                               uint32_t *r) {
   const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
   const uint32_t sp = s_bits | (s_bits << 16);
   const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&sp);
@@ -117,8 +122,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const uint32_t bars = base + C::BAR_OFF;
   // stage s: the tokens tile and decoded buffer s; full when the tokens have
-  // landed and all sixteen decoding warps have stored, empty once both MMA
-  // issuers' commits arrive
+  // landed and the step's eight decoding warps have stored, empty once both
+  // MMA issuers' commits arrive
   auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
   auto empty_bar = [&](uint32_t s) { return bars + 8u * (C::A_STAGES + s); };
   auto cfull_bar = [&](uint32_t s) { return bars + 8u * (2 * C::A_STAGES + s); };
@@ -142,12 +147,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::A_STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), 1 + C::DEC_WARPS);  // the tokens' expect_tx and the decoders
+      ptx::mbar_init(full_bar(s), 1 + C::DEC_PER_STEP);  // the tokens' expect_tx and the decoders
       ptx::mbar_init(empty_bar(s), 2);                // both MMA issuers' commits
     }
     for (int s = 0; s < C::C_STAGES; ++s) {
       ptx::mbar_init(cfull_bar(s), 1);
-      ptx::mbar_init(cempty_bar(s), C::DEC_WARPS);  // every decoding warp
+      ptx::mbar_init(cempty_bar(s), C::DEC_PER_STEP);  // the step's decoding warps
     }
     ptx::mbar_init(accf_bar, 2);
     ptx::mbar_init(acce_bar, C::DEC_WARPS);
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ------------------------------------------------------------ decode, then epilogue (warps 0-15)
     const int q = warp & 3;          // TMEM lanes [32q, 32q + 32): weight columns n0 + 32q + lane
     const int mtx = (warp >> 2) & 1; // decode: 0 = W1 (gate), 1 = W2 (up)
-    const int kh = warp >> 3;        // decode: K values [32 kh, 32 kh + 32) of a step
+    const int par = warp >> 3;       // decode: the steps g with g % 2 == par
     const int tq = warp >> 2;        // epilogue: tokens [tq TOK/4, (tq + 1) TOK/4)
     const int c = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
@@ -269,6 +274,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int tb = 0; tb < nt && ok; ++tb) {
       for (int i = 0; i < nk; ++i) {
         const int g = tb * nk + i;
+        if ((g & 1) != par) continue;
         const uint32_t s = static_cast<uint32_t>(g % C::C_STAGES);
         const uint32_t b = static_cast<uint32_t>(g % C::NBUF);  // = the tokens stage
         ok = wait_bar(cfull_bar(s), static_cast<uint32_t>(g / C::C_STAGES) & 1u, p.timeout_ns,
@@ -276,11 +282,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint8_t *st = smem + C::C_OFF + s * C::C_BYTES;
-        const uint4 w = *reinterpret_cast<const uint4 *>(st + mtx * C::CODE_BYTES + c * 32 + kh * 16);
+        const uint4 *cw = reinterpret_cast<const uint4 *>(st + mtx * C::CODE_BYTES + c * 32);
+        const uint4 w0 = cw[0], w1 = cw[1];
         const uint32_t sbits =
             *reinterpret_cast<const uint16_t *>(st + 2 * C::CODE_BYTES + mtx * C::SCALE_BYTES + c * 2);
-        uint32_t r[16];
-        decode_kmajor_int4_half(w, sbits, r);
+        uint32_t r[32];
+        decode_kmajor_int4_half(w0, sbits, r);
+        decode_kmajor_int4_half(w1, sbits, r + 16);
         // The codes were consumed by the decode above: release the stage.
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(cempty_bar(s));
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        ptx::tmem_st16(tmem_base + lane_off + C::BUF_COL0 + 64u * b + 32u * mtx + 16u * kh, r);
+        ptx::tmem_st32(tmem_base + lane_off + C::BUF_COL0 + 64u * b + 32u * mtx, r);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
