@@ -87,6 +87,34 @@ struct SwabCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+// One K step of 64 on the pair: four MMAs of K = 16 from stage descriptors
+// stepped by immediates (slice j: adesc + j * A_STEP, bdesc + j * B_STEP, in
+// 16-byte units); `first` = 1 starts the accumulator.  These MMAs are short
+// (64 weight rows per CTA x the rows of A x 16), so the issuing thread's own
+// work per MMA matters: two descriptors and a predicate built per MMA would
+// take about as long as the MMA itself.
+template <int A_STEP, int B_STEP>
+__device__ __forceinline__ static void swab_mma_k64(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                                    uint32_t idesc, uint32_t first) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.eq.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %1, %5;\n\t"
+      "add.s64 a2, %1, %6;\n\t"
+      "add.s64 a3, %1, %7;\n\t"
+      "add.s64 b1, %2, %8;\n\t"
+      "add.s64 b2, %2, %9;\n\t"
+      "add.s64 b3, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(first), "n"(A_STEP), "n"(2 * A_STEP),
+      "n"(3 * A_STEP), "n"(B_STEP), "n"(2 * B_STEP), "n"(3 * B_STEP)
+      : "memory");
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     swiglu_swab_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -182,24 +210,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      // Stage 0's descriptors; stage s adds s * STAGE_BYTES (16-byte units).
+      // Weights (MMA A, M side): MN-major, boxes W_LBO apart, 8-row K groups
+      // W_SBO apart, one MMA's 16 K rows = W_KSTEP bytes; rows of A (MMA B,
+      // N side): K-major, 128-byte swizzle, 32 bytes of K per MMA.
+      const uint64_t adesc0 = ptx::smem_desc(base, C::W_LBO, C::W_SBO, C::W_SWIZZLE);
+      const uint64_t bdesc0 = ptx::smem_desc(base + C::W_BYTES, 16, 1024, ptx::SW_128B);
+      static_assert(C::BK == 64, "four MMAs of K = 16 per stage");
       for (int kb = 0; kb < nk; ++kb) {
         if (!wait_bar(full_bar(stage), phase, p.timeout_ns, abort_flag, p.err, WAIT_MMA_FULL)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t sw = base + stage * C::STAGE_BYTES;
-        const uint32_t sa = sw + C::W_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk) {
-          // weights (MMA A, M side): MN-major, boxes W_LBO apart, 8-row K
-          // groups W_SBO apart, one MMA's 16 K rows = W_KSTEP bytes;
-          // rows of A (MMA B, N side): K-major, 128-byte swizzle, 32 bytes of K.
-          const uint64_t adesc =
-              ptx::smem_desc(sw + kk * C::W_KSTEP, C::W_LBO, C::W_SBO, C::W_SWIZZLE);
-          const uint64_t bdesc = ptx::smem_desc(sa + kk * 32, 16, 1024, ptx::SW_128B);
-          ptx::mma_f16_pair(tmem_base, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
-        }
+        const uint64_t off = (stage * C::STAGE_BYTES) >> 4;
+        swab_mma_k64<C::W_KSTEP / 16, 32 / 16>(tmem_base, adesc0 + off, bdesc0 + off, C::IDESC,
+                                               kb == 0 ? 1u : 0u);
         ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
         if (++stage == C::STAGES) {
           stage = 0;
@@ -269,10 +295,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           ystg[row * C::COLS + col] = __float2bfloat16_rn(y);
         }
       } else {
+        // the partner's values first, into registers: the output stores below
+        // go to the same shared array, so loads interleaved with them would
+        // wait for each store in turn
+        float o[H2];
+#pragma unroll
+        for (int t = 0; t < H2; ++t) o[t] = from_partner[lane * C::XCH_STRIDE + t];
 #pragma unroll
         for (int t = 0; t < H2; ++t) {
-          const float o = from_partner[lane * C::XCH_STRIDE + t];
-          const float y = gate ? silu_mul(v[t], o) : silu_mul(o, v[H2 + t]);
+          const float y = gate ? silu_mul(v[t], o[t]) : silu_mul(o[t], v[H2 + t]);
           const int row = rbase + (gate ? t : H2 + t);
           ystg[row * C::COLS + lane] = __float2bfloat16_rn(y);
         }
@@ -292,8 +323,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   }
 
+  // Both CTAs have passed their last use of the pair's resources (the
+  // leader has drained its MMAs, each producer has seen every commit aimed at
+  // its barriers) before either frees the tensor memory and leaves.  Only the
+  // order of execution matters here, so the arrive is relaxed: a release
+  // would also wait for this CTA's output stores to reach global memory.
   ptx::tc_fence_before();
-  ptx::cluster_sync();
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+  asm volatile("barrier.cluster.wait;" ::: "memory");
   if (warp == C::MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
