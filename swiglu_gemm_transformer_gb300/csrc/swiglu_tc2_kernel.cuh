@@ -378,8 +378,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   }
 
+  // Both CTAs have passed their last use of the pair's resources (tensor
+  // memory, the barriers the other CTA signals, the schedule responses)
+  // before either frees the tensor memory and leaves.  Only the order of
+  // execution matters here, so the arrive is relaxed: a release would also
+  // wait for this CTA's output stores to reach global memory (~0.6 us).
   ptx::tc_fence_before();
-  ptx::cluster_sync();
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+  asm volatile("barrier.cluster.wait;" ::: "memory");
   if (warp == C::MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
