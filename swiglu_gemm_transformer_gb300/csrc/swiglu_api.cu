@@ -209,12 +209,10 @@ int choose_variant(int64_t M, int64_t N, int64_t K, bool /*interleaved*/, int sm
   // Two 128-row blocks of 64-column tiles in one wave (M = 256, N = 4864:
   // 8.4 us against 9.8 us for the CTA-pair tiles).
   if (M <= 256 && cdiv(M, 128) * cdiv(N, 64) <= sm_count) return SWIGLU_VARIANT_1SM_N64;
-  // Up to one wave of 128 x 128 tiles (0.5B, M = 512: 152 tiles on 152 SMs):
-  // one tile per SM over all of K, 10.6 us against 10.9 us for the CTA-pair
-  // tiles (measured variant table).
-  if (M > 128 && cdiv(M, 128) * cdiv(N, 128) <= sm_count) return SWIGLU_VARIANT_1SM_N128;
   // Larger M: one 256x128 tile per CTA pair halves the weight bytes each SM
-  // streams per K step (32 KB instead of 48 KB).
+  // streams per K step (32 KB instead of 48 KB).  This holds for a single
+  // wave too (0.5B, M = 512: 9.9 us against 10.1 us for one 128 x 128 tile
+  // per SM, measured variant table).
   if (M > 128) return SWIGLU_VARIANT_2SM_N128;
   // Small M (one 128-row block): narrow the tiles until they occupy every SM
   // (the page's Kernel-2 argument: more thread blocks for small batches); a
