@@ -220,6 +220,53 @@ def test_pair_schedules_agree_with_oracle_and_each_other(sg, form):
     assert torch.equal(out[0].view(torch.int16), out[1].view(torch.int16))
 
 
+def test_pair_kernels_back_to_back_are_bit_identical(sg):
+    """The CTA-pair kernels end with a relaxed cluster barrier: a pair's CTAs
+    only wait for each other's execution before freeing tensor memory and
+    leaving.  Launched back to back on one stream (each launch's prologue
+    overlapping the previous one's end), every result must equal the first
+    computation of the same call bit for bit, with no device-side timeout,
+    for multi-wave shapes of both forms on the dynamic and the static
+    schedule, and for the transposed-product pair kernel."""
+    cases = [("separate", SCHED_SHAPE, "2sm_n128", 21), ("interleaved", SCHED_SHAPE, "2sm_n128", 22),
+             ("separate", (2048, 4864, 896), "2sm_n128", 23),
+             ("separate", (128, 4864, 896), "2sm_swap", 24),
+             ("interleaved", (100, 1000, 264), "2sm_swap", 25)]
+    bufs = []
+    for form, (M, N, K), variant, seed in cases:
+        A, W1, W2 = si.make_bf16(M, N, K, seed=seed)
+        Ad, W1d, W2d = A.to(DEV), W1.to(DEV), W2.to(DEV)
+        Wf = sg.swiglu_pack_interleaved(W1d, W2d) if form == "interleaved" else None
+        bufs.append((form, Ad, W1d, W2d, Wf, sg.VARIANTS[variant], (A, W1, W2)))
+
+    def call(b, Y=None):
+        form, Ad, W1d, W2d, Wf, v, _ = b
+        if form == "interleaved":
+            return sg.swiglu_fused_interleaved(Ad, Wf, Y, variant=v)
+        return sg.swiglu_fused(Ad, W1d, W2d, Y, variant=v)
+
+    try:
+        for dyn in (1, 0):
+            sg.swiglu_set_pair_schedule(dyn)
+            first = [call(b) for b in bufs]
+            torch.cuda.synchronize()
+            outs = [torch.empty_like(y) for y in first]
+            for _ in range(12):
+                for b, y in zip(bufs, outs):
+                    call(b, y)
+                torch.cuda.synchronize()
+                for i, (y, y0) in enumerate(zip(outs, first)):
+                    assert torch.equal(y.view(torch.int16), y0.view(torch.int16)), \
+                        f"launch result differs: case {i}, dynamic={dyn}"
+            rc, detail = sg.swiglu_device_status()
+            assert rc == sg.OK, f"device status {sg.status_string(rc)} detail {detail}"
+    finally:
+        sg.swiglu_set_pair_schedule(1)
+    for b, y in zip(bufs, first):  # and the computation itself is right
+        A, W1, W2 = b[6]
+        _check(y, A, W1, W2, rows=si.sample_rows(A.shape[0], 128, 32, seed=5), what=f"{b[0]} {b[5]}")
+
+
 def test_dynamic_schedule_skips_while_a_timeout_is_recorded(sg):
     """While a device-side timeout is recorded, a multi-wave CTA-pair launch
     does no work (so a kernel that keeps timing out ends quickly); once the
