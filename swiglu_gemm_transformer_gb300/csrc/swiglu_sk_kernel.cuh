@@ -22,8 +22,10 @@
 //     rows.  Eight epilogue warps (four TMEM lane groups x two 16-column
 //     halves, so all four SM sub-partitions share the work) each send the
 //     peer their partial gate/up sums of 16 of the peer's columns with
-//     st.async (16 bytes per store, counted on the peer's receive mbarrier),
-//     then wait for the peer's sums of their own 16 columns, add them, apply
+//     st.async (16 bytes per store, counted on the mbarrier of the peer's
+//     warp that keeps those columns, so each warp can go on as soon as its
+//     own 4 KB are in), then wait for the peer's sums of their own 16
+//     columns, add them, apply
 //     y = g * u / (1 + e^-g) in FP32, round to BF16 and store their 32 bytes
 //     of each row directly.  With few rows this epilogue is not hidden behind
 //     MMAs, so its length is what the exchange and the activation take.
@@ -101,7 +103,8 @@ struct SkCfg {
   static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
   static constexpr int RECV_BYTES = BM * 2 * KEEP * 4;  // 32 KB
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
-  static constexpr int NUM_BARS = 3 * STAGES + 3;  // full[S], empty[S], decoded[S], acc_full, recv, drain
+  // full[S], empty[S], acc_full, drain, decoded[S], recv[EPI_WARPS] (one per receiving warp)
+  static constexpr int NUM_BARS = 3 * STAGES + 2 + 8;
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
   static constexpr int EPI_WARPS = 8;            // 4 TMEM lane groups x 2 column halves
   static constexpr int PRODUCER_WARP = 8;
@@ -179,9 +182,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (C::STAGES + s); };
   const uint32_t accf_bar = bars + 8u * (2 * C::STAGES);
-  const uint32_t recv_bar = bars + 8u * (2 * C::STAGES + 1);
-  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 2);
-  auto dec_bar = [&](int s) { return bars + 8u * (2 * C::STAGES + 3 + s); };
+  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 1);
+  auto dec_bar = [&](int s) { return bars + 8u * (2 * C::STAGES + 2 + s); };
+  // Epilogue warp w receives the peer's partial sums of its rows and columns
+  // on its own barrier, so it can finish as soon as its 4 KB are in.
+  auto recv_bar = [&](int w) { return bars + 8u * (3 * C::STAGES + 2 + w); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -198,9 +203,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // Epilogue warps on TMEM lanes (tile rows) [32q, 32q+32) are live when
   // those rows exist; the peer's live warps send what this CTA keeps.
   auto live = [&](int q) { return mb * C::BM + q * 32 < p.M; };
-  // the peer's two warps of each live lane group send 4 KB each
-  const uint32_t recv_bytes = (live(0) ? 8192u : 0u) + (live(1) ? 8192u : 0u) +
-                              (live(2) ? 8192u : 0u) + (live(3) ? 8192u : 0u);
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -208,12 +210,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ptx::mbar_init(empty_bar(s), 1);
     }
     ptx::mbar_init(accf_bar, 1);
-    ptx::mbar_init(recv_bar, 1);
+    for (int w = 0; w < C::EPI_WARPS; ++w) ptx::mbar_init(recv_bar(w), 1);
     ptx::mbar_init(drain_bar, 1);
     for (int s = 0; s < C::STAGES; ++s) ptx::mbar_init(dec_bar(s), C::EPI_WARPS);
     *abort_flag = 0;
     ptx::fence_barrier_init();
-    if (recv_bytes) ptx::mbar_arrive_expect_tx(recv_bar, recv_bytes);
+    // the peer's warp w (same rows and output half) sends warp w 4 KB when its rows exist
+    for (int w = 0; w < C::EPI_WARPS; ++w)
+      if (live(w & 3)) ptx::mbar_arrive_expect_tx(recv_bar(w), 4096u);
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB0);
     if (!C::INTERLEAVED) ptx::prefetch_tmap(&tmB1);
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         sk_load16<C>(tacc, have_acc, C::KEEP * peer + 16 * h, g, u);
         const uint32_t recv_local = base + C::RECV_OFF + static_cast<uint32_t>(row) * 16u;
         const uint32_t dst = ptx::mapa_shared(recv_local, static_cast<uint32_t>(peer));
-        const uint32_t rbar = ptx::mapa_shared(recv_bar, static_cast<uint32_t>(peer));
+        const uint32_t rbar = ptx::mapa_shared(recv_bar(warp), static_cast<uint32_t>(peer));
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // gate values 16h + 4k .. +3 -> group 4h + k; up values -> group 8 + 4h + k
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // wait for the peer's partial sums of the kept outputs
       bool got = true;
       const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait_cluster(recv_bar, 0)) {
+      while (!ptx::mbar_try_wait_cluster(recv_bar(warp), 0)) {
         if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
           got = false;
           break;
