@@ -18,10 +18,11 @@
 //     [r KEEP, (r+1) KEEP) of the tile, KEEP = BN / CS.  Eight epilogue
 //     warps (four TMEM lane groups x two BN/2-column halves) read their
 //     partial sums and send each peer its KEEP columns with st.async
-//     (16-byte stores into the peer's shared memory, counted on the peer's
-//     receive mbarrier); the warps that hold the kept columns wait for the
-//     CS - 1 partial tiles sent to this CTA, add them and R in FP32, round to
-//     BF16 and store their KEEP columns of each row.
+//     (16-byte stores into the peer's shared memory, counted on the
+//     mbarrier of the peer's finishing warp for those rows); the warps that
+//     hold the kept columns each wait for their rows of the CS - 1 partial
+//     tiles sent to this CTA, add them and R in FP32, round to BF16 and store
+//     their KEEP columns of each row.
 // No workspace, no second kernel: the partial sums never leave the cluster.
 // One tile per cluster (no persistent loop); the launcher sizes the grid.
 //
@@ -63,7 +64,8 @@ struct LinSkCfg {
   static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
   static constexpr int RECV_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], acc_full, recv, drain
+  // full[S], empty[S], acc_full, drain, recv[4] (one per TMEM lane group)
+  static constexpr int NUM_BARS = 2 * STAGES + 2 + 4;
   static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
   static constexpr int EPI_WARPS = 8;            // 4 TMEM lane groups x 2 column halves
   static constexpr int PRODUCER_WARP = 8;
@@ -91,8 +93,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (C::STAGES + s); };
   const uint32_t accf_bar = bars + 8u * (2 * C::STAGES);
-  const uint32_t recv_bar = bars + 8u * (2 * C::STAGES + 1);
-  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 2);
+  const uint32_t drain_bar = bars + 8u * (2 * C::STAGES + 1);
+  // the finishing warp of lane group q receives its rows' partial sums on its
+  // own barrier, so it can go on as soon as they are in
+  auto recv_bar = [&](int q) { return bars + 8u * (2 * C::STAGES + 2 + q); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -107,10 +111,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // Epilogue warps on TMEM lanes (tile rows) [32q, 32q+32) take part when
   // those rows exist; every peer agrees on which do.
   auto live = [&](int q) { return mb * C::BM + q * 32 < p.M; };
-  uint32_t live_groups = 0;
-  for (int q = 0; q < 4; ++q) live_groups += live(q) ? 1u : 0u;
   // per live lane group, each of the CS - 1 peers sends 32 rows x KEEP floats
-  const uint32_t recv_bytes = live_groups * (C::CS - 1) * 32u * C::KEEP * 4u;
+  const uint32_t recv_bytes = (C::CS - 1) * 32u * C::KEEP * 4u;
 
   if (warp == C::PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -118,11 +120,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ptx::mbar_init(empty_bar(s), 1);
     }
     ptx::mbar_init(accf_bar, 1);
-    ptx::mbar_init(recv_bar, 1);
+    for (int q = 0; q < 4; ++q) ptx::mbar_init(recv_bar(q), 1);
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
-    if (recv_bytes) ptx::mbar_arrive_expect_tx(recv_bar, recv_bytes);
+    for (int q = 0; q < 4; ++q)
+      if (live(q)) ptx::mbar_arrive_expect_tx(recv_bar(q), recv_bytes);
     ptx::prefetch_tmap(&tmX);
     ptx::prefetch_tmap(&tmW);
   }
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint32_t local =
             base + C::RECV_OFF + static_cast<uint32_t>((slot * C::BM + row) * C::KEEP * 4);
         const uint32_t dst = ptx::mapa_shared(local, static_cast<uint32_t>(g));
-        const uint32_t rbar = ptx::mapa_shared(recv_bar, static_cast<uint32_t>(g));
+        const uint32_t rbar = ptx::mapa_shared(recv_bar(q), static_cast<uint32_t>(g));
 #pragma unroll
         for (int k = 0; k < C::KEEP / 4; ++k) {
           const int c = j * C::KEEP + 4 * k;
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (h == rank / GPH) {
         bool got = true;
         const uint64_t t0 = ptx::globaltimer_ns();
-        while (!ptx::mbar_try_wait_cluster(recv_bar, 0)) {
+        while (!ptx::mbar_try_wait_cluster(recv_bar(q), 0)) {
           if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
             got = false;
             break;
