@@ -268,9 +268,10 @@ class Workload:
         self.mxfmt = name.rsplit("-", 1)[1] if self.kind == "mx" else None
         self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
-        # INT4: the [K, N/2] codes, and the K-major arrangement decoded into
-        # tensor memory (packed once at set-up, like a model load)
-        forms = (("mlp",) if self.kind == "mlp" else ("separate", "kmajor") if self.kind == "w4"
+        # INT4 and NVFP4: the [K, N/2] codes, and the K-major arrangement decoded
+        # into tensor memory (packed once at set-up, like a model load)
+        forms = (("mlp",) if self.kind == "mlp"
+                 else ("separate", "kmajor") if self.kind == "w4" or self.mxfmt == "nvfp4"
                  else ("separate",) if self.kind == "mx" else ("separate", "interleaved"))
         self.host = {}
         for M in Ms:
@@ -352,6 +353,9 @@ class Workload:
         if self.kind == "w4" and form == "kmajor":   # (A, W1k, S1, W2k, S2, Y)
             return (h[0].to(dev), sg.swiglu_pack_w4_kmajor(h[1].to(dev)), h[2].to(dev),
                     sg.swiglu_pack_w4_kmajor(h[3].to(dev)), h[4].to(dev), out)
+        if self.kind == "mx" and form == "kmajor":   # (A, C1k, S1, g1, C2k, S2, g2, Y)
+            return (h[0].to(dev), sg.swiglu_pack_w4_kmajor(h[1].to(dev)), h[2].to(dev), h[3].to(dev),
+                    sg.swiglu_pack_w4_kmajor(h[4].to(dev)), h[5].to(dev), h[6].to(dev), out)
         if self.kind in ("w4", "mx"):
             return tuple(t.to(dev) for t in h) + (out,)
         if self.kind == "mlp":
@@ -392,6 +396,9 @@ class Workload:
         if self.kind == "mx" and self.mxfmt == "mxfp8":
             return lambda: check("swiglu_fused_mxfp8", lib.swiglu_fused_mxfp8(
                 d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, self._stream()))
+        if self.kind == "mx" and form == "kmajor":
+            return lambda: check("swiglu_fused_nvfp4_kmajor", lib.swiglu_fused_nvfp4_kmajor(
+                d[0], d[1], d[2], d[3], d[4], d[5], d[6], d[7], M, N, K, self._stream()))
         if self.kind == "mx":
             return lambda: check("swiglu_fused_nvfp4", lib.swiglu_fused_nvfp4(
                 d[0], d[1], d[2], d[3], d[4], d[5], d[6], d[7], M, N, K, self._stream()))
@@ -449,6 +456,8 @@ class Workload:
             return sg.swiglu_fused_w4(*bufs[:5], bufs[5], group=W4_GROUP)
         if self.kind == "mx" and self.mxfmt == "mxfp8":
             return sg.swiglu_fused_mxfp8(*bufs[:5], bufs[5])
+        if self.kind == "mx" and form == "kmajor":
+            return sg.swiglu_fused_nvfp4_kmajor(*bufs[:7], bufs[7])
         if self.kind == "mx":
             return sg.swiglu_fused_nvfp4(*bufs[:7], bufs[7])
         if self.kind == "mlp":
@@ -481,8 +490,8 @@ class Workload:
             return "mlp"
         if self.producer:
             return "rmsnorm_quant+2sm_fp8"
-        if self.kind == "w4" and form == "kmajor":
-            return "w4_kmajor_tmem"
+        if form == "kmajor":
+            return ("w4" if self.kind == "w4" else self.mxfmt) + "_kmajor_tmem"
         if self.kind in ("w4", "mx"):   # the library's choice of kernel
             fmt = "w4" if self.kind == "w4" else self.mxfmt
             return f"{fmt}_{self.sg.WEIGHT_KERNELS[self.sg.swiglu_select_weight_kernel(M, self.N)]}"
@@ -967,8 +976,8 @@ class OracleSampler:
             a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
             wf = oracle.pack_interleaved(w1, w2)
             w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
-        self.forms = (("mlp",) if mlp else ("separate", "kmajor") if w4 else ("separate",) if mxf
-                      else ("separate", "interleaved"))
+        self.forms = (("mlp",) if mlp else ("separate", "kmajor") if w4 or mxf == "nvfp4"
+                      else ("separate",) if mxf else ("separate", "interleaved"))
         self.per_row = (6 if mlp else 4) * N * K
 
         def call(form, M, rows):

@@ -226,6 +226,20 @@ int swiglu_fused_nvfp4(const void *A, const void *C1, const void *S1, const floa
                        int64_t N, int64_t K, void *stream);
 
 /*
+ * NVFP4 weights in the K-major layout, for few tokens: the same result and
+ * scales as swiglu_fused_nvfp4, run by swiglu_fused_w4_kmajor's kernel.
+ * E2M1 codes are four-bit codes in the same [K, N/2] byte layout as INT4, so
+ * swiglu_pack_w4_kmajor turns C1, C2 into C1k, C2k ([N, K/2]) once at model
+ * load.  S1, S2: E4M3 [K/16, N] as swiglu_fused_nvfp4; g1, g2: device FP32.
+ * The codes are decoded exactly to BF16 (E2M1 * E4M3) straight into tensor
+ * memory; g1 and g2 multiply the gate and up sums before the activation.
+ * K a multiple of 64, N of 32; pointers 16-byte aligned (g1, g2: 4-byte).
+ */
+int swiglu_fused_nvfp4_kmajor(const void *A, const void *C1k, const void *S1, const float *g1,
+                              const void *C2k, const void *S2, const float *g2, void *Y,
+                              int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * The producer of the FP8 form's A operand: RMSNorm of each row of X followed
  * by per-tensor E4M3 quantisation (FP8 quantisation is what the page's
  * section "Definizione del Problema" names as raising tensor-core density; the

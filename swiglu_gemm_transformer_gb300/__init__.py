@@ -44,6 +44,7 @@ EXPORTS = {
     "swiglu_fused_w4_kmajor": ("ppppp p lll l p", ctypes.c_int),
     "swiglu_fused_mxfp8": ("ppppp p lll p", ctypes.c_int),
     "swiglu_fused_nvfp4": ("pppppppp lll p", ctypes.c_int),
+    "swiglu_fused_nvfp4_kmajor": ("pppppppp lll p", ctypes.c_int),
     "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
     "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
     "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
@@ -443,6 +444,26 @@ def swiglu_fused_nvfp4(A, C1, S1, g1, C2, S2, g2, Y=None, *, stream=None):
                                   C2.data_ptr(), S2.data_ptr(), _scale(g2, "g2"), Y.data_ptr(),
                                   M, N, K, _stream(stream))
     _check("swiglu_fused_nvfp4", rc)
+    return Y
+
+
+@_on_tensor_device
+def swiglu_fused_nvfp4_kmajor(A, C1k, S1, g1, C2k, S2, g2, Y=None, *, stream=None):
+    """swiglu_fused_nvfp4 with the codes in the K-major layout [N, K/2] of
+    swiglu_pack_w4_kmajor (weights decoded into tensor memory)."""
+    import torch
+    _need(A, "A", torch.bfloat16)
+    for t, n in ((C1k, "C1k"), (C2k, "C2k"), (S1, "S1"), (S2, "S2")):
+        _need(t, n, torch.uint8)
+    M, K = A.shape
+    N = C1k.shape[0]
+    if C1k.shape[1] * 2 != K or C2k.shape != C1k.shape or S1.shape != (K // 16, N) or S2.shape != S1.shape:
+        raise ValueError("shape mismatch")
+    Y = _out(A, N, Y)
+    rc = lib().swiglu_fused_nvfp4_kmajor(A.data_ptr(), C1k.data_ptr(), S1.data_ptr(), _scale(g1, "g1"),
+                                         C2k.data_ptr(), S2.data_ptr(), _scale(g2, "g2"), Y.data_ptr(),
+                                         M, N, K, _stream(stream))
+    _check("swiglu_fused_nvfp4_kmajor", rc)
     return Y
 
 

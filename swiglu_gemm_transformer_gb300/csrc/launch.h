@@ -64,7 +64,7 @@ cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la);
 cudaError_t launch_dq_kernel(int wf, int m_blocks, const LaunchArgs &la);
 // INT4 weights decoded into tensor memory: tok 64 or 128 tokens per pass;
 // la.p.num_n_blk CTAs of 128 weight columns, la.p.num_m_blk token blocks
-cudaError_t launch_dqt(int tok, const LaunchArgs &la);
+cudaError_t launch_dqt(int tok, bool nvfp4, const LaunchArgs &la);
 cudaError_t launch_pack_w4_kmajor(const void *Wq, void *Wk, int64_t K, int64_t N, int sm_count,
                                   cudaStream_t s);
 int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *ctx_gen);

@@ -416,24 +416,31 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
-// INT4 weights in the K-major layout of swiglu_pack_w4_kmajor ([N, K/2]
+// 4-bit weights in the K-major layout of swiglu_pack_w4_kmajor ([N, K/2]
 // bytes), decoded into tensor memory: one CTA per 128 weight columns, tokens
-// in passes of 64 or 128.
-int run_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2k,
-                  const void *S2, void *Y, int64_t M, int64_t N, int64_t K, int64_t G,
-                  void *stream) {
+// in passes of 64 or 128.  INT4 (nvfp4 = false): BF16 scales [K/G, N], G a
+// multiple of 64.  NVFP4: E4M3 scales [K/16, N] and per-tensor scales g1, g2
+// (G is 16 and not read).
+int run_kmajor(bool nvfp4, const void *A, const void *W1k, const void *S1, const float *g1,
+               const void *W2k, const void *S2, const float *g2, void *Y, int64_t M, int64_t N,
+               int64_t K, int64_t G, void *stream) {
   if (M < 0 || N < 0 || K < 0 || G <= 0) return SWIGLU_ERR_INVALID_ARG;
   if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return SWIGLU_OK;
   if (!Y) return SWIGLU_ERR_INVALID_ARG;
-  if (G % 64 != 0 || K % G != 0) return SWIGLU_ERR_UNSUPPORTED;
+  if (nvfp4 ? K % 64 != 0 : (G % 64 != 0 || K % G != 0)) return SWIGLU_ERR_UNSUPPORTED;
   if (N % 32 != 0 || K % 8 != 0) return SWIGLU_ERR_MISALIGNED;
-  if (K > 0 && (!A || !W1k || !W2k || !S1 || !S2)) return SWIGLU_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !W1k || !W2k || !S1 || !S2 || (nvfp4 && (!g1 || !g2))))
+    return SWIGLU_ERR_INVALID_ARG;
   if (!aligned16(Y) || (K > 0 && (!aligned16(A) || !aligned16(W1k) || !aligned16(W2k) ||
                                   !aligned16(S1) || !aligned16(S2))))
     return SWIGLU_ERR_MISALIGNED;
+  if (nvfp4 && K > 0 &&
+      ((reinterpret_cast<uintptr_t>(g1) & 3u) || (reinterpret_cast<uintptr_t>(g2) & 3u)))
+    return SWIGLU_ERR_MISALIGNED;
   const uint64_t y_bytes = uint64_t(M) * N * 2, a_bytes = uint64_t(M) * K * 2;
-  const uint64_t q_bytes = uint64_t(K) * N / 2, s_bytes = uint64_t(K / G) * N * 2;
+  const uint64_t q_bytes = uint64_t(K) * N / 2;
+  const uint64_t s_bytes = nvfp4 ? uint64_t(K / 16) * N : uint64_t(K / G) * N * 2;
   if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, W1k, q_bytes) ||
       overlaps(Y, y_bytes, W2k, q_bytes) || overlaps(Y, y_bytes, S1, s_bytes) ||
       overlaps(Y, y_bytes, S2, s_bytes))
@@ -454,8 +461,13 @@ int run_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, uint32_t(tok), CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1k, K / 2, N, K / 2, 32, 128, NOSW);
   if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2k, K / 2, N, K / 2, 32, 128, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, BF16, S1, N, K / G, N * 2, 128, 1, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, BF16, S2, N, K / G, N * 2, 128, 1, NOSW);
+  if (nvfp4) {
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, U8, S1, N, K / 16, N, 128, 4, NOSW);
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, U8, S2, N, K / 16, N, 128, 4, NOSW);
+  } else {
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, BF16, S1, N, K / G, N * 2, 128, 1, NOSW);
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, BF16, S2, N, K / G, N * 2, 128, 1, NOSW);
+  }
   if (rc == SWIGLU_OK) rc = encode_2d(&la.y, BF16, Y, N, M, 2 * N, 32, uint32_t(tok / 4), NOSW);
   if (rc != SWIGLU_OK) return rc;
   KParams &p = la.p;
@@ -472,10 +484,12 @@ int run_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2
   p.kb_per_split = p.num_k_blk;
   p.Y = Y;
   p.w4_group = int32_t(G);
+  p.sW1 = g1;
+  p.sW2 = g2;
   la.device = dev;
   la.ctx_gen = st->gen;
   la.stream = s;
-  return launch_dqt(tok, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  return launch_dqt(tok, nvfp4, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
 // MXFP8 (nvfp4 = false) or NVFP4 (true) weights: the split-K cluster kernel
@@ -919,7 +933,13 @@ int swiglu_pack_w4_kmajor(const void *Wq, void *Wk, int64_t K, int64_t N, void *
 int swiglu_fused_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2k,
                            const void *S2, void *Y, int64_t M, int64_t N, int64_t K,
                            int64_t group, void *stream) {
-  return run_w4_kmajor(A, W1k, S1, W2k, S2, Y, M, N, K, group, stream);
+  return run_kmajor(false, A, W1k, S1, nullptr, W2k, S2, nullptr, Y, M, N, K, group, stream);
+}
+
+int swiglu_fused_nvfp4_kmajor(const void *A, const void *C1k, const void *S1, const float *g1,
+                              const void *C2k, const void *S2, const float *g2, void *Y,
+                              int64_t M, int64_t N, int64_t K, void *stream) {
+  return run_kmajor(true, A, C1k, S1, g1, C2k, S2, g2, Y, M, N, K, 16, stream);
 }
 
 int swiglu_fused_mxfp8(const void *A, const void *C1, const void *S1, const void *C2,

@@ -42,12 +42,18 @@
 
 #include "sm103_ptx.cuh"
 #include "tc_common.cuh"
+#include "weight_decode.cuh"
 
 namespace swiglu {
 
-template <int TOK_>
+// WF_: WF_INT4 (BF16 scale per column and group of >= 64 K rows) or WF_NVFP4
+// (E2M1 codes in the same nibble layout, E4M3 scale per column and 16 K
+// rows, FP32 scale per tensor applied to the gate and up sums).
+template <int TOK_, int WF_ = WF_INT4>
 struct DqtCfg {
   static constexpr int TOK = TOK_;              // tokens per pass (MMA N)
+  static constexpr int WF = WF_;
+  static constexpr bool NV = WF_ == WF_NVFP4;
   static constexpr int BW = 128;                // weight columns per CTA (MMA M)
   static constexpr int BK = 64;                 // K per step
   // Two rings: the tokens (from L2, read by the MMA, freed by its commit) and
@@ -56,8 +62,10 @@ struct DqtCfg {
   static constexpr int A_BYTES = TOK * 128;     // tokens [TOK x 64 K], 128-byte swizzle
   static constexpr int A_STAGES = 4;            // = NBUF: stage s holds tokens and decoded buffer s
   static constexpr int CODE_BYTES = BW * 32;    // per matrix: 128 columns x 64 codes
-  static constexpr int SCALE_BYTES = BW * 2;    // per matrix: one BF16 scale per column
-  static constexpr int C_BYTES = 2 * CODE_BYTES + 2 * SCALE_BYTES;  // 8.5 KB
+  // per matrix and K step: one BF16 scale row (INT4) or four E4M3 rows (NVFP4)
+  static constexpr int SCALE_ROWS = NV ? 4 : 1;
+  static constexpr int SCALE_BYTES = BW * (NV ? 4 : 2);
+  static constexpr int C_BYTES = 2 * CODE_BYTES + 2 * SCALE_BYTES;  // 8.5 KB (INT4), 9 KB (NVFP4)
   static constexpr int C_STAGES = 12;
   static constexpr int NBUF = 4;                // decoded K steps in TMEM
   static constexpr int BUF_COL0 = 256;          // decoded buffers: columns [256 + 64 b, +64)
@@ -78,6 +86,7 @@ struct DqtCfg {
   static constexpr int THREADS = 32 * 20;
   static constexpr uint32_t IDESC = ptx::idesc_bf16(128, TOK, false, false);
   static_assert(TOK == 64 || TOK == 128, "tokens per pass");
+  static_assert(WF == WF_INT4 || WF == WF_NVFP4, "4-bit codes");
   static_assert(2 * TOK <= BUF_COL0 && BUF_COL0 + NBUF * 64 <= TMEM_COLS, "TMEM map");
   static_assert(C_BYTES % 128 == 0 && STG_BYTES % 128 == 0, "128-byte aligned copies");
   static_assert(A_STAGES == NBUF, "one barrier pair per tokens stage and decoded buffer");
@@ -102,6 +111,36 @@ __device__ __forceinline__ static void decode_kmajor_int4_half(const uint4 &w, u
       const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&t), k136);
       const __nv_bfloat162 v = __hmul2(q, s2);
       r[4 * j + i] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+  }
+}
+
+// Half a step of NVFP4: 32 K values of one column from 16 bytes of codes
+// (words of eight, the pair (k, k + 1) in nibbles i and 4 + i as for INT4),
+// with the E4M3 scales of its two 16-row blocks in the low two bytes of
+// `s01` (first block low), 16 pairs into r[0..15].  An E2M1 code s e1 e0 m
+// with e1 e0 m placed at BF16 bits 8..6 and s at bit 15 is the BF16 number
+// E2M1 * 2^-126 (e = 0, m = 1: the subnormal 2^-127); the multiplies by 2^126
+// and by the scale are exact (at most 2 + 4 significant bits).
+__device__ __forceinline__ static void decode_kmajor_nvfp4_half(const uint4 &w, uint32_t s01,
+                                                                uint32_t *r) {
+  const float2 sf = e4m3x2_to_float2(s01 & 0xFFFFu);
+  const uint32_t sp[2] = {bf16x2_bits(sf.x, sf.x), bf16x2_bits(sf.y, sf.y)};
+  const uint32_t k126 = 0x7E807E80u;  // 2^126 in both halves
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x = words[j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // magnitude bits of nibbles i, 4 + i to bits 8..6 and 24..22; sign bits to 15 and 31
+      const uint32_t mag = (i == 0 ? x << 6 : i == 1 ? x << 2 : i == 2 ? x >> 2 : x >> 6) & 0x01C001C0u;
+      const uint32_t sgn = (i == 0 ? x << 12 : i == 1 ? x << 8 : i == 2 ? x << 4 : x) & 0x80008000u;
+      const uint32_t y = mag | sgn;
+      const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&y),
+                                       *reinterpret_cast<const __nv_bfloat162 *>(&k126));
+      const __nv_bfloat162 o = __hmul2(v, *reinterpret_cast<const __nv_bfloat162 *>(&sp[j >> 1]));
+      r[4 * j + i] = *reinterpret_cast<const uint32_t *>(&o);
     }
   }
 }
@@ -215,7 +254,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       produce(C::C_STAGES, cfull_bar, cempty_bar, C::C_BYTES, [&](uint32_t s, uint32_t fb, int g) {
         const int kb = kstep(g % nk);
         const uint32_t r = base + C::C_OFF + s * C::C_BYTES;
-        const int srow = kb * C::BK / p.w4_group;
+        const int srow = C::NV ? kb * C::SCALE_ROWS : kb * C::BK / p.w4_group;
         ptx::tma_load_2d(r, &tmC1, fb, kb * (C::BK / 2), n0);
         ptx::tma_load_2d(r + C::CODE_BYTES, &tmC2, fb, kb * (C::BK / 2), n0);
         ptx::tma_load_2d(r + 2 * C::CODE_BYTES, &tmS1, fb, n0, srow);
@@ -270,6 +309,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int c = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stg = base + C::STG_OFF + warp * C::STG_BYTES;
+    const float gs = C::NV ? *p.sW1 : 1.0f;  // per-tensor scales of NVFP4 codes
+    const float us = C::NV ? *p.sW2 : 1.0f;
     bool ok = true;
     for (int tb = 0; tb < nt && ok; ++tb) {
       for (int i = 0; i < nk; ++i) {
@@ -284,11 +325,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint8_t *st = smem + C::C_OFF + s * C::C_BYTES;
         const uint4 *cw = reinterpret_cast<const uint4 *>(st + mtx * C::CODE_BYTES + c * 32);
         const uint4 w0 = cw[0], w1 = cw[1];
-        const uint32_t sbits =
-            *reinterpret_cast<const uint16_t *>(st + 2 * C::CODE_BYTES + mtx * C::SCALE_BYTES + c * 2);
+        const uint8_t *sc = st + 2 * C::CODE_BYTES + mtx * C::SCALE_BYTES;
         uint32_t r[32];
-        decode_kmajor_int4_half(w0, sbits, r);
-        decode_kmajor_int4_half(w1, sbits, r + 16);
+        if constexpr (C::NV) {
+          // scale rows 0..3 (16 K rows each) at sc + 128 row: column c's byte
+          decode_kmajor_nvfp4_half(w0, uint32_t(sc[c]) | (uint32_t(sc[C::BW + c]) << 8), r);
+          decode_kmajor_nvfp4_half(w1, uint32_t(sc[2 * C::BW + c]) | (uint32_t(sc[3 * C::BW + c]) << 8),
+                                   r + 16);
+        } else {
+          const uint32_t sbits = *reinterpret_cast<const uint16_t *>(sc + c * 2);
+          decode_kmajor_int4_half(w0, sbits, r);
+          decode_kmajor_int4_half(w1, sbits, r + 16);
+        }
         // The codes were consumed by the decode above: release the stage.
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(cempty_bar(s));
@@ -321,7 +369,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          yv[16 * j + e] = silu_mul(__uint_as_float(g16[e]), __uint_as_float(u16[e]));
+          yv[16 * j + e] = C::NV ? silu_mul(gs * __uint_as_float(g16[e]), us * __uint_as_float(u16[e]))
+                                 : silu_mul(__uint_as_float(g16[e]), __uint_as_float(u16[e]));
       }
       // accumulators read: the next token block's MMAs may start
       ptx::tc_fence_before();

@@ -68,6 +68,64 @@ def test_mx_7b_shape_sampled(sg, fmt, M):
     _run(sg, fmt, M, N, K, seed=2, rows=si.sample_rows(M, 128, 32, seed=2))
 
 
+# ---- NVFP4 codes in the K-major layout, decoded into tensor memory --------------------------
+
+def _run_nvfp4_kmajor(sg, M, N, K, seed, rows=None):
+    A, w1, w2 = si.make_mx(M, N, K, seed, "nvfp4")
+    # E2M1 codes share INT4's [K, N/2] nibble layout: the INT4 packer serves both
+    C1k = sg.swiglu_pack_w4_kmajor(w1[0].to(DEV))
+    C2k = sg.swiglu_pack_w4_kmajor(w2[0].to(DEV))
+    g1 = torch.tensor([w1[2]], dtype=torch.float32, device=DEV)
+    g2 = torch.tensor([w2[2]], dtype=torch.float32, device=DEV)
+    Y = sg.swiglu_fused_nvfp4_kmajor(A.to(DEV), C1k, w1[1].to(DEV), g1, C2k, w2[1].to(DEV), g2)
+    rc, detail = sg.swiglu_device_status()
+    assert rc == sg.OK, (sg.status_string(rc), detail)
+    assert np.array_equal(C2k.cpu().numpy(), oracle.pack_w4_kmajor(w2[0].numpy()))
+    o1 = (w1[0].numpy(), w1[1].numpy(), float(np.float32(w1[2])))
+    o2 = (w2[0].numpy(), w2[1].numpy(), float(np.float32(w2[2])))
+    ref = oracle.swiglu_mx(si.bits_u16(A), "nvfp4", o1, o2, rows=rows)
+    got = Y.double().cpu().numpy()
+    if rows is not None:
+        got = got[rows]
+    oracle.assert_parity(got, ref, f"nvfp4 k-major {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("shape", [(1, 64, 64), (7, 96, 128), (63, 288, 384), (64, 4864, 896),
+                                   (65, 4896, 896), (128, 1152, 448),
+                                   # several 128-token passes, the last one ragged
+                                   (300, 640, 256), (129, 256, 128),
+                                   # ragged last column block (9760 = 76 x 128 + 32)
+                                   (100, 9760, 256)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_nvfp4_kmajor_shapes(sg, shape):
+    M, N, K = shape
+    _run_nvfp4_kmajor(sg, M, N, K, seed=5 * M + N + K)
+
+
+@pytest.mark.parametrize("M", [64, 128])
+def test_nvfp4_kmajor_7b_shape_sampled(sg, M):
+    N, K = 18944, 3584
+    _run_nvfp4_kmajor(sg, M, N, K, seed=6, rows=si.sample_rows(M, 64, 24, seed=6))
+
+
+def test_nvfp4_kmajor_argument_errors(sg):
+    lib = sg.lib()
+    A = torch.zeros(4, 128, dtype=torch.bfloat16, device=DEV)
+    Ck = torch.zeros(64, 64, dtype=torch.uint8, device=DEV)
+    S = torch.zeros(8, 64, dtype=torch.uint8, device=DEV)
+    g = torch.ones(1, device=DEV)
+    Y = torch.empty(4, 64, dtype=torch.bfloat16, device=DEV)
+    p = [A.data_ptr(), Ck.data_ptr(), S.data_ptr(), g.data_ptr(), Ck.data_ptr(), S.data_ptr(), g.data_ptr(),
+         Y.data_ptr()]
+    f = lib.swiglu_fused_nvfp4_kmajor
+    assert f(*p, 4, 64, 96, None) == sg.ERR_UNSUPPORTED                        # K not a multiple of 64
+    assert f(*p, 4, 48, 128, None) == sg.ERR_MISALIGNED                        # N not a multiple of 32
+    assert f(*p[:3], None, *p[4:], 4, 64, 128, None) == sg.ERR_INVALID_ARG     # missing tensor scale
+    assert f(*p[:7], A.data_ptr(), 4, 64, 128, None) == sg.ERR_INVALID_ARG     # Y overlaps A
+    assert f(*p, 0, 64, 128, None) == sg.OK
+    torch.cuda.synchronize()
+
+
 def test_mx_argument_errors(sg):
     lib = sg.lib()
     A = torch.zeros(4, 128, dtype=torch.bfloat16, device=DEV)
