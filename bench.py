@@ -268,11 +268,10 @@ class Workload:
         self.mxfmt = name.rsplit("-", 1)[1] if self.kind == "mx" else None
         self.fp8 = self.kind == "fp8"
         self.eb = 1 if self.fp8 else 2
-        # INT4 and NVFP4: the [K, N/2] codes, and the K-major arrangement decoded
-        # into tensor memory (packed once at set-up, like a model load)
-        forms = (("mlp",) if self.kind == "mlp"
-                 else ("separate", "kmajor") if self.kind == "w4" or self.mxfmt == "nvfp4"
-                 else ("separate",) if self.kind == "mx" else ("separate", "interleaved"))
+        # INT4, MXFP8 and NVFP4: the codes as [K, N], and K-major, decoded into
+        # tensor memory (packed once at set-up, like a model load)
+        forms = (("mlp",) if self.kind == "mlp" else ("separate", "kmajor") if self.kind in ("w4", "mx")
+                 else ("separate", "interleaved"))
         self.host = {}
         for M in Ms:
             if self.producer:   # X and gamma in BF16; the FP8 weights of the same recipe
@@ -353,6 +352,9 @@ class Workload:
         if self.kind == "w4" and form == "kmajor":   # (A, W1k, S1, W2k, S2, Y)
             return (h[0].to(dev), sg.swiglu_pack_w4_kmajor(h[1].to(dev)), h[2].to(dev),
                     sg.swiglu_pack_w4_kmajor(h[3].to(dev)), h[4].to(dev), out)
+        if self.mxfmt == "mxfp8" and form == "kmajor":   # (A, C1k, S1, C2k, S2, Y)
+            return (h[0].to(dev), h[1].t().contiguous().to(dev), h[2].to(dev),
+                    h[3].t().contiguous().to(dev), h[4].to(dev), out)
         if self.kind == "mx" and form == "kmajor":   # (A, C1k, S1, g1, C2k, S2, g2, Y)
             return (h[0].to(dev), sg.swiglu_pack_w4_kmajor(h[1].to(dev)), h[2].to(dev), h[3].to(dev),
                     sg.swiglu_pack_w4_kmajor(h[4].to(dev)), h[5].to(dev), h[6].to(dev), out)
@@ -393,6 +395,9 @@ class Workload:
         if self.kind == "w4":
             return lambda: check("swiglu_fused_w4", lib.swiglu_fused_w4(
                 d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, W4_GROUP, self._stream()))
+        if self.mxfmt == "mxfp8" and form == "kmajor":
+            return lambda: check("swiglu_fused_mxfp8_kmajor", lib.swiglu_fused_mxfp8_kmajor(
+                d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, self._stream()))
         if self.kind == "mx" and self.mxfmt == "mxfp8":
             return lambda: check("swiglu_fused_mxfp8", lib.swiglu_fused_mxfp8(
                 d[0], d[1], d[2], d[3], d[4], d[5], M, N, K, self._stream()))
@@ -454,6 +459,8 @@ class Workload:
             return sg.swiglu_fused_w4_kmajor(*bufs[:5], bufs[5], group=W4_GROUP)
         if self.kind == "w4":
             return sg.swiglu_fused_w4(*bufs[:5], bufs[5], group=W4_GROUP)
+        if self.mxfmt == "mxfp8" and form == "kmajor":
+            return sg.swiglu_fused_mxfp8_kmajor(*bufs[:5], bufs[5])
         if self.kind == "mx" and self.mxfmt == "mxfp8":
             return sg.swiglu_fused_mxfp8(*bufs[:5], bufs[5])
         if self.kind == "mx" and form == "kmajor":
@@ -976,8 +983,8 @@ class OracleSampler:
             a, w1, w2 = si.bits_u16(A), si.bits_u16(W1), si.bits_u16(W2)
             wf = oracle.pack_interleaved(w1, w2)
             w3 = si.bits_u16(si.make_bf16(1, K, N, seed + 100)[1]) if mlp else None
-        self.forms = (("mlp",) if mlp else ("separate", "kmajor") if w4 or mxf == "nvfp4"
-                      else ("separate",) if mxf else ("separate", "interleaved"))
+        self.forms = (("mlp",) if mlp else ("separate", "kmajor") if w4 or mxf
+                      else ("separate", "interleaved"))
         self.per_row = (6 if mlp else 4) * N * K
 
         def call(form, M, rows):

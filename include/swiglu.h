@@ -226,6 +226,21 @@ int swiglu_fused_nvfp4(const void *A, const void *C1, const void *S1, const floa
                        int64_t N, int64_t K, void *stream);
 
 /*
+ * MXFP8 weights in a K-major layout, for few tokens: the same result and
+ * scales as swiglu_fused_mxfp8, run by swiglu_fused_w4_kmajor's kernel.
+ *   C1k, C2k: E4M3 codes, uint8 [N, K]: the byte transpose of
+ *             swiglu_fused_mxfp8's [K, N] codes (row n holds column n's K
+ *             codes), made once at model load.
+ *   S1, S2:   E8M0 scales, uint8 [K/32, N], as swiglu_fused_mxfp8.
+ * The codes are decoded to BF16 (E4M3 * 2^(e-127), exact in FP32, rounded
+ * once) straight into tensor memory.  K a multiple of 64, N of 32; pointers
+ * 16-byte aligned.
+ */
+int swiglu_fused_mxfp8_kmajor(const void *A, const void *C1k, const void *S1, const void *C2k,
+                              const void *S2, void *Y, int64_t M, int64_t N, int64_t K,
+                              void *stream);
+
+/*
  * NVFP4 weights in the K-major layout, for few tokens: the same result and
  * scales as swiglu_fused_nvfp4, run by swiglu_fused_w4_kmajor's kernel.
  * E2M1 codes are four-bit codes in the same [K, N/2] byte layout as INT4, so

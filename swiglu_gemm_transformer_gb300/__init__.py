@@ -45,6 +45,7 @@ EXPORTS = {
     "swiglu_fused_mxfp8": ("ppppp p lll p", ctypes.c_int),
     "swiglu_fused_nvfp4": ("pppppppp lll p", ctypes.c_int),
     "swiglu_fused_nvfp4_kmajor": ("pppppppp lll p", ctypes.c_int),
+    "swiglu_fused_mxfp8_kmajor": ("ppppp p lll p", ctypes.c_int),
     "swiglu_linear_workspace_size": ("lll", ctypes.c_uint64),
     "swiglu_linear": ("pppp lll pQ p", ctypes.c_int),
     "swiglu_mlp_workspace_size": ("lll", ctypes.c_uint64),
@@ -423,6 +424,25 @@ def swiglu_fused_mxfp8(A, C1, S1, C2, S2, Y=None, *, stream=None):
     rc = lib().swiglu_fused_mxfp8(A.data_ptr(), C1.data_ptr(), S1.data_ptr(), C2.data_ptr(),
                                   S2.data_ptr(), Y.data_ptr(), M, N, K, _stream(stream))
     _check("swiglu_fused_mxfp8", rc)
+    return Y
+
+
+@_on_tensor_device
+def swiglu_fused_mxfp8_kmajor(A, C1k, S1, C2k, S2, Y=None, *, stream=None):
+    """swiglu_fused_mxfp8 with the codes K-major: C1k/C2k uint8 [N,K], the
+    transposes of the [K,N] codes (weights decoded into tensor memory)."""
+    import torch
+    _need(A, "A", torch.bfloat16)
+    for t, n in ((C1k, "C1k"), (C2k, "C2k"), (S1, "S1"), (S2, "S2")):
+        _need(t, n, torch.uint8)
+    M, K = A.shape
+    N = C1k.shape[0]
+    if C1k.shape != (N, K) or C2k.shape != C1k.shape or S1.shape != (K // 32, N) or S2.shape != S1.shape:
+        raise ValueError("shape mismatch")
+    Y = _out(A, N, Y)
+    rc = lib().swiglu_fused_mxfp8_kmajor(A.data_ptr(), C1k.data_ptr(), S1.data_ptr(), C2k.data_ptr(),
+                                         S2.data_ptr(), Y.data_ptr(), M, N, K, _stream(stream))
+    _check("swiglu_fused_mxfp8_kmajor", rc)
     return Y
 
 

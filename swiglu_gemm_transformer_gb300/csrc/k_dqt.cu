@@ -1,4 +1,4 @@
-// k_dqt.cu -- INT4 and NVFP4 weights decoded into tensor memory (swiglu_dqt_kernel.cuh),
+// k_dqt.cu -- INT4, MXFP8 and NVFP4 weights decoded into tensor memory (swiglu_dqt_kernel.cuh),
 // and the packer that writes the K-major code layout it reads.
 #include "launch.h"
 #include "swiglu_dqt_kernel.cuh"
@@ -56,9 +56,11 @@ __global__ void pack_w4_kmajor_kernel(const uint8_t *__restrict__ Wq, uint32_t *
 
 }  // namespace
 
-cudaError_t launch_dqt(int tok, bool nvfp4, const LaunchArgs &la) {
-  if (nvfp4)
+cudaError_t launch_dqt(int tok, int wf, const LaunchArgs &la) {
+  if (wf == WF_NVFP4)
     return tok == 64 ? launch_dqt_cfg<DqtCfg<64, WF_NVFP4>>(la) : launch_dqt_cfg<DqtCfg<128, WF_NVFP4>>(la);
+  if (wf == WF_MXFP8)
+    return tok == 64 ? launch_dqt_cfg<DqtCfg<64, WF_MXFP8>>(la) : launch_dqt_cfg<DqtCfg<128, WF_MXFP8>>(la);
   return tok == 64 ? launch_dqt_cfg<DqtCfg<64>>(la) : launch_dqt_cfg<DqtCfg<128>>(la);
 }
 

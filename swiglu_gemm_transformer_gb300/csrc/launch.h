@@ -62,9 +62,9 @@ cudaError_t launch_mx_sk(bool nvfp4, const LaunchArgs &la);
 // wf: 1 INT4, 2 MXFP8, 3 NVFP4 (weight_decode.cuh); m_blocks: 128-row blocks
 // per CTA (1, or 2 with la.p.num_m_blk counting 256-row blocks)
 cudaError_t launch_dq_kernel(int wf, int m_blocks, const LaunchArgs &la);
-// INT4 weights decoded into tensor memory: tok 64 or 128 tokens per pass;
-// la.p.num_n_blk CTAs of 128 weight columns, la.p.num_m_blk token blocks
-cudaError_t launch_dqt(int tok, bool nvfp4, const LaunchArgs &la);
+// INT4, MXFP8 or NVFP4 weights (wf 1, 2, 3) decoded into tensor memory: tok 64
+// or 128 tokens per pass; la.p.num_n_blk CTAs of 128 weight columns
+cudaError_t launch_dqt(int tok, int wf, const LaunchArgs &la);
 cudaError_t launch_pack_w4_kmajor(const void *Wq, void *Wk, int64_t K, int64_t N, int sm_count,
                                   cudaStream_t s);
 int device_info(uint32_t **err, int *sm_count, uint64_t *timeout_ns, uint64_t *ctx_gen);

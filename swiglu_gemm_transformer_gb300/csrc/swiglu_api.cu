@@ -416,19 +416,21 @@ int run_w4(const void *A, const void *W1q, const void *S1, const void *W2q, cons
   return e == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
-// 4-bit weights in the K-major layout of swiglu_pack_w4_kmajor ([N, K/2]
-// bytes), decoded into tensor memory: one CTA per 128 weight columns, tokens
-// in passes of 64 or 128.  INT4 (nvfp4 = false): BF16 scales [K/G, N], G a
-// multiple of 64.  NVFP4: E4M3 scales [K/16, N] and per-tensor scales g1, g2
-// (G is 16 and not read).
-int run_kmajor(bool nvfp4, const void *A, const void *W1k, const void *S1, const float *g1,
+// Weights in a K-major layout, decoded into tensor memory: one CTA per 128
+// weight columns, tokens in passes of 64 or 128.  wf 1, INT4: codes [N, K/2]
+// (swiglu_pack_w4_kmajor), BF16 scales [K/G, N], G a multiple of 64.  wf 2,
+// MXFP8: E4M3 codes [N, K], E8M0 scales [K/32, N].  wf 3, NVFP4: E2M1 codes
+// [N, K/2] (swiglu_pack_w4_kmajor), E4M3 scales [K/16, N], per-tensor scales
+// g1, g2.  G is read for INT4 only.
+int run_kmajor(int wf, const void *A, const void *W1k, const void *S1, const float *g1,
                const void *W2k, const void *S2, const float *g2, void *Y, int64_t M, int64_t N,
                int64_t K, int64_t G, void *stream) {
+  const bool nvfp4 = wf == 3, mxfp8 = wf == 2;
   if (M < 0 || N < 0 || K < 0 || G <= 0) return SWIGLU_ERR_INVALID_ARG;
   if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return SWIGLU_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return SWIGLU_OK;
   if (!Y) return SWIGLU_ERR_INVALID_ARG;
-  if (nvfp4 ? K % 64 != 0 : (G % 64 != 0 || K % G != 0)) return SWIGLU_ERR_UNSUPPORTED;
+  if (wf == 1 ? (G % 64 != 0 || K % G != 0) : K % 64 != 0) return SWIGLU_ERR_UNSUPPORTED;
   if (N % 32 != 0 || K % 8 != 0) return SWIGLU_ERR_MISALIGNED;
   if (K > 0 && (!A || !W1k || !W2k || !S1 || !S2 || (nvfp4 && (!g1 || !g2))))
     return SWIGLU_ERR_INVALID_ARG;
@@ -439,8 +441,9 @@ int run_kmajor(bool nvfp4, const void *A, const void *W1k, const void *S1, const
       ((reinterpret_cast<uintptr_t>(g1) & 3u) || (reinterpret_cast<uintptr_t>(g2) & 3u)))
     return SWIGLU_ERR_MISALIGNED;
   const uint64_t y_bytes = uint64_t(M) * N * 2, a_bytes = uint64_t(M) * K * 2;
-  const uint64_t q_bytes = uint64_t(K) * N / 2;
-  const uint64_t s_bytes = nvfp4 ? uint64_t(K / 16) * N : uint64_t(K / G) * N * 2;
+  const uint64_t q_bytes = mxfp8 ? uint64_t(K) * N : uint64_t(K) * N / 2;
+  const uint64_t s_bytes = nvfp4 ? uint64_t(K / 16) * N
+                           : mxfp8 ? uint64_t(K / 32) * N : uint64_t(K / G) * N * 2;
   if (overlaps(Y, y_bytes, A, a_bytes) || overlaps(Y, y_bytes, W1k, q_bytes) ||
       overlaps(Y, y_bytes, W2k, q_bytes) || overlaps(Y, y_bytes, S1, s_bytes) ||
       overlaps(Y, y_bytes, S2, s_bytes))
@@ -459,12 +462,20 @@ int run_kmajor(bool nvfp4, const void *A, const void *W1k, const void *S1, const
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto NOSW = CU_TENSOR_MAP_SWIZZLE_NONE;
   rc = encode_2d(&la.a, BF16, A, K, M, K * 2, 64, uint32_t(tok), CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1k, K / 2, N, K / 2, 32, 128, NOSW);
-  if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2k, K / 2, N, K / 2, 32, 128, NOSW);
+  if (mxfp8) {   // a column's 64 codes per K step, 64-byte swizzle (the kernel undoes it)
+    const auto SW64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1k, K, N, K, 64, 128, SW64);
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2k, K, N, K, 64, 128, SW64);
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, U8, S1, N, K / 32, N, 128, 2, NOSW);
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, U8, S2, N, K / 32, N, 128, 2, NOSW);
+  } else {
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.b0, U8, W1k, K / 2, N, K / 2, 32, 128, NOSW);
+    if (rc == SWIGLU_OK) rc = encode_2d(&la.b1, U8, W2k, K / 2, N, K / 2, 32, 128, NOSW);
+  }
   if (nvfp4) {
     if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, U8, S1, N, K / 16, N, 128, 4, NOSW);
     if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, U8, S2, N, K / 16, N, 128, 4, NOSW);
-  } else {
+  } else if (!mxfp8) {
     if (rc == SWIGLU_OK) rc = encode_2d(&la.s1, BF16, S1, N, K / G, N * 2, 128, 1, NOSW);
     if (rc == SWIGLU_OK) rc = encode_2d(&la.s2, BF16, S2, N, K / G, N * 2, 128, 1, NOSW);
   }
@@ -489,7 +500,7 @@ int run_kmajor(bool nvfp4, const void *A, const void *W1k, const void *S1, const
   la.device = dev;
   la.ctx_gen = st->gen;
   la.stream = s;
-  return launch_dqt(tok, nvfp4, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
+  return launch_dqt(tok, wf, la) == cudaSuccess ? SWIGLU_OK : SWIGLU_ERR_CUDA;
 }
 
 // MXFP8 (nvfp4 = false) or NVFP4 (true) weights: the split-K cluster kernel
@@ -933,13 +944,19 @@ int swiglu_pack_w4_kmajor(const void *Wq, void *Wk, int64_t K, int64_t N, void *
 int swiglu_fused_w4_kmajor(const void *A, const void *W1k, const void *S1, const void *W2k,
                            const void *S2, void *Y, int64_t M, int64_t N, int64_t K,
                            int64_t group, void *stream) {
-  return run_kmajor(false, A, W1k, S1, nullptr, W2k, S2, nullptr, Y, M, N, K, group, stream);
+  return run_kmajor(1, A, W1k, S1, nullptr, W2k, S2, nullptr, Y, M, N, K, group, stream);
+}
+
+int swiglu_fused_mxfp8_kmajor(const void *A, const void *C1k, const void *S1, const void *C2k,
+                              const void *S2, void *Y, int64_t M, int64_t N, int64_t K,
+                              void *stream) {
+  return run_kmajor(2, A, C1k, S1, nullptr, C2k, S2, nullptr, Y, M, N, K, 32, stream);
 }
 
 int swiglu_fused_nvfp4_kmajor(const void *A, const void *C1k, const void *S1, const float *g1,
                               const void *C2k, const void *S2, const float *g2, void *Y,
                               int64_t M, int64_t N, int64_t K, void *stream) {
-  return run_kmajor(true, A, C1k, S1, g1, C2k, S2, g2, Y, M, N, K, 16, stream);
+  return run_kmajor(3, A, C1k, S1, g1, C2k, S2, g2, Y, M, N, K, 16, stream);
 }
 
 int swiglu_fused_mxfp8(const void *A, const void *C1, const void *S1, const void *C2,

@@ -46,14 +46,16 @@
 
 namespace swiglu {
 
-// WF_: WF_INT4 (BF16 scale per column and group of >= 64 K rows) or WF_NVFP4
+// WF_: WF_INT4 (BF16 scale per column and group of >= 64 K rows), WF_NVFP4
 // (E2M1 codes in the same nibble layout, E4M3 scale per column and 16 K
-// rows, FP32 scale per tensor applied to the gate and up sums).
+// rows, FP32 scale per tensor applied to the gate and up sums) or WF_MXFP8
+// (E4M3 codes, one byte each, [N, K]; E8M0 scale per column and 32 K rows).
 template <int TOK_, int WF_ = WF_INT4>
 struct DqtCfg {
   static constexpr int TOK = TOK_;              // tokens per pass (MMA N)
   static constexpr int WF = WF_;
   static constexpr bool NV = WF_ == WF_NVFP4;
+  static constexpr bool MX = WF_ == WF_MXFP8;
   static constexpr int BW = 128;                // weight columns per CTA (MMA M)
   static constexpr int BK = 64;                 // K per step
   // Two rings: the tokens (from L2, read by the MMA, freed by its commit) and
@@ -61,12 +63,15 @@ struct DqtCfg {
   // they are decoded), so the weight stream runs many steps ahead of the MMAs.
   static constexpr int A_BYTES = TOK * 128;     // tokens [TOK x 64 K], 128-byte swizzle
   static constexpr int A_STAGES = 4;            // = NBUF: stage s holds tokens and decoded buffer s
-  static constexpr int CODE_BYTES = BW * 32;    // per matrix: 128 columns x 64 codes
-  // per matrix and K step: one BF16 scale row (INT4) or four E4M3 rows (NVFP4)
-  static constexpr int SCALE_ROWS = NV ? 4 : 1;
+  static constexpr int ROW_BYTES = MX ? 64 : 32;  // a column's 64 codes
+  static constexpr int CODE_BYTES = BW * ROW_BYTES;  // per matrix: 128 columns x 64 codes
+  // per matrix and K step: one BF16 scale row (INT4), two E8M0 rows (MXFP8)
+  // or four E4M3 rows (NVFP4)
+  static constexpr int SCALE_ROWS = NV ? 4 : MX ? 2 : 1;
   static constexpr int SCALE_BYTES = BW * (NV ? 4 : 2);
-  static constexpr int C_BYTES = 2 * CODE_BYTES + 2 * SCALE_BYTES;  // 8.5 KB (INT4), 9 KB (NVFP4)
-  static constexpr int C_STAGES = 12;
+  // 8.5 KB (INT4), 9 KB (NVFP4), 16.5 KB (MXFP8)
+  static constexpr int C_BYTES = 2 * CODE_BYTES + 2 * SCALE_BYTES;
+  static constexpr int C_STAGES = MX ? 6 : 12;
   static constexpr int NBUF = 4;                // decoded K steps in TMEM
   static constexpr int BUF_COL0 = 256;          // decoded buffers: columns [256 + 64 b, +64)
   static constexpr int TMEM_COLS = 512;
@@ -86,7 +91,10 @@ struct DqtCfg {
   static constexpr int THREADS = 32 * 20;
   static constexpr uint32_t IDESC = ptx::idesc_bf16(128, TOK, false, false);
   static_assert(TOK == 64 || TOK == 128, "tokens per pass");
-  static_assert(WF == WF_INT4 || WF == WF_NVFP4, "4-bit codes");
+  static_assert(WF == WF_INT4 || WF == WF_NVFP4 || WF == WF_MXFP8, "weight format");
+  // MXFP8 codes arrive with the 64-byte swizzle, whose pattern repeats every 512 bytes
+  static_assert(!MX || (C_OFF % 512 == 0 && C_BYTES % 512 == 0 && CODE_BYTES % 512 == 0),
+                "swizzled code tiles start on 512-byte boundaries");
   static_assert(2 * TOK <= BUF_COL0 && BUF_COL0 + NBUF * 64 <= TMEM_COLS, "TMEM map");
   static_assert(C_BYTES % 128 == 0 && STG_BYTES % 128 == 0, "128-byte aligned copies");
   static_assert(A_STAGES == NBUF, "one barrier pair per tokens stage and decoded buffer");
@@ -142,6 +150,22 @@ __device__ __forceinline__ static void decode_kmajor_nvfp4_half(const uint4 &w, 
       const __nv_bfloat162 o = __hmul2(v, *reinterpret_cast<const __nv_bfloat162 *>(&sp[j >> 1]));
       r[4 * j + i] = *reinterpret_cast<const uint32_t *>(&o);
     }
+  }
+}
+
+// Half a step of MXFP8: 32 K values of one column from 32 bytes of E4M3
+// codes (byte i = K row i), all under one E8M0 block scale `p` (2^(e-127) as
+// a float), 16 pairs into r[0..15].  E4M3 * 2^(e-127) is exact in FP32 and
+// rounded once to BF16, as in the shared-memory decode.
+__device__ __forceinline__ static void decode_kmajor_mxfp8_half(const uint4 &lo, const uint4 &hi,
+                                                                float p, uint32_t *r) {
+  const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 f0 = e4m3x2_to_float2(words[j] & 0xFFFFu);
+    const float2 f1 = e4m3x2_to_float2(words[j] >> 16);
+    r[2 * j] = bf16x2_bits(__fmul_rn(f0.x, p), __fmul_rn(f0.y, p));
+    r[2 * j + 1] = bf16x2_bits(__fmul_rn(f1.x, p), __fmul_rn(f1.y, p));
   }
 }
 
@@ -254,9 +278,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       produce(C::C_STAGES, cfull_bar, cempty_bar, C::C_BYTES, [&](uint32_t s, uint32_t fb, int g) {
         const int kb = kstep(g % nk);
         const uint32_t r = base + C::C_OFF + s * C::C_BYTES;
-        const int srow = C::NV ? kb * C::SCALE_ROWS : kb * C::BK / p.w4_group;
-        ptx::tma_load_2d(r, &tmC1, fb, kb * (C::BK / 2), n0);
-        ptx::tma_load_2d(r + C::CODE_BYTES, &tmC2, fb, kb * (C::BK / 2), n0);
+        const int srow = C::WF == WF_INT4 ? kb * C::BK / p.w4_group : kb * C::SCALE_ROWS;
+        ptx::tma_load_2d(r, &tmC1, fb, kb * C::ROW_BYTES, n0);
+        ptx::tma_load_2d(r + C::CODE_BYTES, &tmC2, fb, kb * C::ROW_BYTES, n0);
         ptx::tma_load_2d(r + 2 * C::CODE_BYTES, &tmS1, fb, n0, srow);
         ptx::tma_load_2d(r + 2 * C::CODE_BYTES + C::SCALE_BYTES, &tmS2, fb, n0, srow);
       });
@@ -323,16 +347,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint8_t *st = smem + C::C_OFF + s * C::C_BYTES;
-        const uint4 *cw = reinterpret_cast<const uint4 *>(st + mtx * C::CODE_BYTES + c * 32);
-        const uint4 w0 = cw[0], w1 = cw[1];
         const uint8_t *sc = st + 2 * C::CODE_BYTES + mtx * C::SCALE_BYTES;
         uint32_t r[32];
-        if constexpr (C::NV) {
+        if constexpr (C::MX) {
+          // column c's 64 bytes, 16-byte chunk j at chunk j ^ ((c >> 1) & 3) (the
+          // 64-byte swizzle: address bits 4-5 ^= bits 7-8), so that the eight
+          // lanes of a load phase hit eight different bank groups
+          const uint8_t *row = st + mtx * C::CODE_BYTES + c * C::ROW_BYTES;
+          const uint32_t sw = static_cast<uint32_t>(c >> 1) & 3u;
+          uint4 w[4];
+#pragma unroll
+          for (uint32_t j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(row + ((j ^ sw) << 4));
+          const uint32_t e0 = sc[c], e1 = sc[C::BW + c];  // E8M0 of K rows 0-31, 32-63
+          decode_kmajor_mxfp8_half(w[0], w[1], __uint_as_float(e0 ? e0 << 23 : 0x00400000u), r);
+          decode_kmajor_mxfp8_half(w[2], w[3], __uint_as_float(e1 ? e1 << 23 : 0x00400000u), r + 16);
+        } else if constexpr (C::NV) {
+          const uint4 *cw = reinterpret_cast<const uint4 *>(st + mtx * C::CODE_BYTES + c * C::ROW_BYTES);
+          const uint4 w0 = cw[0], w1 = cw[1];
           // scale rows 0..3 (16 K rows each) at sc + 128 row: column c's byte
           decode_kmajor_nvfp4_half(w0, uint32_t(sc[c]) | (uint32_t(sc[C::BW + c]) << 8), r);
           decode_kmajor_nvfp4_half(w1, uint32_t(sc[2 * C::BW + c]) | (uint32_t(sc[3 * C::BW + c]) << 8),
                                    r + 16);
         } else {
+          const uint4 *cw = reinterpret_cast<const uint4 *>(st + mtx * C::CODE_BYTES + c * C::ROW_BYTES);
+          const uint4 w0 = cw[0], w1 = cw[1];
           const uint32_t sbits = *reinterpret_cast<const uint16_t *>(sc + c * 2);
           decode_kmajor_int4_half(w0, sbits, r);
           decode_kmajor_int4_half(w1, sbits, r + 16);

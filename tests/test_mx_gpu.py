@@ -68,6 +68,57 @@ def test_mx_7b_shape_sampled(sg, fmt, M):
     _run(sg, fmt, M, N, K, seed=2, rows=si.sample_rows(M, 128, 32, seed=2))
 
 
+# ---- MXFP8 codes K-major ([N, K], the transpose), decoded into tensor memory ----------------
+
+def _run_mxfp8_kmajor(sg, M, N, K, seed, rows=None):
+    A, w1, w2 = si.make_mx(M, N, K, seed, "mxfp8")
+    C1k = w1[0].t().contiguous().to(DEV)
+    C2k = w2[0].t().contiguous().to(DEV)
+    Y = sg.swiglu_fused_mxfp8_kmajor(A.to(DEV), C1k, w1[1].to(DEV), C2k, w2[1].to(DEV))
+    rc, detail = sg.swiglu_device_status()
+    assert rc == sg.OK, (sg.status_string(rc), detail)
+    o1, o2 = (w1[0].numpy(), w1[1].numpy()), (w2[0].numpy(), w2[1].numpy())
+    ref = oracle.swiglu_mx(si.bits_u16(A), "mxfp8", o1, o2, rows=rows)
+    got = Y.double().cpu().numpy()
+    if rows is not None:
+        got = got[rows]
+    oracle.assert_parity(got, ref, f"mxfp8 k-major {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("shape", [(1, 64, 64), (7, 96, 128), (63, 288, 384), (64, 4864, 896),
+                                   (65, 4896, 896), (128, 1152, 448),
+                                   # several 128-token passes, the last one ragged
+                                   (300, 640, 256), (129, 256, 128),
+                                   # ragged last column block (9760 = 76 x 128 + 32)
+                                   (100, 9760, 256)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_mxfp8_kmajor_shapes(sg, shape):
+    M, N, K = shape
+    _run_mxfp8_kmajor(sg, M, N, K, seed=7 * M + N + K)
+
+
+@pytest.mark.parametrize("M", [64, 128])
+def test_mxfp8_kmajor_7b_shape_sampled(sg, M):
+    N, K = 18944, 3584
+    _run_mxfp8_kmajor(sg, M, N, K, seed=8, rows=si.sample_rows(M, 64, 24, seed=8))
+
+
+def test_mxfp8_kmajor_argument_errors(sg):
+    lib = sg.lib()
+    A = torch.zeros(4, 128, dtype=torch.bfloat16, device=DEV)
+    Ck = torch.zeros(64, 128, dtype=torch.uint8, device=DEV)
+    S = torch.zeros(4, 64, dtype=torch.uint8, device=DEV)
+    Y = torch.empty(4, 64, dtype=torch.bfloat16, device=DEV)
+    p = [t.data_ptr() for t in (A, Ck, S, Ck, S, Y)]
+    f = lib.swiglu_fused_mxfp8_kmajor
+    assert f(*p, 4, 64, 96, None) == sg.ERR_UNSUPPORTED                        # K not a multiple of 64
+    assert f(*p, 4, 48, 128, None) == sg.ERR_MISALIGNED                        # N not a multiple of 32
+    assert f(*p[:5], A.data_ptr(), 4, 64, 128, None) == sg.ERR_INVALID_ARG     # Y overlaps A
+    assert f(p[0], None, *p[2:], 4, 64, 128, None) == sg.ERR_INVALID_ARG       # missing codes
+    assert f(*p, 0, 64, 128, None) == sg.OK
+    torch.cuda.synchronize()
+
+
 # ---- NVFP4 codes in the K-major layout, decoded into tensor memory --------------------------
 
 def _run_nvfp4_kmajor(sg, M, N, K, seed, rows=None):
