@@ -1,10 +1,12 @@
-// swiglu_dqt_kernel.cuh -- INT4 weights decoded into tensor memory, with the
-// weights on the MMA's M side and the tokens on its N side.
+// swiglu_dqt_kernel.cuh -- INT4, NVFP4 and MXFP8 weights decoded into tensor
+// memory, with the weights on the MMA's M side and the tokens on its N side.
 //
 // Same result as swiglu_fused_w4 (page "Riepilogo Tecnico: Sovrapposizione
 // delle Attivazioni a Livello di Tile per l'Inferenza Efficiente di LLM",
 // section "Definizione del Problema": INT4 raises tensor-core density; the
-// weights are BF16(q * s)), computed as the transposed product
+// weights are BF16(q * s)), or as swiglu_fused_nvfp4 / swiglu_fused_mxfp8 (the
+// formats the GEMM page's benchmark paragraph names), computed as the
+// transposed product
 //     Y^T[n, t] = SiLU(sum_k W1[k, n] A[t, k]) * (sum_k W2[k, n] A[t, k]).
 // For few tokens the call is a stream of 4-bit codes, and the cost of the
 // shared-memory decode kernels is the decode's round trip: every K step they
@@ -17,7 +19,8 @@
 //     codes contiguous, eight per 32-bit word ordered k0 k2 k4 k6 k1 k3 k5 k7
 //     from the low nibble), so one shift and one logic operation give a
 //     column's BF16 pair (k, k + 1) -- exactly one 32-bit TMEM column of the A
-//     operand (row = TMEM lane, two K values per column);
+//     operand (row = TMEM lane, two K values per column); MXFP8 codes are
+//     bytes, [N, K], two adjacent bytes giving the pair;
 //   * sixteen decoding warps: warp w owns TMEM lanes [32 (w % 4), +32) (thread
 //     = weight column), decodes W1 (bit 2 of w clear) or W2, and every other
 //     K step (bit 3: the step's parity), all 64 K values of it, stored with
