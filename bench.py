@@ -242,6 +242,28 @@ def roofline_entry(flops: float, nbytes: float, us: float, peak_tflops: float, p
             "frac_of_roofline": max(t_tc, t_hbm) / (us * 1e-6)}
 
 
+def describe_workload(name: str) -> str:
+    """The config.workload text of a workload, the same for both arms."""
+    K, N, Ms, seed = WORKLOADS[name]
+    if name.endswith("-mlp"):
+        return (f"{name} SwiGLU MLP block H={K} F={N} M={list(Ms)} "
+                f"(fused gate/up projection + down projection), seed {seed}")
+    if name.endswith("-fp8-rmsnorm"):
+        return (f"{name} FP8 projection K={K} N={N} M={list(Ms)} fed by its producer (RMSNorm "
+                f"of X, eps {RMS_EPS}, per-tensor E4M3 quantisation), separate and interleaved "
+                f"weights, seed {seed}")
+    if name.endswith("-w4"):
+        return (f"{name} MLP projection K={K} N={N} M={list(Ms)} with INT4 weights (group "
+                f"{W4_GROUP}, BF16 scales) as [K, N/2] codes and K-major, BF16 A and Y, seed {seed}")
+    if name.endswith(("-mxfp8", "-nvfp4")):
+        fmt = name.rsplit("-", 1)[1]
+        codes = "[K, N]" if fmt == "mxfp8" else "[K, N/2]"
+        return (f"{name} MLP projection K={K} N={N} M={list(Ms)} with {fmt.upper()} weights as "
+                f"{codes} codes and K-major, BF16 A and Y, seed {seed}")
+    return (f"{name} MLP projection K={K} N={N} M={list(Ms)}, separate and interleaved weights, "
+            f"seed {seed}")
+
+
 # ----------------------------------------------------------------------------- our arm
 
 class Workload:
@@ -687,21 +709,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic",
         "impl": "ours",
         "config": {
-            "workload": (f"{wl.name} SwiGLU MLP block H={wl.K} F={wl.N} M={list(wl.Ms)} "
-                         f"(fused gate/up projection + down projection), seed {wl.seed}"
-                         if wl.kind == "mlp" else
-                         f"{wl.name} FP8 projection K={wl.K} N={wl.N} M={list(wl.Ms)} fed by its "
-                         f"producer (RMSNorm of X, eps {RMS_EPS}, per-tensor E4M3 quantisation), "
-                         f"separate and interleaved weights, seed {wl.seed}"
-                         if wl.producer else
-                         f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)} with INT4 "
-                         f"weights (group {W4_GROUP}, BF16 scales), BF16 A and Y, seed {wl.seed}"
-                         if wl.kind == "w4" else
-                         f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)} with "
-                         f"{wl.mxfmt.upper()} weights, BF16 A and Y, seed {wl.seed}"
-                         if wl.kind == "mx" else
-                         f"{wl.name} MLP projection K={wl.K} N={wl.N} M={list(wl.Ms)}, "
-                         f"separate and interleaved weights, seed {wl.seed}"),
+            "workload": describe_workload(wl.name),
             "calls_per_step": n_calls,
             "l2": f"inputs larger than L2: each call has its own A, weights and Y; "
                   f"{wl.bytes_touched / 2**20:.0f} MiB per step vs {L2_BYTES / 2**20:.0f} MiB L2",
@@ -1087,14 +1095,12 @@ def run_reference(args, ws, rank):
     tot_flops = sum(v * s for v, s in vals)
     tot_s = sum(s for _, s in vals)
     value = tot_flops / tot_s
-    K, N, Ms, seed = WORKLOADS[args.workload]
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / max(1, len(vals)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{args.workload} MLP projection K={K} N={N} M={list(Ms)}, "
-                               f"separate and interleaved weights, seed {seed}",
+        "config": {"workload": describe_workload(args.workload),
                    "sample": "each step is a bounded row sample; see cpu_baseline"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
