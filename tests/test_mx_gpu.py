@@ -116,7 +116,10 @@ def test_mxfp8_kmajor_argument_errors(sg):
     assert f(*p[:5], A.data_ptr(), 4, 64, 128, None) == sg.ERR_INVALID_ARG     # Y overlaps A
     assert f(p[0], None, *p[2:], 4, 64, 128, None) == sg.ERR_INVALID_ARG       # missing codes
     assert f(*p, 0, 64, 128, None) == sg.OK
+    Y.fill_(3.0)                                                               # K = 0: Y = 0
+    assert f(*p, 4, 64, 0, None) == sg.OK
     torch.cuda.synchronize()
+    assert torch.all(Y == 0)
 
 
 # ---- NVFP4 codes in the K-major layout, decoded into tensor memory --------------------------
@@ -174,7 +177,10 @@ def test_nvfp4_kmajor_argument_errors(sg):
     assert f(*p[:3], None, *p[4:], 4, 64, 128, None) == sg.ERR_INVALID_ARG     # missing tensor scale
     assert f(*p[:7], A.data_ptr(), 4, 64, 128, None) == sg.ERR_INVALID_ARG     # Y overlaps A
     assert f(*p, 0, 64, 128, None) == sg.OK
+    Y.fill_(3.0)                                                               # K = 0: Y = 0
+    assert f(*p, 4, 64, 0, None) == sg.OK
     torch.cuda.synchronize()
+    assert torch.all(Y == 0)
 
 
 def test_mx_argument_errors(sg):

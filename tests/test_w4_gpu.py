@@ -135,5 +135,9 @@ def test_w4_kmajor_argument_errors(sg):
     assert lib.swiglu_fused_w4_kmajor(*p, 4, 48, 128, 128, None) == sg.ERR_MISALIGNED
     assert lib.swiglu_fused_w4_kmajor(p[0], p[1], p[2], p[3], p[4], p[0], 4, 64, 128, 128, None) == sg.ERR_INVALID_ARG
     assert lib.swiglu_fused_w4_kmajor(*p, 0, 64, 128, 128, None) == sg.OK
+    Y.fill_(3.0)                                                               # K = 0: Y = 0
+    assert lib.swiglu_fused_w4_kmajor(*p, 4, 64, 0, 128, None) == sg.OK
+    torch.cuda.synchronize()
+    assert torch.all(Y == 0)
     assert lib.swiglu_pack_w4_kmajor(p[1], p[1], 128, 64, None) == sg.ERR_INVALID_ARG  # overlap
     assert lib.swiglu_pack_w4_kmajor(p[1], Y.data_ptr(), 12, 64, None) == sg.ERR_MISALIGNED
