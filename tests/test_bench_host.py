@@ -99,6 +99,20 @@ def test_reference_arm_rank0_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 2
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
+    # the same workload text as the library's arm prints for this workload
+    assert d["config"]["workload"] == bench.describe_workload("qwen2.5-0.5b-m64")
+
+
+def test_workload_descriptions_name_every_timed_form():
+    for name, (K, N, Ms, seed) in bench.WORKLOADS.items():
+        text = bench.describe_workload(name)
+        assert text.startswith(name)
+        assert f"K={K}" in text or f"H={K}" in text
+        assert f"seed {seed}" in text and str(list(Ms)) in text
+        if name.endswith(("-w4", "-mxfp8", "-nvfp4")):
+            assert "K-major" in text
+        elif not name.endswith("-mlp"):
+            assert "interleaved" in text
 
 
 def test_reference_arm_many_steps_sample_one_call_each():
